@@ -1,0 +1,360 @@
+"""Benchmark: KDA prefill Mtok/s and decode tok/s on GB300, with roofline fractions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step of the headline is one kda_chunk_fwd over the single-sequence prefill
+workload (B=1, H=96, T=8192, dk=dv=128, bf16 inputs, fp32 state carried in and
+out, chunk 64).  Inputs are resident in HBM before timing and are larger than
+L2, so no flush is needed between steps.  The same run times the decode
+workload (256 sequences x 96 heads, 64 consecutive kda_decode_step calls) and
+reports it under "decode".  Under torchrun every rank runs its own replica
+(weak scaling; the only collective is the max-reduction of the timings).
+--impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill Mtok/s & decode tok/s (H=96,d=128); % of GB300 roofline"
+PREFILL = "prefill_T8192_H96_d128_bf16"
+DECODE = "decode_256seq_H96_d128_64steps"
+FALLBACK_HBM_GBS = 6800.0
+STATE_BYTES = 128 * 128 * 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def prefill_bytes(T, H, dk, dv, elt=2, n_states=1):
+    """Algorithmic bytes: read q, k, g (dk each), v (dv), beta once, write out
+    (dv) once, plus one fp32 state read and one written per (sequence, head)."""
+    per_token_head = elt * (3 * dk + dv + 1 + dv)
+    return T * H * per_token_head + n_states * H * 2 * dk * dv * 4
+
+
+def decode_bytes(N, H, dk, dv, elt=2):
+    return N * H * (2 * dk * dv * 4 + elt * (3 * dk + dv + 1 + dv))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, a in enumerate(r[3]) if a == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def kernel_traffic(kernel_file, profile_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (its sha256 is recorded in the summary)."""
+    src = os.path.join(ROOT, "hybrid_linear_attention_02_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        text = open(prof).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The fp64 CPU oracle timed on the host cores on a bounded sample."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from hybrid_linear_attention_02_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL]
+    sample_T = 1024
+    d = inputs.make_prefill(w, seed=0, device="cpu", seq_len=sample_T)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    value = sample_T / per_step / 1e6
+    cores = oracle.prefill.last_threads
+    sample = f"all {w.heads} heads x first {sample_T} tokens of the workload per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL, "B": 1, "H": w.heads, "T": w.seq_len, "dk": w.dk,
+                   "dv": w.dv, "chunk": w.chunk},
+        "cpu_baseline": {"value": value, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "Mtok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_gpu(args):
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm_peak, peak_src = peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---------------- prefill (headline) ----------------
+    w = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_prefill(w, seed=rank, device=dev)
+    T, H = w.seq_len, w.heads
+    out = torch.empty((T, H, w.dv), dtype=w.torch_dtype, device=dev)
+    fin = torch.empty((1, H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    args_pf = [d[n] for n in ("q", "k", "v", "g", "beta")]
+
+    def prefill_step():
+        kda.chunk_fwd(*args_pf, d["init_state"], None, chunk=w.chunk, out=out,
+                      final_state=fin)
+
+    for _ in range(max(args.warmup, 3)):
+        prefill_step()
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        prefill_step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    barrier()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+    ms_total = max_over_ranks(start.elapsed_time(end))
+    ms_step = ms_total / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    value = world * T / (ms_step * 1e-3) / 1e6
+    alg_bytes = prefill_bytes(T, H, w.dk, w.dv)
+    achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+    tc = kda.algorithm(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk) == "tcgen05"
+    traffic = kernel_traffic("kda_chunk_tc.cu" if tc else "kda_recurrent.cu",
+                             "chunk_fwd_prefill_T8192_H96.md")
+
+    # ---------------- e2e through the public API with host buffers ----------------
+    host_in = [x.cpu().pin_memory() for x in args_pf + [d["init_state"]]]
+    dev_in = [torch.empty_like(x) for x in args_pf + [d["init_state"]]]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * host_fin.element_size()
+
+    def e2e_step():
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        kda.chunk_fwd(*dev_in[:5], dev_in[5], None, chunk=w.chunk, out=out, final_state=fin)
+        host_out.copy_(out, non_blocking=True)
+        host_fin.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e2e_steps = max(1, min(args.steps, 20))
+    start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    end.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(start.elapsed_time(end)) / e2e_steps
+    e2e_value = world * T / (e2e_ms * 1e-3) / 1e6
+    del host_in, dev_in, host_out, host_fin, d, args_pf, out, fin
+    torch.cuda.empty_cache()
+
+    # ---------------- decode ----------------
+    wd = inputs.WORKLOADS[DECODE]
+    N, Hd = wd.n_seqs, wd.heads
+    state = inputs.make_decode_state(wd, seed=rank, device=dev)
+    toks = [inputs.make_decode_tokens(wd, s, seed=rank, device=dev)
+            for s in range(wd.decode_steps)]
+    dout = torch.empty((N, Hd, wd.dv), dtype=wd.torch_dtype, device=dev)
+    for s in range(3):
+        kda.decode_step(*toks[s], state, out=dout)
+    barrier()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(wd.decode_steps)]
+    start.record(stream)
+    for s in range(wd.decode_steps):
+        dev_ev[s][0].record(stream)
+        kda.decode_step(*toks[s], state, out=dout)
+        dev_ev[s][1].record(stream)
+    end.record(stream)
+    barrier()
+    dec_ms = max_over_ranks(start.elapsed_time(end)) / wd.decode_steps
+    dec_kern_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = decode_bytes(N, Hd, wd.dk, wd.dv)
+    dec_gbs = dec_bytes / (dec_kern_ms * 1e-3) / 1e9
+
+    # ---------------- CPU baseline (oracle, rank 0, N=1 only) ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ws = inputs.WORKLOADS[PREFILL]
+        dc = inputs.make_prefill(ws, seed=0, device="cpu")
+        t0 = time.perf_counter()
+        oracle.prefill(*(dc[n] for n in ("q", "k", "v", "g", "beta")), dc["init_state"],
+                       dc["cu_seqlens"])
+        dt = time.perf_counter() - t0
+        cpu = {"value": ws.seq_len / dt / 1e6, "unit": "Mtok/s",
+               "cores": oracle.prefill.last_threads, "kind": "oracle",
+               "sample": f"the whole workload once (1 x {ws.seq_len} tokens x {ws.heads} heads),"
+                         f" fp64, {dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if tc else "f32", "data": "synthetic",
+            "config": {"workload": PREFILL, "B": 1, "H": H, "T": T, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "init_state": "N(0,0.02) fp32",
+                       "l2": f"inputs ({alg_bytes / 1e9:.2f} GB) larger than L2 (129 MB); "
+                             "no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                         "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic,
+                         "kernel": "kda_chunk_tc" if tc else "kda_recurrent",
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "kernel_ms": kern_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * 1,
+            "clocks": clocks,
+            "decode": {"workload": DECODE, "value": world * N / (dec_ms * 1e-3),
+                       "unit": "tok/s", "ms_per_step": dec_ms, "steps": wd.decode_steps,
+                       "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
+                                    "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+                                    "algorithmic_bytes_per_launch": dec_bytes,
+                                    "kernel": "kda_recurrent (one token)",
+                                    "kernel_ms": dec_kern_ms},
+                       "gpu_launches": wd.decode_steps},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+"""Kimi Delta Attention (KDA) on GB300: Python binding of libkda.so.
+
+The binding only marshals arguments: it checks tensor shapes, dtypes and
+devices, allocates outputs with PyTorch, and passes raw device pointers and the
+current CUDA stream to the C ABI declared in ``include/kda.h``.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.  If
+``libkda.so`` is missing or fails to load, every call raises.
+
+    out, final_state = chunk_fwd(q, k, v, g, beta, init_state, cu_seqlens, chunk=64)
+    out = decode_step(q, k, v, g, beta, state)          # state updated in place
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["chunk_fwd", "decode_step", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libkda.so"
+_lock = threading.Lock()
+_lib = None
+
+KDA_F32, KDA_BF16 = 0, 1
+_DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = load().kda_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("n_seqs", ctypes.c_int), ("total_tokens", ctypes.c_longlong),
+                ("heads", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+def lib_path() -> str:
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+def load():
+    """Load libkda.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} not found: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(path)
+            vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            dp = ctypes.POINTER(_Dims)
+            lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ip]
+            lib.kda_chunk_fwd_workspace_size.restype = sz
+            lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
+                                          vp]
+            lib.kda_chunk_fwd.restype = ip
+            lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, dp, vp, vp]
+            lib.kda_decode_step.restype = ip
+            lib.kda_status_string.argtypes = [ip]
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_version.restype = ip
+            lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
+            lib.kda_chunk_fwd_algorithm.restype = ip
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_input(name, t, shape, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(n_seqs, total_tokens, heads, dk, dv, dtype):
+    return _Dims(int(n_seqs), int(total_tokens), int(heads), int(dk), int(dv), _DTYPES[dtype])
+
+
+def workspace_size(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=64) -> int:
+    d = _dims(n_seqs, total_tokens, heads, dk, dv, dtype)
+    return int(load().kda_chunk_fwd_workspace_size(ctypes.byref(d), int(chunk)))
+
+
+def algorithm(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=64) -> str:
+    """Name of the kernel kda_chunk_fwd dispatches to for these sizes."""
+    d = _dims(n_seqs, total_tokens, heads, dk, dv, dtype)
+    rc = int(load().kda_chunk_fwd_algorithm(ctypes.byref(d), int(chunk)))
+    if rc < 0:
+        raise KDAError(rc, "kda_chunk_fwd_algorithm")
+    return {0: "recurrent", 1: "tcgen05"}[rc]
+
+
+def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 64, *,
+              n_seqs: int | None = None, out=None, final_state=None,
+              output_final_state: bool = True, workspace=None, dev_status=None, stream=None):
+    """Chunkwise KDA prefill over packed sequences (``kda_chunk_fwd``).
+
+    q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H] (fp32 or bf16, one dtype,
+    on one CUDA device).  init_state: [N, H, dk, dv] fp32 or None (zeros).
+    cu_seqlens: int32 [N+1] on the device, or None for ``n_seqs`` (default 1)
+    equal-length sequences.  Returns (out [T, H, dv], final_state or None).
+    """
+    lib = load()
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, dk]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported dtype {dt}")
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
+                         ("v", v, (T, H, dv)), ("beta", beta, (T, H))):
+        _check_input(name, t, shp, dt, dev)
+    if cu_seqlens is not None:
+        _check_input("cu_seqlens", cu_seqlens, (cu_seqlens.numel(),), torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if n_seqs is None else int(n_seqs)
+    if init_state is not None:
+        _check_input("init_state", init_state, (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    else:
+        _check_input("out", out, (T, H, dv), dt, dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _check_input("final_state", final_state, (N, H, dk, dv), torch.float32, dev)
+    d = _dims(N, T, H, dk, dv, dt)
+    need = int(lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), int(chunk)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                               _ptr(cu_seqlens), _ptr(out), _ptr(final_state), int(chunk),
+                               ctypes.byref(d), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                               _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_chunk_fwd")
+    return out, final_state
+
+
+def decode_step(q, k, v, g, beta, state, *, out=None, dev_status=None, stream=None):
+    """One KDA decode step (``kda_decode_step``): q, k, g [N, H, dk], v [N, H, dv],
+    beta [N, H]; state [N, H, dk, dv] fp32 is updated in place.  Returns out."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported dtype {dt}")
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
+                         ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
+        _check_input(name, t, shp, dt, dev)
+    _check_input("state", state, (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=dt, device=dev)
+    else:
+        _check_input("out", out, (N, H, dv), dt, dev)
+    d = _dims(N, N, H, dk, dv, dt)
+    with torch.cuda.device(dev):
+        rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                 _ptr(out), ctypes.byref(d), _ptr(dev_status),
+                                 _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_decode_step")
+    return out

@@ -1,0 +1,156 @@
+// C ABI of libkda.so: argument validation and dispatch.  Every check here
+// runs on the host before any CUDA call, so an invalid call returns without
+// touching the device.
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+using kda::LaunchArgs;
+
+constexpr size_t kWorkspaceAlign = 256;
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+
+size_t order_bytes(int n_seqs) {
+  if (n_seqs <= 1) return 0;
+  const size_t b = sizeof(int) * static_cast<size_t>(n_seqs);
+  return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+}
+
+// Shared shape checks for prefill and decode.
+int check_dims(const kda_dims* d) {
+  if (!d) return KDA_ERR_INVALID;
+  if (d->n_seqs < 0 || d->heads < 0 || d->total_tokens < 0 || d->dk <= 0 || d->dv <= 0)
+    return KDA_ERR_INVALID;
+  if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(d->dk) || !supported_head_dim(d->dv)) return KDA_ERR_UNSUPPORTED;
+  if (d->heads > 65535 && d->n_seqs > 0) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+int check_io_pointers(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const void* out, const kda_dims* d) {
+  if (d->total_tokens == 0 || d->heads == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !out) return KDA_ERR_INVALID;
+  // Vector loads and stores need 16-byte rows; rows are dk/dv elements long.
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+      !aligned(out, 16))
+    return KDA_ERR_ALIGNMENT;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 10000; }
+
+const char* kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported dims, dtype or chunk size";
+    case KDA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case KDA_ERR_TIMEOUT: return "device wait timed out";
+    case KDA_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk) {
+  (void)chunk;
+  if (check_dims(dims) != KDA_OK) return 0;
+  return order_bytes(dims->n_seqs);
+}
+
+int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk) {
+  const int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+  LaunchArgs a{};
+  a.n_seqs = dims->n_seqs; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
+  a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
+  return kda::chunk_tc_supported(a) ? KDA_ALGO_TCGEN05 : KDA_ALGO_RECURRENT;
+}
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                  const float* init_state, const int* cu_seqlens, void* out, float* final_state,
+                  int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                  int* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+  rc = check_io_pointers(q, k, v, g, beta, out, dims);
+  if (rc != KDA_OK) return rc;
+  const int N = dims->n_seqs;
+  if (N == 0 || dims->heads == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
+  long long seq_len = 0;
+  if (!cu_seqlens) {
+    if (dims->total_tokens % N != 0) return KDA_ERR_INVALID;
+    seq_len = dims->total_tokens / N;
+  }
+  if ((init_state && !aligned(init_state, 16)) || (final_state && !aligned(final_state, 16)))
+    return KDA_ERR_ALIGNMENT;
+  const size_t need = order_bytes(N);
+  if (need > 0 && cu_seqlens && (!workspace || workspace_bytes < need))
+    return KDA_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, kWorkspaceAlign)) return KDA_ERR_ALIGNMENT;
+
+  LaunchArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.init_state = init_state;
+  a.final_state = final_state;
+  a.cu_seqlens = cu_seqlens;
+  a.seq_len = seq_len;
+  a.out = out;
+  a.order = nullptr;
+  a.dev_status = dev_status;
+  a.n_seqs = N; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
+  a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (need > 0 && cu_seqlens) {
+    int* order = static_cast<int*>(workspace);
+    if (kda::launch_length_order(cu_seqlens, N, order, s) != cudaSuccess) return KDA_ERR_CUDA;
+    a.order = order;
+  }
+  cudaError_t e;
+  if (kda::chunk_tc_supported(a))
+    e = kda::launch_chunk_tc(a, s);
+  else
+    e = kda::launch_recurrent(a, s);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                    float* state, void* out, const kda_dims* dims, int* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (dims->total_tokens != dims->n_seqs) return KDA_ERR_INVALID;
+  if (dims->n_seqs == 0 || dims->heads == 0) return KDA_OK;
+  rc = check_io_pointers(q, k, v, g, beta, out, dims);
+  if (rc != KDA_OK) return rc;
+  if (!state) return KDA_ERR_INVALID;
+  if (!aligned(state, 16)) return KDA_ERR_ALIGNMENT;
+  LaunchArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.init_state = state;
+  a.final_state = state;
+  a.cu_seqlens = nullptr;
+  a.seq_len = 1;
+  a.out = out;
+  a.order = nullptr;
+  a.dev_status = dev_status;
+  a.n_seqs = dims->n_seqs; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
+  a.dtype = dims->dtype; a.chunk = 1; a.total_tokens = dims->total_tokens;
+  return kda::launch_recurrent(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// Internal declarations shared by the translation units of libkda.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Arguments of one prefill or decode launch, already validated on the host.
+struct LaunchArgs {
+  const void *q, *k, *v, *g, *beta;
+  const float* init_state;  // nullable: zeros
+  float* final_state;       // nullable
+  const int* cu_seqlens;    // nullable: equal lengths seq_len
+  long long seq_len;        // tokens per sequence when cu_seqlens is null
+  void* out;
+  const int* order;         // nullable: sequence processing order (longest first)
+  int* dev_status;          // nullable
+  int n_seqs, heads, dk, dv, dtype, chunk;
+  long long total_tokens;
+};
+
+// fp32 CUDA-core kernel that walks the recurrence token by token with the
+// state on chip.  Serves fp32 prefill, the shapes the tensor-core kernel does
+// not cover, and (with one token per sequence) the decode step.
+cudaError_t launch_recurrent(const LaunchArgs& a, cudaStream_t stream);
+
+// Writes order[0..N) = sequence indices by decreasing length (ties by index).
+cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,
+                                cudaStream_t stream);
+
+// bf16 chunkwise tcgen05/TMA kernel (dk = dv = 128, chunk = 64).
+bool chunk_tc_supported(const LaunchArgs& a);
+cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream);
+
+}  // namespace kda

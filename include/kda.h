@@ -1,0 +1,137 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) on one GB300 (sm_103a).
+ *
+ * The operation is the KDA recurrence of "[Paper Review] Kimi K3: Open Frontier
+ * Intelligence" (baba9811.github.io), section "Kimi Delta Attention (KDA)".
+ * Per sequence and head, with state S in R^{dk x dv}:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t,          alpha_t = exp(g_t) in (0, 1]^{dk}
+ *
+ * Diag(alpha_t) is the channel-wise forget gate applied to the prior state and
+ * (I - beta_t k_t k_t^T) erases the key direction before the new pair is
+ * written (same section).  The caller supplies g itself; the same section's
+ * lower-bounded decay g = g_min * sigmoid(.) with g_min = -5 makes g lie in
+ * [-5, 0], which is the precondition of the chunked tensor-core path.  There
+ * is no 1/sqrt(dk) output scale: q and k are L2-normalised upstream.
+ *
+ * Layouts (row-major, tokens packed back to back, all buffers on the device):
+ *   q, k, g     [T_total, H, dk]      v, out  [T_total, H, dv]
+ *   beta        [T_total, H]          states  [N, H, dk, dv]  fp32, dv fastest
+ * q, k, v, g, beta and out share one element type (kda_dtype); states are
+ * always fp32.
+ *
+ * Ownership: the caller owns every buffer.  The library keeps no pointer past
+ * the call and allocates no device memory; scratch comes from the caller's
+ * workspace.
+ * Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns without synchronising.
+ * Errors: argument errors are detected on the host and returned before any
+ * launch; launch failures return KDA_ERR_CUDA.  Errors found while kernels run
+ * (a bounded wait that expired) are written to the optional device word
+ * *dev_status (0 = fine), which the caller reads after synchronising.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID = -1,     /* null pointer, negative or inconsistent size      */
+  KDA_ERR_UNSUPPORTED = -2, /* well-formed but not implemented (dims, dtype)    */
+  KDA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed     */
+  KDA_ERR_TIMEOUT = -4,     /* device: a bounded wait expired (via dev_status)  */
+  KDA_ERR_ALIGNMENT = -5,   /* a buffer is not 16-byte aligned where required   */
+  KDA_ERR_WORKSPACE = -6    /* workspace missing or smaller than required       */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef struct {
+  int n_seqs;              /* N: sequences (prefill) or concurrent streams (decode) */
+  long long total_tokens;  /* T_total: packed tokens; decode: must equal n_seqs     */
+  int heads;               /* H                                                     */
+  int dk, dv;              /* key / value head dims: each 64 or 128                 */
+  int dtype;               /* kda_dtype of q, k, v, g, beta, out                    */
+} kda_dims;
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for these dims and chunk size
+ * (0 when none is needed).  Never fails; returns 0 for invalid dims.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
+
+/*
+ * Chunkwise prefill over packed variable-length sequences (the chunkwise
+ * parallel form the same section names; the page's 16-token tiles inside a
+ * chunk are what make it run on tensor cores).
+ *
+ *   q, k, v, g, beta  inputs, layouts above.
+ *   init_state        [N, H, dk, dv] fp32 state entering each sequence, or NULL
+ *                     for zeros.
+ *   cu_seqlens        device int32 [N + 1]: sequence n owns tokens
+ *                     [cu[n], cu[n+1]); cu[0] = 0, cu[N] = T_total, non-
+ *                     decreasing (empty sequences pass init_state through).
+ *                     NULL: N sequences of equal length T_total / N.
+ *   out               [T_total, H, dv] outputs o_t (same dtype as v).
+ *   final_state       [N, H, dk, dv] fp32 state after each sequence, or NULL.
+ *                     May alias init_state.
+ *   chunk             tokens per chunk: 16, 32 or 64.  Results agree across
+ *                     chunk sizes up to rounding.
+ *   workspace         device scratch of kda_chunk_fwd_workspace_size() bytes
+ *                     (256-byte aligned), or NULL when that size is 0.
+ *   dev_status        optional device int, set non-zero by a kernel whose
+ *                     bounded wait expired (KDA_ERR_TIMEOUT); never cleared.
+ *   stream            cudaStream_t to enqueue on.
+ * Paths: bf16 with dk = dv = 128 and chunk = 64 runs the tcgen05/TMA tensor-
+ * core kernel (requires q, k, v, g, out 16-byte aligned); every other
+ * supported case runs the fp32 CUDA-core kernel that walks the recurrence.
+ * Inputs with g outside [-5, 0] are outside the tensor-core path's contract.
+ */
+KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                  const float* init_state, const int* cu_seqlens, void* out, float* final_state,
+                  int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                  int* dev_status, void* stream);
+
+/*
+ * One recurrent decode step (the "dedicated kernels for KDA decode" of the
+ * section "Infrastructure: how to actually run trillion-scale"; the state is
+ * the fixed-size d_k x d_v cache object per head).  Every one of the N
+ * sequences advances by one token: q, k, g [N, H, dk], v [N, H, dv],
+ * beta [N, H].  `state` [N, H, dk, dv] fp32 is read and overwritten in place;
+ * out [N, H, dv] receives o.  dims->total_tokens must equal dims->n_seqs.
+ */
+KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                    float* state, void* out, const kda_dims* dims, int* dev_status, void* stream);
+
+typedef enum { KDA_ALGO_RECURRENT = 0, KDA_ALGO_TCGEN05 = 1 } kda_algo;
+
+/*
+ * Which kernel kda_chunk_fwd runs for these dims and chunk size: the chunked
+ * tcgen05 tensor-core kernel or the CUDA-core recurrence.  Returns a negative
+ * kda_status for dims kda_chunk_fwd would reject.
+ */
+KDA_API int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk);
+
+/* Static description of a status code (never NULL). */
+KDA_API const char* kda_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

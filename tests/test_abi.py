@@ -1,0 +1,96 @@
+"""The C ABI loads on a machine without a GPU, exports what include/kda.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_linear_attention_02_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return kda.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = _declared_symbols()
+    assert {"kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+            "kda_status_string", "kda_version"} <= syms
+    for s in sorted(syms):
+        assert hasattr(lib, s), f"{s} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.kda_status_string(code)
+    assert lib.kda_status_string(12345) == b"unknown status"
+    assert lib.kda_version() >= 10000
+
+
+def _dims(n=1, t=64, h=2, dk=128, dv=128, dtype=1):
+    return kda._Dims(n, t, h, dk, dv, dtype)
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def _prefill(lib, d, chunk=64, q=FAKE, cu=None, ws=None, ws_bytes=0):
+    return lib.kda_chunk_fwd(q, FAKE, FAKE, FAKE, FAKE, None, cu, FAKE, None, chunk,
+                             ctypes.byref(d), ws, ws_bytes, None, None)
+
+
+def test_host_validation_prefill(lib):
+    assert _prefill(lib, _dims(), chunk=48) == -2          # unsupported chunk
+    assert _prefill(lib, _dims(dk=96)) == -2               # unsupported head dim
+    assert _prefill(lib, _dims(dtype=7)) == -2             # unknown dtype
+    assert _prefill(lib, _dims(t=-1)) == -1                # negative size
+    assert _prefill(lib, _dims(), q=None) == -1            # null input
+    assert _prefill(lib, _dims(), q=MISALIGNED) == -5      # misaligned input
+    assert _prefill(lib, _dims(n=3, t=64)) == -1           # 64 tokens not divisible by 3
+    assert _prefill(lib, _dims(n=3, t=63), cu=FAKE) == -6  # varlen needs workspace
+    assert lib.kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, 64, None,
+                             None, 0, None, None) == -1    # null dims
+    # nothing to do: no tokens, no sequences
+    assert _prefill(lib, _dims(n=0, t=0)) == 0
+
+
+def test_host_validation_decode(lib):
+    d = _dims(n=4, t=5)
+    assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d),
+                               None, None) == -1           # total_tokens != n_seqs
+    d = _dims(n=4, t=4)
+    assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, ctypes.byref(d),
+                               None, None) == -1           # null state
+    assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, MISALIGNED, FAKE,
+                               ctypes.byref(d), None, None) == -5
+
+
+def test_workspace_size(lib):
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(n=1)), 64) == 0
+    ws = lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(n=32, t=1000)), 64)
+    assert ws >= 32 * 4 and ws % 256 == 0
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(dk=7)), 64) == 0
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 2, 128)
+    with pytest.raises(ValueError):
+        kda.chunk_fwd(x, x, x, x, torch.zeros(4, 2))

@@ -1,0 +1,123 @@
+"""Prefill (kda_chunk_fwd) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_02_gb300 as kda
+import oracle
+from hybrid_linear_attention_02_gb300 import inputs
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+W = inputs.WORKLOADS
+
+
+def _run(d, chunk=64):
+    out, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                             d["cu_seqlens"], chunk=chunk)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def _oracle(d, heads=None):
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    s0 = d["init_state"]
+    if heads is not None:
+        hs = torch.tensor(heads, device=x[0].device)
+        x = [t[:, hs] for t in x]
+        s0 = None if s0 is None else s0[:, hs]
+    return oracle.prefill(*x, s0, d["cu_seqlens"])
+
+
+def test_oracle_scale_fp32_config():
+    """B=1, H=1, T=256, dk=dv=64, fp32, zero state, chunk 64."""
+    w = W["prefill_T256_H1_d64_f32"]
+    d = inputs.make_prefill(w, seed=0, device=DEV)
+    out, fin = _run(d)
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "f32", "out")
+    assert_close(fin, rf, "f32", "final_state")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("lengths", [[300], [0, 1, 63, 64, 65, 129, 200]])
+def test_bf16_ragged_and_varlen(lengths, chunk):
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=1, device=DEV, lengths=lengths, heads=3)
+    out, fin = _run(d, chunk)
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "out")
+    assert_close(fin, rf, "bf16", "final_state")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128), (128, 128)])
+def test_fp32_head_dims(dk, dv):
+    w = inputs.Workload("f32_dims", heads=2, dk=dk, dv=dv, dtype="f32", init_state=True)
+    d = inputs.make_prefill(w, seed=2, device=DEV, lengths=[70, 0, 33])
+    out, fin = _run(d)
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "f32", "out")
+    assert_close(fin, rf, "f32", "final_state")
+
+
+def test_empty_sequence_passes_state_through():
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=3, device=DEV, lengths=[0, 5, 0], heads=2)
+    out, fin = _run(d)
+    assert torch.equal(fin[0], d["init_state"][0]) and torch.equal(fin[2], d["init_state"][2])
+
+
+def test_final_state_may_alias_init_state():
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=4, device=DEV, lengths=[90], heads=2)
+    ref_out, ref_fin = _run(d)
+    s = d["init_state"].clone()
+    out, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], s, d["cu_seqlens"],
+                             final_state=s)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(s, ref_fin)
+
+
+def test_deterministic():
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=5, device=DEV, lengths=[200, 77], heads=4)
+    o1, f1 = _run(d)
+    o2, f2 = _run(d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_prefill_8k_full_size():
+    """H=96, T=8192, bf16, random initial state: every head checked."""
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=0, device=DEV)
+    out, fin = _run(d)
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "out")
+    assert_close(fin, rf, "bf16", "final_state")
+
+
+def test_varlen_32seq_full_size_sampled():
+    """32 packed sequences (~270K tokens), H=96: all outputs computed on the
+    GPU, a sample of heads followed by the oracle over every sequence."""
+    w = W["varlen_32seq_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=0, device=DEV)
+    out, fin = _run(d)
+    heads = [0, 61]
+    ro, rf = _oracle(d, heads)
+    hs = torch.tensor(heads, device=DEV)
+    assert_close(out[:, hs], ro, "bf16", "out")
+    assert_close(fin[:, hs], rf, "bf16", "final_state")
+
+
+def test_prefill_1m_full_size_sampled():
+    """T = 1,048,576, H=32, saturated a in [-8, 8]: one head followed by the
+    oracle end to end (outputs and final state)."""
+    w = W["prefill_T1M_H32_d128_bf16"]
+    d = inputs.make_prefill(w, seed=0, device=DEV)
+    out, fin = _run(d)
+    heads = [13]
+    ro, rf = _oracle(d, heads)
+    hs = torch.tensor(heads, device=DEV)
+    assert_close(fin[:, hs], rf, "bf16", "final_state")
+    assert_close(out[:, hs], ro, "bf16", "out")
