@@ -197,6 +197,9 @@ def run_gpu(args):
     hbm_peak, peak_src = peaks()
     stream = torch.cuda.current_stream()
 
+    if args.only == "decode":
+        run_decode_only(args, dev)
+        return
     # ---------------- prefill (headline) ----------------
     w = inputs.WORKLOADS[PREFILL]
     d = inputs.make_prefill(w, seed=rank, device=dev)
@@ -266,6 +269,8 @@ def run_gpu(args):
     e2e_value = world * T / (e2e_ms * 1e-3) / 1e6
     del host_in, dev_in, host_out, host_fin, d, args_pf, out, fin
     torch.cuda.empty_cache()
+    if args.only == "prefill":
+        return
 
     # ---------------- decode ----------------
     wd = inputs.WORKLOADS[DECODE]
@@ -342,6 +347,22 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_decode_only(args, dev):
+    """Profiling aid: the decode kernel alone on N sequences x 96 heads."""
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    wd = inputs.WORKLOADS[DECODE]
+    N = args.decode_seqs or wd.n_seqs
+    state = inputs.make_decode_state(wd, seed=0, device=dev, n_seqs=N)
+    toks = [inputs.make_decode_tokens(wd, s, seed=0, device=dev, n_seqs=N)
+            for s in range(args.warmup + args.steps)]
+    for t in toks:
+        kda.decode_step(*t, state)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,6 +370,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="profiling aid: run one part only (no JSON line unless 'all')")
+    ap.add_argument("--decode-seqs", type=int, default=None,
+                    help="profiling aid: fewer decode sequences (small ncu case)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
