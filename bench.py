@@ -124,6 +124,22 @@ def kernel_traffic(kernel_file, profile_name):
     return float(m_tr.group(1))
 
 
+def reduce_max(x, device="cpu"):
+    """Max of a float over all ranks of the default process group (1 rank: x)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, max_ms):
+    """Whole-job units per second: every rank did the same work in <= max_ms."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -187,12 +203,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev)
 
     hbm_peak, peak_src = peaks()
     stream = torch.cuda.current_stream()
@@ -234,7 +245,7 @@ def run_gpu(args):
     ms_total = max_over_ranks(start.elapsed_time(end))
     ms_step = ms_total / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    value = world * T / (ms_step * 1e-3) / 1e6
+    value = job_throughput(world, T, ms_step) / 1e6
     alg_bytes = prefill_bytes(T, H, w.dk, w.dv)
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
     tc = kda.algorithm(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk) == "tcgen05"
@@ -266,7 +277,7 @@ def run_gpu(args):
     end.record(stream)
     barrier()
     e2e_ms = max_over_ranks(start.elapsed_time(end)) / e2e_steps
-    e2e_value = world * T / (e2e_ms * 1e-3) / 1e6
+    e2e_value = job_throughput(world, T, e2e_ms) / 1e6
     del host_in, dev_in, host_out, host_fin, d, args_pf, out, fin
     torch.cuda.empty_cache()
     if args.only == "prefill":
@@ -295,6 +306,7 @@ def run_gpu(args):
     dec_kern_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
     dec_bytes = decode_bytes(N, Hd, wd.dk, wd.dv)
     dec_gbs = dec_bytes / (dec_kern_ms * 1e-3) / 1e9
+    dec_traffic = kernel_traffic("kda_recurrent.cu", "decode_step_64x96.md")
 
     # ---------------- CPU baseline (oracle, rank 0, N=1 only) ----------------
     cpu = None
@@ -332,12 +344,13 @@ def run_gpu(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * 1,
             "clocks": clocks,
-            "decode": {"workload": DECODE, "value": world * N / (dec_ms * 1e-3),
+            "decode": {"workload": DECODE, "value": job_throughput(world, N, dec_ms),
                        "unit": "tok/s", "ms_per_step": dec_ms, "steps": wd.decode_steps,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
                                     "unit": "GB/s", "frac": dec_gbs / hbm_peak,
                                     "algorithmic_bytes_per_launch": dec_bytes,
                                     "kernel": "kda_recurrent (one token)",
+                                    "traffic": dec_traffic,
                                     "kernel_ms": dec_kern_ms},
                        "gpu_launches": wd.decode_steps},
         }
