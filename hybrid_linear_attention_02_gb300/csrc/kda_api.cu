@@ -58,6 +58,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_TIMEOUT: return "device wait timed out";
     case KDA_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_SCRATCH_LIMIT: return "more sequences than the no-alloc scratch array holds";
     default: return "unknown status";
   }
 }

@@ -53,7 +53,8 @@ typedef enum {
   KDA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed     */
   KDA_ERR_TIMEOUT = -4,     /* device: a bounded wait expired (via dev_status)  */
   KDA_ERR_ALIGNMENT = -5,   /* a buffer is not 16-byte aligned where required   */
-  KDA_ERR_WORKSPACE = -6    /* workspace missing or smaller than required       */
+  KDA_ERR_WORKSPACE = -6,   /* workspace missing or smaller than required       */
+  KDA_ERR_SCRATCH_LIMIT = -7 /* more sequences than kda_chunk_fwd_noalloc holds */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -114,6 +115,36 @@ KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const voi
  */
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
                     float* state, void* out, const kda_dims* dims, int* dev_status, void* stream);
+
+/*
+ * kda_chunk_fwd without a workspace, for callers that cannot allocate device
+ * memory: for example a plugin inside an inference engine that owns every
+ * device buffer and hands out only the tensors it planned, or a serving loop
+ * that must not call cudaMalloc because it synchronises the device and
+ * fragments a pool sized once at start-up.  The paper has no counterpart to
+ * this entry point; it exists for those callers only.
+ *
+ * Arguments, layouts, paths and results are those of kda_chunk_fwd.  The only
+ * scratch (the longest-first order of the packed sequences) lives in a fixed
+ * device array inside libkda.so that holds KDA_NOALLOC_MAX_SEQS entries
+ * (256 KiB); every GPU that loads the library keeps it until the process
+ * exits.  No call allocates or frees memory.
+ *   - More than KDA_NOALLOC_MAX_SEQS sequences: returns KDA_ERR_SCRATCH_LIMIT
+ *     before any launch.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and each call rewrites the entries it
+ *     uses before reading them, so nothing carries over between calls.  Calls
+ *     that overlap on the GPU (different streams, no ordering between them)
+ *     race on the array: order them on one stream or with events.
+ */
+#define KDA_NOALLOC_MAX_SEQS 65536
+KDA_API int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* init_state,
+                                  const int* cu_seqlens, void* out, float* final_state,
+                                  int chunk, const kda_dims* dims, int* dev_status,
+                                  void* stream);
 
 typedef enum { KDA_ALGO_RECURRENT = 0, KDA_ALGO_TCGEN05 = 1 } kda_algo;
 
