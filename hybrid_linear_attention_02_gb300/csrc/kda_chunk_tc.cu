@@ -9,23 +9,28 @@
 //   O  = (q e^G) S0 + lower_incl((q e^G)(k e^-G)^T) U
 //   S_C = Diag(e^{G_C}) S0 + (k e^{G_C - G})^T U
 // The same section's lower-bounded decay (g >= -5) keeps the cumulative
-// log-decay of a 16-token tile above -80, so the masked intra-chunk products
-// are formed per 16-token row tile a with the reference point R_a (the
-// cumulative decay where tile a starts): rows use k e^{G - R_a} <= 1 and keys
-// use k e^{R_a - G} < e^80, both inside the bf16/fp32 range.  Every product
-// is then a dense tensor-core MMA, which is the point of that section.
+// log-decay of a 16-token tile above -80.  The masked intra-chunk products
+// are therefore formed per 16-token row tile a with the reference point R_a
+// (the cumulative decay where tile a starts): rows use k e^{G - R_a} <= 1 and
+// keys use k e^{R_a - G} < e^80, both inside the bf16/fp32 range, and every
+// product is one dense tensor-core MMA.
 //
-// One CTA (256 threads) owns one (sequence, head) and walks its chunks in
-// order with the fp32 state in registers (thread j of each warpgroup holds
-// column j of S, half of the dk rows) and a bf16 copy of S^T in shared memory
-// as the MMA operand.  Every MMA is M = 128 (cta_group::1) with bf16 operands
-// and fp32 accumulators in TMEM:
-//   AP  [K';Q'] (128 x dk)  x  Khat blocks (160 x dk)^T     -> A and P rows
-//   W^T = Ktil^T (T')^T,   U0^T = V^T (T')^T                 (T' = T diag beta)
-//   U^T = U0^T + S^T (-W)^T,   O^T = S^T Qtil^T
-//   dS^T = U^T Kbar,   O^T += U^T P^T
-// T = (I + A)^-1 is solved on CUDA cores in fp32 (16 x 16 diagonal blocks by
-// forward substitution, then block merges).
+// One CTA (384 threads) owns one (sequence, head) and walks its chunks in
+// order.  The work of a chunk splits into a state-independent "prep" part and
+// the serial state pass, and the two run concurrently on different warps:
+//   prep  (warps 4..11) for chunk c+1:  cumulative decay, scaled operand tiles,
+//         AP = [K';Q'] x Khat^T (one M=128 N=160 K=128 MMA), A and P rows,
+//         T = (I + A)^-1 in fp32, W^T = Ktil^T T'^T and U0^T = V^T T'^T
+//         (T' = T diag(beta)), -W^T to shared memory.
+//   state (warps 0..3) for chunk c:  U^T = U0^T + S^T(-W)^T, O^T = S^T Qtil^T;
+//         S <- Diag(e^{G_C}) S (fp32, in TMEM);  U^T -> bf16 in TMEM;
+//         S^T += U^T Kbar, O^T += U^T P^T;  S^T -> bf16 in TMEM;  O -> out.
+// The fp32 state lives in tensor memory for the whole sequence (the MMA adds
+// dS onto the decayed state); its bf16 copy and U^T are A operands read from
+// tensor memory.  Every MMA is M = 128 (cta_group::1), bf16 x bf16 -> fp32.
+// Handoffs use mbarriers (a two-slot ring for the per-chunk tiles the state
+// pass consumes).  Every wait is bounded; on expiry the CTA stops issuing
+// work, reports KDA_ERR_TIMEOUT and exits.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -38,43 +43,49 @@ using namespace sm100;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 256;
+constexpr int kStateThreads = 128;                  // warps 0..3
+constexpr int kPrepThreads = 256;                   // warps 4..11
+constexpr int kThreads = kStateThreads + kPrepThreads;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared-memory tiles (byte offsets from a 1024-aligned base).  bf16 tiles
-// use the 128B-swizzled layout of sw128_off().
-constexpr uint32_t kOffKQ = 0;                 // [K'; Q']        128 x 128
-constexpr uint32_t kOffKH = kOffKQ + 32768;    // Khat blocks     160 x 128
-constexpr uint32_t kOffKT = kOffKH + 40960;    // Ktil = k e^G     64 x 128
-constexpr uint32_t kOffQT = kOffKT + 16384;    // Qtil = q e^G     64 x 128
-constexpr uint32_t kOffKB = kOffQT + 16384;    // Kbar             64 x 128
-constexpr uint32_t kOffV = kOffKB + 16384;     // V                64 x 128
-constexpr uint32_t kOffP = kOffV + 16384;      // P                64 x 64
-constexpr uint32_t kOffTB = kOffP + 8192;      // T diag(beta)     64 x 64
-constexpr uint32_t kOffWT = kOffTB + 8192;     // -W^T            128 x 64
-constexpr uint32_t kOffUT = kOffWT + 16384;    // U^T             128 x 64
-constexpr uint32_t kOffS = kOffUT + 16384;     // S^T (bf16)      128 x 128
-constexpr uint32_t kTileBytes = kOffS + 32768;
-// fp32 work matrices and the output staging reuse tiles that are dead then.
-constexpr int kLd = 65;                        // padded fp32 row length
-constexpr uint32_t kOffA = kOffKH;             // A  64 x 65 fp32
-constexpr uint32_t kOffT = kOffKH + 64 * kLd * 4;  // T 64 x 65 fp32
-constexpr uint32_t kOffX = kOffKQ;             // merge scratch 64 x 65 fp32
-constexpr uint32_t kOffO = kOffKQ;             // O staging 64 x 136 bf16
-constexpr int kLdO = 136;
+// Shared-memory tiles (byte offsets from a 1024-aligned base); bf16 tiles use
+// the 128B-swizzled layout of sw128_off().
+constexpr uint32_t kOffKQ = 0;                 // [K'_a; Q'_a] for a = 0..3   128 x 128
+constexpr uint32_t kOffKH = kOffKQ + 32768;    // Khat blocks                 160 x 128
+constexpr uint32_t kOffKT = kOffKH + 40960;    // Ktil = k e^G                 64 x 128
+constexpr uint32_t kOffV = kOffKT + 16384;     // V                            64 x 128
+constexpr uint32_t kOffTB = kOffV + 16384;     // T diag(beta)                 64 x 64
+constexpr uint32_t kOffQT = kOffTB + 8192;     // Qtil = q e^G, 2 slots        64 x 128
+constexpr uint32_t kOffKB = kOffQT + 32768;    // Kbar, 2 slots                64 x 128
+constexpr uint32_t kOffWT = kOffKB + 32768;    // -W^T                        128 x 64
+constexpr uint32_t kOffP = kOffWT + 16384;     // P, 2 slots                   64 x 64
+constexpr uint32_t kTileBytes = kOffP + 16384;
 constexpr uint32_t kSmemBytes = kTileBytes + 1024;
-static_assert(2 * 64 * kLd * 4 <= 40960, "A and T fit in the Khat tile");
-static_assert(64 * kLdO * 2 <= 32768, "O staging fits in the [K';Q'] tile");
+// fp32 work matrices of the inverse reuse the Khat tile once AP is done.
+constexpr int kLdA = 68;                                 // 16-byte aligned rows
+constexpr uint32_t kOffA = kOffKH;                       // A  64 x 68
+constexpr uint32_t kOffT = kOffA + 64 * kLdA * 4;        // T  64 x 68
+constexpr uint32_t kOffX = kOffT + 64 * kLdA * 4;        // X  3 x 16 x 20
+static_assert(kOffX + 3 * 16 * 20 * 4 <= kOffKH + 40960, "inverse scratch fits");
 
-// TMEM columns (fp32, lane = M row).
-constexpr uint32_t kColAP = 0;    // 160 columns
-constexpr uint32_t kColW = 0;     // 64, after AP is read
-constexpr uint32_t kColU = 64;    // 64
-constexpr uint32_t kColDS = 0;    // 128, after W and U are read
-constexpr uint32_t kColO = 160;   // 64
-constexpr uint32_t kTmemCols = 256;
+// TMEM columns (512 allocated).
+constexpr uint32_t kColAP = 0;     // 160 fp32: AP;  W^T reuses columns 0..63
+constexpr uint32_t kColW = 0;
+constexpr uint32_t kColU = 160;    // 64 fp32: U0^T, then U^T
+constexpr uint32_t kColO = 224;    // 64 fp32: O^T
+constexpr uint32_t kColS = 288;    // 128 fp32: S^T (lane j = value column, col = key row)
+constexpr uint32_t kColSB = 416;   // 64: bf16 S^T, A operand
+constexpr uint32_t kColUT = 480;   // 32: bf16 U^T, A operand
+constexpr uint32_t kTmemCols = 512;
 
-__device__ __forceinline__ int khat_block_row0(int a) { return 8 * a * (a + 1); }  // 0,16,48,96
+enum { kBarAP = 0, kBarWU, kBarFull0, kBarFull1, kBarEmpty0, kBarEmpty1, kBarMMA1, kBarUFree,
+       kBarMMA2, kNumBars };
+
+__device__ __forceinline__ int khat_row0(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ uint4 ldg16(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
@@ -94,34 +105,44 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
-}
-
 __device__ __forceinline__ void st_tile8(uint8_t* tile, int row, int col, int rows,
                                          const float (&f)[8]) {
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) = pack8(f);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
+      make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
-__device__ __forceinline__ void st_tile8_raw(uint8_t* tile, int row, int col, int rows, uint4 v) {
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) = v;
-}
+// Shared by all roles: a wait that also gives up once any thread has given up.
+struct Sync {
+  uint64_t* bars;
+  volatile int* abort;
+  __device__ __forceinline__ bool wait(int b, uint32_t parity) {
+    if (*abort) return false;
+    if (mbar_try_wait(&bars[b], parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(&bars[b], parity)) return true;
+      if ((it & 255u) == 0) {
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > 2000000000ull) {
+          *abort = 1;
+          return false;
+        }
+      }
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ float s_gamma[kD];
+  __shared__ __align__(16) float s_gamma[2][kD];     // e^{G_C} per channel, per slot
+  __shared__ __align__(16) float s_tile_tot[4][kD];  // per-tile sums of g (log2 units)
+  __shared__ __align__(16) float s_fac[4][3][kD];    // e^{R_{a+1+i} - R_a}, tile a
   __shared__ float s_beta[kC];
-  __shared__ uint64_t s_bar;
+  __shared__ uint64_t s_bars[kNumBars];
   __shared__ uint32_t s_tmem;
-
-  const __nv_bfloat16* __restrict__ gq = static_cast<const __nv_bfloat16*>(args.q);
-  const __nv_bfloat16* __restrict__ gk = static_cast<const __nv_bfloat16*>(args.k);
-  const __nv_bfloat16* __restrict__ gv = static_cast<const __nv_bfloat16*>(args.v);
-  const __nv_bfloat16* __restrict__ gg = static_cast<const __nv_bfloat16*>(args.g);
-  const __nv_bfloat16* __restrict__ gb = static_cast<const __nv_bfloat16*>(args.beta);
-  __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = args.heads;
@@ -135,410 +156,516 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
     t0 = static_cast<long long>(n) * args.seq_len;
     t1 = t0 + args.seq_len;
   }
+  const int n_chunks = static_cast<int>((t1 - t0 + kC - 1) / kC);
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&s_bar, 1);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&s_bars[b], 1);
+    s_abort = 0;
     fence_mbar_init();
   }
-
-  // State: thread (sj, sh) holds S[c][sj] for c in [64 sh, 64 sh + 64).
-  const int sj = tid & 127, sh = tid >> 7;
-  const long long soff = (static_cast<long long>(n) * H + h) * kD * kD;
-  float S[64];
-#pragma unroll
-  for (int i = 0; i < 64; ++i)
-    S[i] = args.init_state ? __ldcs(args.init_state + soff + (64 * sh + i) * kD + sj) : 0.f;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    float f[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) f[u] = S[8 * m + u];
-    st_tile8(smem + kOffS, sj, 64 * sh + 8 * m, 128, f);
-  }
-
-  // Prep layout: thread (cg, rg) owns channels [8 cg, 8 cg + 8) of rows
-  // [4 rg, 4 rg + 4); the 16 row groups of one channel group share a warp half.
-  const int cg = tid >> 4, rg = tid & 15, ta = rg >> 2;
-  const uint32_t kSeg = 0xFFFFFFFFu;
-
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s_tmem;
-  uint32_t phase = 0;
-  bool ok = true;
+  Sync sync{s_bars, &s_abort};
 
-  auto wait_mma = [&]() -> bool {
-    bool done = mbar_wait(&s_bar, phase);
-    phase ^= 1u;
-    done = __syncthreads_and(done) != 0;
-    tc_fence_after();
-    return done;
-  };
+  if (tid < kStateThreads) {
+    // =============================== state pass ===============================
+    const int j = tid;                                   // TMEM lane = value column
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const long long soff = (static_cast<long long>(n) * H + h) * kD * kD;
+    __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
 
-  // Raw inputs of the current chunk, prefetched one chunk ahead.
-  uint4 rq[4], rk[4], rgt[4], rv[4];
-  float rb[4];
-  auto load_chunk = [&](long long c0, int L) {
+    // S^T[j][c] = S[c][j]: fp32 copy and bf16 operand copy.
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t f[32], b[16];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int r = 4 * rg + m;
-      if (r < L) {
-        const long long off = ((c0 + r) * H + h) * kD + 8 * cg;
-        rq[m] = ldg16(gq + off);
-        rk[m] = ldg16(gk + off);
-        rgt[m] = ldg16(gg + off);
-        rv[m] = ldg16(gv + off);
-        rb[m] = cg == 0 ? __bfloat162float(gb[(c0 + r) * H + h]) : 0.f;
-      } else {
-        rq[m] = rk[m] = rgt[m] = rv[m] = make_uint4(0, 0, 0, 0);
-        rb[m] = 0.f;
-      }
+      for (int u = 0; u < 32; ++u)
+        f[u] = __float_as_uint(args.init_state ? __ldcs(args.init_state + soff +
+                                                        (32 * cb + u) * kD + j)
+                                               : 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        b[u] = pack2(__uint_as_float(f[2 * u]), __uint_as_float(f[2 * u + 1]));
+      tmem_st32(tbase + lane_base + kColS + 32 * cb, f);
+      tmem_st16(tbase + lane_base + kColSB + 16 * cb, b);
     }
-  };
+    tmem_st_wait();
+    tc_fence_before();
+    named_bar(1, kStateThreads);
 
-  const long long n_tok = t1 - t0;
-  if (n_tok > 0) load_chunk(t0, static_cast<int>(n_tok < kC ? n_tok : kC));
-
-  for (long long c0 = t0; c0 < t1 && ok; c0 += kC) {
-    const int L = static_cast<int>((t1 - c0) < kC ? (t1 - c0) : kC);
-
-    // ---- P1: cumulative log2-decay along the chunk, per channel.
-    float G[4][8];
-    {
-      float gf[8];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        unpack8(rgt[m], gf);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) G[m][j] = (m ? G[m - 1][j] : 0.f) + gf[j] * kLog2e;
-      }
-    }
-    float incl[8], R[4][8], Rta[8], GC[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) incl[j] = G[3][j];
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float y = __shfl_up_sync(kSeg, incl[j], o, 16);
-        if (rg >= o) incl[j] += y;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float excl = incl[j] - G[3][j];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) G[m][j] += excl;
-      R[0][j] = 0.f;
-      R[1][j] = __shfl_sync(kSeg, incl[j], 3, 16);
-      R[2][j] = __shfl_sync(kSeg, incl[j], 7, 16);
-      R[3][j] = __shfl_sync(kSeg, incl[j], 11, 16);
-      GC[j] = __shfl_sync(kSeg, incl[j], 15, 16);
-      const float rt = __shfl_sync(kSeg, incl[j], (4 * ta + 15) & 15, 16);
-      Rta[j] = ta ? rt : 0.f;  // reference of this thread's own row tile
-    }
-
-    // ---- P2: scaled operand tiles.
-    {
-      float eR[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) eR[j] = exp2f(Rta[j]);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int r = 4 * rg + m;
-        float kf[8], qf[8], t1v[8], t2v[8];
-        unpack8(rk[m], kf);
-        unpack8(rq[m], qf);
-        float e1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) e1[j] = exp2f(G[m][j] - Rta[j]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { t1v[j] = kf[j] * e1[j]; t2v[j] = qf[j] * e1[j]; }
-        st_tile8(smem + kOffKQ, r, 8 * cg, 128, t1v);
-        st_tile8(smem + kOffKQ, 64 + r, 8 * cg, 128, t2v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { t1v[j] *= eR[j]; t2v[j] *= eR[j]; }
-        st_tile8(smem + kOffKT, r, 8 * cg, 64, t1v);
-        st_tile8(smem + kOffQT, r, 8 * cg, 64, t2v);
-#pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2) {
-          if (a2 < ta) continue;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) t1v[j] = kf[j] * exp2f(R[a2][j] - G[m][j]);
-          st_tile8(smem + kOffKH, khat_block_row0(a2) + r, 8 * cg, 160, t1v);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) t1v[j] = kf[j] * exp2f(GC[j] - G[m][j]);
-        st_tile8(smem + kOffKB, r, 8 * cg, 64, t1v);
-        st_tile8_raw(smem + kOffV, r, 8 * cg, 64, rv[m]);
-        if (cg == 0) s_beta[r] = rb[m];
-      }
-      if (rg == 0) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s_gamma[8 * cg + j] = exp2f(GC[j]);
-      }
-    }
-    // Prefetch the next chunk's raw inputs (consumed at the top of the loop).
-    if (c0 + kC < t1) {
-      const long long rem = t1 - (c0 + kC);
-      load_chunk(c0 + kC, static_cast<int>(rem < kC ? rem : kC));
-    }
-    fence_async_smem();
-    __syncthreads();
-
-    // ---- P3: masked intra-chunk products on the tensor cores.
-    if (tid == 0) {
+#pragma unroll 1
+    for (int c = 0; c < n_chunks; ++c) {
+      const int s = c & 1;
+      const long long c0 = t0 + static_cast<long long>(c) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      const bool ok_full = sync.wait(kBarFull0 + s, (c >> 1) & 1);
       tc_fence_after();
-      const uint32_t idesc = umma_idesc_bf16(128, 160, 0, 0);
-      const uint32_t aK = smem_u32(smem + kOffKQ), bK = smem_u32(smem + kOffKH);
+      if (j == 0 && ok_full) {
+        // U^T += S^T (-W)^T ;  O^T = S^T Qtil^T      (K = dk = 128)
+        const uint32_t iU = umma_idesc_bf16(128, 64, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
+        const uint32_t bW = smem_u32(smem + kOffWT), bQ = smem_u32(smem + kOffQT + s * 16384);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint64_t ad = umma_desc(aK + (s >> 2) * 128 * 128 + (s & 3) * 32, 16, 1024);
-        const uint64_t bd = umma_desc(bK + (s >> 2) * 160 * 128 + (s & 3) * 32, 16, 1024);
-        umma_bf16(tbase + kColAP, ad, bd, idesc, s > 0);
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t aS = tbase + kColSB + 8 * t;
+          umma_bf16_tmem_a(tbase + kColU, aS, umma_desc(bW + t * 2048, 128 * 128, 1024), iU, 1);
+          umma_bf16_tmem_a(tbase + kColO, aS,
+                           umma_desc(bQ + (t >> 2) * 64 * 128 + (t & 3) * 32, 16, 1024), iO,
+                           t > 0);
+        }
+        umma_commit(&s_bars[kBarMMA1]);
       }
-      umma_commit(&s_bar);
+      // Decay the fp32 state in place: S <- Diag(e^{G_C}) S (MMA1 does not read it).
+      if (ok_full) {
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kColS + 32 * cb, v);
+          tmem_ld_wait();
+          uint32_t f[32];
+#pragma unroll
+          for (int u = 0; u < 32; u += 4) {
+            const float4 gm = *reinterpret_cast<const float4*>(&s_gamma[s][32 * cb + u]);
+            f[u] = __float_as_uint(v[u] * gm.x);
+            f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
+            f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
+            f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
+          }
+          tmem_st32(tbase + lane_base + kColS + 32 * cb, f);
+        }
+      }
+      const bool ok1 = sync.wait(kBarMMA1, c & 1);
+      tc_fence_after();
+      if (ok1) {
+        // U^T (fp32) -> bf16 A operand.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kColU + 32 * half, v);
+          tmem_ld_wait();
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          tmem_st16(tbase + lane_base + kColUT + 16 * half, b);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar(1, kStateThreads);
+      if (j == 0 && ok1 && !s_abort) {
+        mbar_arrive(&s_bars[kBarUFree]);
+        tc_fence_after();
+        // S^T += U^T Kbar (K = 64 tokens) ;  O^T += U^T P^T
+        const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
+        const uint32_t bK = smem_u32(smem + kOffKB + s * 16384),
+                       bP = smem_u32(smem + kOffP + s * 8192);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t aU = tbase + kColUT + 8 * t;
+          umma_bf16_tmem_a(tbase + kColS, aU, umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
+          umma_bf16_tmem_a(tbase + kColO, aU, umma_desc(bP + t * 32, 16, 1024), iO, 1);
+        }
+        umma_commit(&s_bars[kBarEmpty0 + s]);
+        umma_commit(&s_bars[kBarMMA2]);
+      }
+      const bool ok2 = sync.wait(kBarMMA2, c & 1);
+      tc_fence_after();
+      float o0[32], o1[32];
+      if (ok2) {
+        // New state -> bf16 operand copy; O^T -> registers.
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kColS + 32 * cb, v);
+          tmem_ld_wait();
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          tmem_st16(tbase + lane_base + kColSB + 16 * cb, b);
+        }
+        tmem_ld32(tbase + lane_base + kColO, o0);
+        tmem_ld32(tbase + lane_base + kColO + 32, o1);
+        tmem_ld_wait();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar(1, kStateThreads);
+      if (ok2) {
+        __nv_bfloat16* dst = gout + (c0 * H + h) * kD + j;
+        const long long rs = static_cast<long long>(H) * kD;
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (r < L) dst[r * rs] = __float2bfloat16_rn(o0[r]);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (32 + r < L) dst[(32 + r) * rs] = __float2bfloat16_rn(o1[r]);
+      }
     }
-    // Zero the P tile while the MMA runs (only in-block entries get written).
-    if (tid >= 128) {
-      uint4* p = reinterpret_cast<uint4*>(smem + kOffP);
-      for (int i = tid - 128; i < 8192 / 16; i += 128) p[i] = make_uint4(0, 0, 0, 0);
+    if (!s_abort && args.final_state) {
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+        tmem_ld32(tbase + lane_base + kColS + 32 * cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) __stcs(args.final_state + soff + (32 * cb + u) * kD + j, v[u]);
+      }
     }
-    if (!(ok = wait_mma())) break;
-
-    // ---- P4: read A (x beta, strictly lower) and P (lower inclusive).
+  } else {
+    // ================================== prep ==================================
+    const int p = tid - kStateThreads;          // 0..255
+    const int pw = p >> 5;                      // prep warp 0..7
+    const int ta = pw & 3;                      // this warp's 16-token row tile
+    const int cg = 8 * (pw >> 2) + (lane & 7);  // channel group: channels 8 cg .. 8 cg + 7
+    const int r4 = lane >> 3;                   // rows 16 ta + 4 r4 + m, m = 0..3
+    const int row0 = 16 * ta + 4 * r4;
+    const bool leader = p == 0;
+    const __nv_bfloat16* __restrict__ gq = static_cast<const __nv_bfloat16*>(args.q);
+    const __nv_bfloat16* __restrict__ gk = static_cast<const __nv_bfloat16*>(args.k);
+    const __nv_bfloat16* __restrict__ gv = static_cast<const __nv_bfloat16*>(args.v);
+    const __nv_bfloat16* __restrict__ gg = static_cast<const __nv_bfloat16*>(args.g);
+    const __nv_bfloat16* __restrict__ gb = static_cast<const __nv_bfloat16*>(args.beta);
     float* Am = reinterpret_cast<float*>(smem + kOffA);
     float* Tm = reinterpret_cast<float*>(smem + kOffT);
     float* Xm = reinterpret_cast<float*>(smem + kOffX);
-    if (warp < 4) {
-      const int row = tid;                 // TMEM lane
-      const bool isP = row >= 64;
-      const int r = row & 63, a = r >> 4;
-      const int a0 = ((32 * warp) & 63) >> 4;  // first row tile of this warp
-      const int lo = khat_block_row0(a0), hi = khat_block_row0(a0 + 1) + 16 * (a0 + 2);
-      const int mylo = khat_block_row0(a), myn = 16 * (a + 1);
-      const float br = s_beta[r];
-      for (int cb = lo; cb < hi; cb += 16) {
-        float v16[16];
-        tmem_ld16(tmem_addr(tbase, 32 * warp, kColAP + cb), v16);
-        tmem_ld_wait();
+
+    uint4 rq[4], rk[4], rgt[4], rv[4];
+    float rb[4];
+    auto load_chunk = [&](int c) {
+      const long long c0 = t0 + static_cast<long long>(c) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int i = cb + u - mylo;
-          if (i < 0 || i >= myn) continue;
-          if (!isP) {
-            Am[r * kLd + i] = i < r ? br * v16[u] : 0.f;
-          } else {
-            const __nv_bfloat16 pv = __float2bfloat16_rn(i <= r ? v16[u] : 0.f);
-            *reinterpret_cast<__nv_bfloat16*>(smem + kOffP + sw128_off(r, i, 64)) = pv;
+      for (int m = 0; m < 4; ++m) {
+        const int r = row0 + m;
+        if (r < L) {
+          const long long off = ((c0 + r) * H + h) * kD + 8 * cg;
+          rq[m] = ldg16(gq + off);
+          rk[m] = ldg16(gk + off);
+          rgt[m] = ldg16(gg + off);
+          rv[m] = ldg16(gv + off);
+          rb[m] = cg == 0 ? __bfloat162float(gb[(c0 + r) * H + h]) : 0.f;
+        } else {
+          rq[m] = rk[m] = rgt[m] = rv[m] = make_uint4(0, 0, 0, 0);
+          rb[m] = 0.f;
+        }
+      }
+    };
+    if (n_chunks > 0) load_chunk(0);
+
+#pragma unroll 1
+    for (int c = 0; c < n_chunks; ++c) {
+      const int s = c & 1;
+      // ---- P1: cumulative decay (log2 units) along the chunk, per channel.
+      float G[4][8];
+      {
+        float gf[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          unpack8(rgt[m], gf);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) G[m][u] = (m ? G[m - 1][u] : 0.f) + gf[u] * kLog2e;
+        }
+      }
+      // Scan the four 4-row groups of this tile (lanes 8 apart), then across tiles.
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float tot = G[3][u];
+        float y = __shfl_up_sync(0xFFFFFFFFu, tot, 8);
+        if (r4 >= 1) tot += y;
+        y = __shfl_up_sync(0xFFFFFFFFu, tot, 16);
+        if (r4 >= 2) tot += y;
+        const float excl = tot - G[3][u];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) G[m][u] += excl;
+        if (r4 == 3) s_tile_tot[ta][8 * cg + u] = tot;
+      }
+      // Slots of the per-chunk tiles the state pass reads: free once the
+      // state pass of chunk c - 2 has finished its last MMA.
+      const bool ok_e = c < 2 || sync.wait(kBarEmpty0 + s, ((c >> 1) - 1) & 1);
+      named_bar(2, kPrepThreads);
+      float R[4][8], GC[8];
+      {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) R[a][u] = acc[u];
+          const float4 t0v = *reinterpret_cast<const float4*>(&s_tile_tot[a][8 * cg]);
+          const float4 t1v = *reinterpret_cast<const float4*>(&s_tile_tot[a][8 * cg + 4]);
+          acc[0] += t0v.x; acc[1] += t0v.y; acc[2] += t0v.z; acc[3] += t0v.w;
+          acc[4] += t1v.x; acc[5] += t1v.y; acc[6] += t1v.z; acc[7] += t1v.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) GC[u] = acc[u];
+      }
+      float Ra[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        Ra[u] = ta == 0 ? R[0][u] : ta == 1 ? R[1][u] : ta == 2 ? R[2][u] : R[3][u];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) G[m][u] += Ra[u];
+      }
+
+      // ---- P2: scaled operand tiles.
+      {
+        uint8_t* qt = smem + kOffQT + s * 16384;
+        uint8_t* kb = smem + kOffKB + s * 16384;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int r = row0 + m;
+          *reinterpret_cast<uint4*>(smem + kOffV + sw128_off(r, 8 * cg, 64)) = rv[m];
+          if (cg == 0) s_beta[r] = rb[m];
+        }
+        float eR[8], eC[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          eR[u] = exp2f(Ra[u]);
+          eC[u] = exp2f(GC[u] - Ra[u]);
+        }
+        // Khat factors for the later key blocks, e^{R_{a2} - R_ta} <= 1, shared
+        // by the warp (all its lanes are in tile ta).
+        if (r4 == 0) {
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const int a2 = ta + 1 + i;
+            if (a2 < 4) {
+              float f8[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const float ra2 = a2 == 1 ? R[1][u] : a2 == 2 ? R[2][u] : R[3][u];
+                f8[u] = exp2f(ra2 - Ra[u]);
+              }
+              *reinterpret_cast<float4*>(&s_fac[ta][i][8 * cg]) =
+                  make_float4(f8[0], f8[1], f8[2], f8[3]);
+              *reinterpret_cast<float4*>(&s_fac[ta][i][8 * cg + 4]) =
+                  make_float4(f8[4], f8[5], f8[6], f8[7]);
+            }
+          }
+          if (ta == 0) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s_gamma[s][8 * cg + u] = exp2f(GC[u]);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int r = row0 + m, rl = 4 * r4 + m;
+          float kf[8], qf[8], x[8], y[8];
+          unpack8(rk[m], kf);
+          unpack8(rq[m], qf);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float e1 = exp2f(G[m][u] - Ra[u]);
+            x[u] = kf[u] * e1;
+            y[u] = qf[u] * e1;
+          }
+          st_tile8(smem + kOffKQ, 32 * ta + rl, 8 * cg, 128, x);
+          st_tile8(smem + kOffKQ, 32 * ta + 16 + rl, 8 * cg, 128, y);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) { x[u] *= eR[u]; y[u] *= eR[u]; }
+          if (ok_e) st_tile8(qt, r, 8 * cg, 64, y);
+          st_tile8(smem + kOffKT, r, 8 * cg, 64, x);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            x[u] = kf[u] * exp2f(Ra[u] - G[m][u]);
+            y[u] = x[u] * eC[u];
+          }
+          if (ok_e) st_tile8(kb, r, 8 * cg, 64, y);
+          st_tile8(smem + kOffKH, khat_row0(ta) + r, 8 * cg, 160, x);
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            if (ta + 1 + i < 4) {
+              const float4 f0 = *reinterpret_cast<const float4*>(&s_fac[ta][i][8 * cg]);
+              const float4 f1 = *reinterpret_cast<const float4*>(&s_fac[ta][i][8 * cg + 4]);
+              y[0] = x[0] * f0.x; y[1] = x[1] * f0.y; y[2] = x[2] * f0.z; y[3] = x[3] * f0.w;
+              y[4] = x[4] * f1.x; y[5] = x[5] * f1.y; y[6] = x[6] * f1.z; y[7] = x[7] * f1.w;
+              st_tile8(smem + kOffKH, khat_row0(ta + 1 + i) + r, 8 * cg, 160, y);
+            }
           }
         }
       }
-    }
-    tc_fence_before();
-    __syncthreads();
+      if (c + 1 < n_chunks) load_chunk(c + 1);
+      fence_async_smem();
+      named_bar(2, kPrepThreads);
 
-    // ---- P5: T = (I + A)^-1, fp32.
-    if (tid < 64) {
-      const int blk = tid >> 4, j = tid & 15;
-      const float* Ab = Am + 16 * blk * kLd + 16 * blk;
-      float x[16];
+      // ---- P3: every masked intra-chunk product in one MMA.
+      if (leader && !s_abort) {
+        tc_fence_after();
+        const uint32_t idesc = umma_idesc_bf16(128, 160, 0, 0);
+        const uint32_t aK = smem_u32(smem + kOffKQ), bK = smem_u32(smem + kOffKH);
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < rr; ++i) acc = fmaf(Ab[rr * kLd + i], x[i], acc);
-        x[rr] = rr == j ? 1.f : (rr < j ? 0.f : -acc);
+        for (int t = 0; t < 8; ++t)
+          umma_bf16(tbase + kColAP, umma_desc(aK + (t >> 2) * 128 * 128 + (t & 3) * 32, 16, 1024),
+                    umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
+        umma_commit(&s_bars[kBarAP]);
       }
+      const bool ok_ap = sync.wait(kBarAP, c & 1);
+      tc_fence_after();
+
+      // ---- P4: A (x beta, strictly lower; fp32) and P (lower inclusive; bf16).
+      if (pw < 4 && ok_ap) {
+        // TMEM lane quarter pw holds rows [K'_pw; Q'_pw].
+        const int a = pw, rl = lane & 15, r = 16 * a + rl;
+        const bool isP = lane >= 16;
+        const float br = s_beta[r];
+        uint8_t* ptile = smem + kOffP + s * 8192;
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * kLd + 16 * blk + j] = x[rr];
-    }
-    __syncthreads();
+        for (int blk = 0; blk < 4; ++blk) {
+          float v[16];
+          if (blk <= a) {
+            tmem_ld16(tbase + (static_cast<uint32_t>(32 * pw) << 16) + kColAP + khat_row0(a) +
+                          16 * blk,
+                      v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int i = 16 * blk + u;
+              v[u] = isP ? (i <= r ? v[u] : 0.f) : (i < r ? br * v[u] : 0.f);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = 0.f;
+          }
+          if (isP) {
+            if (ok_e) {
+#pragma unroll
+              for (int h8 = 0; h8 < 2; ++h8) {
+                float f8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
+                st_tile8(ptile, r, 16 * blk + 8 * h8, 64, f8);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(&Am[r * kLdA + 16 * blk + 4 * q4]) =
+                  make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar(2, kPrepThreads);
+
+      // ---- P5: T = (I + A)^-1 in fp32; T' = T diag(beta) as bf16.
+      if (p < 64) {
+        const int blk = p >> 4, jj = p & 15;
+        const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
+        float x[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < rr; ++i) acc = fmaf(Ab[rr * kLdA + i], x[i], acc);
+          x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -acc);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * kLdA + 16 * blk + jj] = x[rr];
+      }
+      named_bar(2, kPrepThreads);
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int nel = (4 - d) * 256;
-      for (int e = tid; e < nel; e += kThreads) {
-        const int b = e >> 8, a = b + d, rr = (e >> 4) & 15, cc = e & 15;
-        float acc = 0.f;
-        for (int c = b; c < a; ++c) {
-          const float* arow = Am + (16 * a + rr) * kLd + 16 * c;
-          const float* tcol = Tm + (16 * c) * kLd + 16 * b + cc;
+      for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;
+        const int bi = p >> 6, b = bi, a = b + d, rr = (p >> 2) & 15, q = p & 3;
+        if (bi < nb) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cc = b; cc < a; ++cc) {
+            const float* arow = Am + (16 * a + rr) * kLdA + 16 * cc;
+            const float* tcol = Tm + (16 * cc) * kLdA + 16 * b + 4 * q;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) acc = fmaf(arow[u], tcol[u * kLd], acc);
+            for (int u = 0; u < 16; ++u) {
+              const float av = arow[u];
+              const float4 tv = *reinterpret_cast<const float4*>(tcol + u * kLdA);
+              acc.x = fmaf(av, tv.x, acc.x); acc.y = fmaf(av, tv.y, acc.y);
+              acc.z = fmaf(av, tv.z, acc.z); acc.w = fmaf(av, tv.w, acc.w);
+            }
+          }
+          *reinterpret_cast<float4*>(&Xm[(bi * 16 + rr) * 20 + 4 * q]) = acc;
         }
-        Xm[(16 * a + rr) * kLd + 16 * b + cc] = acc;
-      }
-      __syncthreads();
-      for (int e = tid; e < nel; e += kThreads) {
-        const int b = e >> 8, a = b + d, rr = (e >> 4) & 15, cc = e & 15;
-        const float* trow = Tm + (16 * a + rr) * kLd + 16 * a;
-        const float* xcol = Xm + (16 * a) * kLd + 16 * b + cc;
-        float acc = 0.f;
+        named_bar(2, kPrepThreads);
+        if (bi < nb) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float* trow = Tm + (16 * a + rr) * kLdA + 16 * a;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) acc = fmaf(trow[u], xcol[u * kLd], acc);
-        Tm[(16 * a + rr) * kLd + 16 * b + cc] = -acc;
+          for (int u = 0; u < 16; ++u) {
+            const float tv = trow[u];
+            const float4 xv = *reinterpret_cast<const float4*>(&Xm[(bi * 16 + u) * 20 + 4 * q]);
+            acc.x = fmaf(tv, xv.x, acc.x); acc.y = fmaf(tv, xv.y, acc.y);
+            acc.z = fmaf(tv, xv.z, acc.z); acc.w = fmaf(tv, xv.w, acc.w);
+          }
+          *reinterpret_cast<float4*>(&Tm[(16 * a + rr) * kLdA + 16 * b + 4 * q]) =
+              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        named_bar(2, kPrepThreads);
       }
-      __syncthreads();
-    }
-    // T' = T diag(beta) as the bf16 B operand (rows r, K = i).
-    for (int e = tid; e < 64 * 8; e += kThreads) {
-      const int r = e >> 3, i0 = (e & 7) * 8;
-      float f[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u;
-        f[u] = (i >> 4) <= (r >> 4) ? Tm[r * kLd + i] * s_beta[i] : 0.f;
+      for (int e = p; e < 64 * 8; e += kPrepThreads) {
+        const int r = e >> 3, i0 = (e & 7) * 8;
+        float f8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          f8[u] = (i >> 4) <= (r >> 4) ? Tm[r * kLdA + i] * s_beta[i] : 0.f;
+        }
+        st_tile8(smem + kOffTB, r, i0, 64, f8);
       }
-      st_tile8(smem + kOffTB, r, i0, 64, f);
-    }
-    fence_async_smem();
-    __syncthreads();
+      fence_async_smem();
+      named_bar(2, kPrepThreads);
 
-    // ---- P6: W^T = Ktil^T T'^T and U0^T = V^T T'^T.
-    if (tid == 0) {
+      // ---- P6: W^T = Ktil^T T'^T and U0^T = V^T T'^T (U0 goes where the state
+      // pass accumulates U, once it has read the previous chunk's U).
+      const bool ok_u = c < 1 || sync.wait(kBarUFree, (c - 1) & 1);
+      if (leader && ok_u && !s_abort) {
+        tc_fence_after();
+        const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
+        const uint32_t aKT = smem_u32(smem + kOffKT), aV = smem_u32(smem + kOffV),
+                       bT = smem_u32(smem + kOffTB);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint64_t bd = umma_desc(bT + t * 32, 16, 1024);
+          umma_bf16(tbase + kColW, umma_desc(aKT + t * 2048, 64 * 128, 1024), bd, idesc, t > 0);
+          umma_bf16(tbase + kColU, umma_desc(aV + t * 2048, 64 * 128, 1024), bd, idesc, t > 0);
+        }
+        umma_commit(&s_bars[kBarWU]);
+      }
+      const bool ok_wu = sync.wait(kBarWU, c & 1);
+      // -W^T may overwrite the shared tile once the state pass's first MMA of
+      // the previous chunk is done.
+      const bool ok_m1 = c < 1 || sync.wait(kBarMMA1, (c - 1) & 1);
       tc_fence_after();
-      const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
-      const uint32_t aKT = smem_u32(smem + kOffKT), aV = smem_u32(smem + kOffV);
-      const uint32_t bT = smem_u32(smem + kOffTB);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint64_t bd = umma_desc(bT + s * 32, 16, 1024);
-        umma_bf16(tbase + kColW, umma_desc(aKT + s * 2048, 64 * 128, 1024), bd, idesc, s > 0);
-        umma_bf16(tbase + kColU, umma_desc(aV + s * 2048, 64 * 128, 1024), bd, idesc, s > 0);
-      }
-      umma_commit(&s_bar);
-    }
-    if (!(ok = wait_mma())) break;
 
-    // ---- P7: -W^T to shared memory (rows c, K = r) as an MN-major B operand.
-    if (warp < 4) {
-      const int c = tid;
+      // ---- P7: -W^T (rows = key channel, K = token) as an MN-major B operand.
+      if (pw < 4 && ok_wu && ok_m1) {
+        const int cc = 32 * pw + lane;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float w32[32];
-        tmem_ld32(tmem_addr(tbase, 32 * warp, kColW + 32 * half), w32);
-        tmem_ld_wait();
+        for (int half = 0; half < 2; ++half) {
+          float w[32];
+          tmem_ld32(tbase + (static_cast<uint32_t>(32 * pw) << 16) + kColW + 32 * half, w);
+          tmem_ld_wait();
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float f[8];
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float f8[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) f[u] = -w32[8 * m + u];
-          st_tile8(smem + kOffWT, c, 32 * half + 8 * m, 128, f);
+            for (int u = 0; u < 8; ++u) f8[u] = -w[8 * q8 + u];
+            st_tile8(smem + kOffWT, cc, 32 * half + 8 * q8, 128, f8);
+          }
         }
       }
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(2, kPrepThreads);
+      if (leader && !s_abort) mbar_arrive(&s_bars[kBarFull0 + s]);
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- P8: U^T += S^T (-W)^T;  O^T = S^T Qtil^T.
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t iU = umma_idesc_bf16(128, 64, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
-      const uint32_t aS = smem_u32(smem + kOffS), bW = smem_u32(smem + kOffWT),
-                     bQ = smem_u32(smem + kOffQT);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint64_t ad = umma_desc(aS + (s >> 2) * 128 * 128 + (s & 3) * 32, 16, 1024);
-        umma_bf16(tbase + kColU, ad, umma_desc(bW + s * 2048, 128 * 128, 1024), iU, 1);
-        umma_bf16(tbase + kColO, ad,
-                  umma_desc(bQ + (s >> 2) * 64 * 128 + (s & 3) * 32, 16, 1024), iO, s > 0);
-      }
-      umma_commit(&s_bar);
-    }
-    if (!(ok = wait_mma())) break;
-
-    // ---- P9: U^T to shared memory (rows j, K = i) as a K-major A operand.
-    if (warp < 4) {
-      const int j = tid;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float u32v[32];
-        tmem_ld32(tmem_addr(tbase, 32 * warp, kColU + 32 * half), u32v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float f[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) f[u] = u32v[8 * m + u];
-          st_tile8(smem + kOffUT, j, 32 * half + 8 * m, 128, f);
-        }
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- P10: dS^T = U^T Kbar;  O^T += U^T P^T.
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
-      const uint32_t aU = smem_u32(smem + kOffUT), bKB = smem_u32(smem + kOffKB),
-                     bP = smem_u32(smem + kOffP);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint64_t ad = umma_desc(aU + s * 32, 16, 1024);
-        umma_bf16(tbase + kColDS, ad, umma_desc(bKB + s * 2048, 64 * 128, 1024), iS, s > 0);
-        umma_bf16(tbase + kColO, ad, umma_desc(bP + s * 32, 16, 1024), iO, 1);
-      }
-      umma_commit(&s_bar);
-    }
-    if (!(ok = wait_mma())) break;
-
-    // ---- P11: state update, bf16 state copy, outputs.
-    {
-      const uint32_t lane_base = 32 * (warp & 3);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float d32[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, kColDS + 64 * sh + 32 * half), d32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int i = 32 * half + u;
-          S[i] = fmaf(s_gamma[64 * sh + i], S[i], d32[u]);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        float f[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) f[u] = S[8 * m + u];
-        st_tile8(smem + kOffS, sj, 64 * sh + 8 * m, 128, f);
-      }
-      float o32[32];
-      tmem_ld32(tmem_addr(tbase, lane_base, kColO + 32 * sh), o32);
-      tmem_ld_wait();
-      __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kOffO);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) so[(32 * sh + u) * kLdO + sj] = __float2bfloat16_rn(o32[u]);
-    }
-    __syncthreads();
-    for (int e = tid; e < 64 * 16; e += kThreads) {
-      const int row = e >> 4, ch = e & 15;
-      if (row < L) {
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffO + row * kLdO * 2 + ch * 16);
-        *reinterpret_cast<uint4*>(gout + ((c0 + row) * H + h) * kD + 8 * ch) = v;
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
   }
 
-  if (!ok && tid == 0 && args.dev_status) atomicExch(args.dev_status, KDA_ERR_TIMEOUT);
-  if (ok && args.final_state) {
-#pragma unroll
-    for (int i = 0; i < 64; ++i) __stcs(args.final_state + soff + (64 * sh + i) * kD + sj, S[i]);
-  }
   tc_fence_before();
   __syncthreads();
+  if (s_abort && tid == 0 && args.dev_status) atomicExch(args.dev_status, KDA_ERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
