@@ -31,7 +31,15 @@
 // Handoffs use mbarriers (a two-slot ring for the per-chunk tiles the state
 // pass consumes).  Every wait is bounded; on expiry the CTA stops issuing
 // work, reports KDA_ERR_TIMEOUT and exits.
+// Raw q, k, v, g tiles of the next chunk arrive by TMA into tiles that are
+// dead at that point (k and v into the [K';Q'] tile once the masked-product
+// MMA has read it, q and g into the Qtil / Kbar slot the next chunk will
+// overwrite in place), so the prefetch costs no extra shared memory.
+//
+// Building with -DKDA_PHASE_PROFILE records per-phase SM-clock totals of
+// CTA (0, 0) in the device array kda_phase_clocks (instrumentation only).
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -59,7 +67,16 @@ constexpr uint32_t kOffQT = kOffTB + 8192;     // Qtil = q e^G, 2 slots        6
 constexpr uint32_t kOffKB = kOffQT + 32768;    // Kbar, 2 slots                64 x 128
 constexpr uint32_t kOffWT = kOffKB + 32768;    // -W^T                        128 x 64
 constexpr uint32_t kOffP = kOffWT + 16384;     // P, 2 slots                   64 x 64
-constexpr uint32_t kTileBytes = kOffP + 16384;
+constexpr uint32_t kOffO = kOffP + 16384;      // O staging (row-major bf16)   64 x 128
+constexpr uint32_t kTileBytes = kOffO + 16384;
+// Raw tiles of the next chunk (TMA destinations, same swizzled layout).
+constexpr uint32_t kOffRawK = kOffKQ;          // 64 x 128, dead once AP is done
+constexpr uint32_t kOffRawV = kOffKQ + 16384;  // 64 x 128
+// (raw q and g land in the Qtil and Kbar slot of their chunk.)
+// Per-chunk scan sums and Khat factors live in the T' tile until P5 writes it.
+constexpr uint32_t kOffTileTot = kOffTB;       // fp32 [4][128]
+constexpr uint32_t kOffFac = kOffTB + 2048;    // fp32 [4][3][128]
+static_assert(2048 + 4 * 3 * 128 * 4 <= 8192, "scan sums and factors fit in the T' tile");
 constexpr uint32_t kSmemBytes = kTileBytes + 1024;
 // fp32 work matrices of the inverse reuse the Khat tile once AP is done.
 constexpr int kLdA = 68;                                 // 16-byte aligned rows
@@ -79,16 +96,24 @@ constexpr uint32_t kColUT = 480;   // 32: bf16 U^T, A operand
 constexpr uint32_t kTmemCols = 512;
 
 enum { kBarAP = 0, kBarWU, kBarFull0, kBarFull1, kBarEmpty0, kBarEmpty1, kBarMMA1, kBarUFree,
-       kBarMMA2, kNumBars };
+       kBarMMA2, kBarRaw, kNumBars };
+
+#ifdef KDA_PHASE_PROFILE
+__device__ unsigned long long kda_phase_clocks[32];
+#define KDA_MARK(i)                                   \
+  do {                                                \
+    const unsigned long long now_ = clock64();        \
+    prof_acc[i] += now_ - prof_t;                     \
+    prof_t = now_;                                    \
+  } while (0)
+#else
+#define KDA_MARK(i) ((void)0)
+#endif
 
 __device__ __forceinline__ int khat_row0(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
 
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ uint4 ldg16(const __nv_bfloat16* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -132,13 +157,15 @@ struct Sync {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) {
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_tc_kernel(LaunchArgs args, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ __align__(16) float s_gamma[2][kD];     // e^{G_C} per channel, per slot
-  __shared__ __align__(16) float s_tile_tot[4][kD];  // per-tile sums of g (log2 units)
-  __shared__ __align__(16) float s_fac[4][3][kD];    // e^{R_{a+1+i} - R_a}, tile a
   __shared__ float s_beta[kC];
   __shared__ uint64_t s_bars[kNumBars];
   __shared__ uint32_t s_tmem;
@@ -172,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
   tc_fence_after();
   const uint32_t tbase = s_tmem;
   Sync sync{s_bars, &s_abort};
+#ifdef KDA_PHASE_PROFILE
+  unsigned long long prof_acc[16] = {}, prof_t = clock64();
+#endif
 
   if (tid < kStateThreads) {
     // =============================== state pass ===============================
@@ -205,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       const long long c0 = t0 + static_cast<long long>(c) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool ok_full = sync.wait(kBarFull0 + s, (c >> 1) & 1);
+      KDA_MARK(0);
       tc_fence_after();
       if (j == 0 && ok_full) {
         // U^T += S^T (-W)^T ;  O^T = S^T Qtil^T      (K = dk = 128)
@@ -220,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         }
         umma_commit(&s_bars[kBarMMA1]);
       }
+      KDA_MARK(1);
       // Decay the fp32 state in place: S <- Diag(e^{G_C}) S (MMA1 does not read it).
       if (ok_full) {
 #pragma unroll 1
@@ -240,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         }
       }
       const bool ok1 = sync.wait(kBarMMA1, c & 1);
+      KDA_MARK(2);
       tc_fence_after();
       if (ok1) {
         // U^T (fp32) -> bf16 A operand.
@@ -273,7 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         umma_commit(&s_bars[kBarEmpty0 + s]);
         umma_commit(&s_bars[kBarMMA2]);
       }
+      KDA_MARK(3);
       const bool ok2 = sync.wait(kBarMMA2, c & 1);
+      KDA_MARK(4);
       tc_fence_after();
       float o0[32], o1[32];
       if (ok2) {
@@ -295,17 +330,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       tmem_st_wait();
       tc_fence_before();
       named_bar(1, kStateThreads);
+      KDA_MARK(5);
+      // O^T column j -> row-major staging, then 16-byte rows to global memory.
       if (ok2) {
-        __nv_bfloat16* dst = gout + (c0 * H + h) * kD + j;
-        const long long rs = static_cast<long long>(H) * kD;
+        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kOffO) + j;
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (r < L) dst[r * rs] = __float2bfloat16_rn(o0[r]);
+        for (int r = 0; r < 32; ++r) so[r * kD] = __float2bfloat16_rn(o0[r]);
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (32 + r < L) dst[(32 + r) * rs] = __float2bfloat16_rn(o1[r]);
+        for (int r = 0; r < 32; ++r) so[(32 + r) * kD] = __float2bfloat16_rn(o1[r]);
       }
+      named_bar(1, kStateThreads);
+      if (ok2) {
+        __nv_bfloat16* dst = gout + (c0 * H + h) * kD;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = j + kStateThreads * i, r = e >> 4, ch = e & 15;
+          if (r < L)
+            *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H * kD + 8 * ch) =
+                *reinterpret_cast<const uint4*>(smem + kOffO + r * 256 + ch * 16);
+        }
+      }
+      KDA_MARK(6);
     }
+#ifdef KDA_PHASE_PROFILE
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
+      for (int i = 0; i < 8; ++i) kda_phase_clocks[i] = prof_acc[i];
+      kda_phase_clocks[24] = n_chunks;
+    }
+#endif
     if (!s_abort && args.final_state) {
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
@@ -324,42 +376,76 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
     const int cg = 8 * (pw >> 2) + (lane & 7);  // channel group: channels 8 cg .. 8 cg + 7
     const int r4 = lane >> 3;                   // rows 16 ta + 4 r4 + m, m = 0..3
     const int row0 = 16 * ta + 4 * r4;
-    const bool leader = p == 0;
-    const __nv_bfloat16* __restrict__ gq = static_cast<const __nv_bfloat16*>(args.q);
-    const __nv_bfloat16* __restrict__ gk = static_cast<const __nv_bfloat16*>(args.k);
-    const __nv_bfloat16* __restrict__ gv = static_cast<const __nv_bfloat16*>(args.v);
-    const __nv_bfloat16* __restrict__ gg = static_cast<const __nv_bfloat16*>(args.g);
+    const bool leader = p == 0;                 // issues the prep MMAs
+    const bool loader = p == 128;               // issues the raw-tile TMA loads
     const __nv_bfloat16* __restrict__ gb = static_cast<const __nv_bfloat16*>(args.beta);
     float* Am = reinterpret_cast<float*>(smem + kOffA);
     float* Tm = reinterpret_cast<float*>(smem + kOffT);
     float* Xm = reinterpret_cast<float*>(smem + kOffX);
+    float* tile_tot = reinterpret_cast<float*>(smem + kOffTileTot);  // [4][128]
+    float* fac = reinterpret_cast<float*>(smem + kOffFac);           // [4][3][128]
 
-    uint4 rq[4], rk[4], rgt[4], rv[4];
+    auto chunk_len = [&](int c) {
+      const long long rem = t1 - (t0 + static_cast<long long>(c) * kC);
+      return static_cast<int>(rem < kC ? rem : kC);
+    };
+    // Raw q, k, v, g of chunk c: two 64-channel boxes each, by TMA.
+    auto issue_raw = [&](int c) {
+      const int s = c & 1;
+      const int c0 = static_cast<int>(t0 + static_cast<long long>(c) * kC);
+      uint64_t* bar = &s_bars[kBarRaw];
+      mbar_arrive_expect_tx(bar, 4 * 16384);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(smem + kOffRawK + hf * 8192, &tm_k, 64 * hf, h, c0, bar);
+        tma_load_3d(smem + kOffRawV + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
+        tma_load_3d(smem + kOffQT + s * 16384 + hf * 8192, &tm_q, 64 * hf, h, c0, bar);
+        tma_load_3d(smem + kOffKB + s * 16384 + hf * 8192, &tm_g, 64 * hf, h, c0, bar);
+      }
+    };
+    // beta of chunk c: the 16 threads of channel group 0 hold 4 rows each.
     float rb[4];
-    auto load_chunk = [&](int c) {
+    auto load_beta = [&](int c) {
       const long long c0 = t0 + static_cast<long long>(c) * kC;
-      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      const int L = chunk_len(c);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int r = row0 + m;
-        if (r < L) {
-          const long long off = ((c0 + r) * H + h) * kD + 8 * cg;
-          rq[m] = ldg16(gq + off);
-          rk[m] = ldg16(gk + off);
-          rgt[m] = ldg16(gg + off);
-          rv[m] = ldg16(gv + off);
-          rb[m] = cg == 0 ? __bfloat162float(gb[(c0 + r) * H + h]) : 0.f;
-        } else {
-          rq[m] = rk[m] = rgt[m] = rv[m] = make_uint4(0, 0, 0, 0);
-          rb[m] = 0.f;
-        }
+        rb[m] = (cg == 0 && r < L) ? __bfloat162float(gb[(c0 + r) * H + h]) : 0.f;
       }
     };
-    if (n_chunks > 0) load_chunk(0);
+    if (n_chunks > 0) {
+      if (loader) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_g);
+        issue_raw(0);
+      }
+      load_beta(0);
+    }
 
 #pragma unroll 1
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
+      const int L = chunk_len(c);
+      const bool ok_raw = sync.wait(kBarRaw, c & 1);
+      KDA_MARK(8);
+      // Raw rows of this chunk (rows past the end of the sequence read as 0).
+      uint4 rq[4], rk[4], rgt[4], rv[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int r = row0 + m;
+        const uint32_t off = sw128_off(r, 8 * cg, 64);
+        if (r < L && ok_raw) {
+          rgt[m] = *reinterpret_cast<const uint4*>(smem + kOffKB + s * 16384 + off);
+          rq[m] = *reinterpret_cast<const uint4*>(smem + kOffQT + s * 16384 + off);
+          rk[m] = *reinterpret_cast<const uint4*>(smem + kOffRawK + off);
+          rv[m] = *reinterpret_cast<const uint4*>(smem + kOffRawV + off);
+        } else {
+          rgt[m] = rq[m] = rk[m] = rv[m] = make_uint4(0, 0, 0, 0);
+        }
+      }
       // ---- P1: cumulative decay (log2 units) along the chunk, per channel.
       float G[4][8];
       {
@@ -382,11 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         const float excl = tot - G[3][u];
 #pragma unroll
         for (int m = 0; m < 4; ++m) G[m][u] += excl;
-        if (r4 == 3) s_tile_tot[ta][8 * cg + u] = tot;
+        if (r4 == 3) tile_tot[ta * kD + 8 * cg + u] = tot;
       }
-      // Slots of the per-chunk tiles the state pass reads: free once the
-      // state pass of chunk c - 2 has finished its last MMA.
-      const bool ok_e = c < 2 || sync.wait(kBarEmpty0 + s, ((c >> 1) - 1) & 1);
+      // Tile sums are visible, and every raw k / v read is done before the
+      // [K';Q'] tile is rewritten.
       named_bar(2, kPrepThreads);
       float R[4][8], GC[8];
       {
@@ -395,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         for (int a = 0; a < 4; ++a) {
 #pragma unroll
           for (int u = 0; u < 8; ++u) R[a][u] = acc[u];
-          const float4 t0v = *reinterpret_cast<const float4*>(&s_tile_tot[a][8 * cg]);
-          const float4 t1v = *reinterpret_cast<const float4*>(&s_tile_tot[a][8 * cg + 4]);
+          const float4 t0v = *reinterpret_cast<const float4*>(&tile_tot[a * kD + 8 * cg]);
+          const float4 t1v = *reinterpret_cast<const float4*>(&tile_tot[a * kD + 8 * cg + 4]);
           acc[0] += t0v.x; acc[1] += t0v.y; acc[2] += t0v.z; acc[3] += t0v.w;
           acc[4] += t1v.x; acc[5] += t1v.y; acc[6] += t1v.z; acc[7] += t1v.w;
         }
@@ -411,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         for (int m = 0; m < 4; ++m) G[m][u] += Ra[u];
       }
 
-      // ---- P2: scaled operand tiles.
+      // ---- P2: scaled operand tiles (packed fp32 pairs, one rounding each).
       {
         uint8_t* qt = smem + kOffQT + s * 16384;
         uint8_t* kb = smem + kOffKB + s * 16384;
@@ -421,11 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
           *reinterpret_cast<uint4*>(smem + kOffV + sw128_off(r, 8 * cg, 64)) = rv[m];
           if (cg == 0) s_beta[r] = rb[m];
         }
-        float eR[8], eC[8];
+        uint64_t eR[4], eC[4], Rp[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          eR[u] = exp2f(Ra[u]);
-          eC[u] = exp2f(GC[u] - Ra[u]);
+        for (int w = 0; w < 4; ++w) {
+          eR[w] = f2_pack(ex2_fast(Ra[2 * w]), ex2_fast(Ra[2 * w + 1]));
+          eC[w] = f2_pack(ex2_fast(GC[2 * w] - Ra[2 * w]), ex2_fast(GC[2 * w + 1] - Ra[2 * w + 1]));
+          Rp[w] = f2_pack(Ra[2 * w], Ra[2 * w + 1]);
         }
         // Khat factors for the later key blocks, e^{R_{a2} - R_ta} <= 1, shared
         // by the warp (all its lanes are in tile ta).
@@ -438,60 +524,76 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
                 const float ra2 = a2 == 1 ? R[1][u] : a2 == 2 ? R[2][u] : R[3][u];
-                f8[u] = exp2f(ra2 - Ra[u]);
+                f8[u] = ex2_fast(ra2 - Ra[u]);
               }
-              *reinterpret_cast<float4*>(&s_fac[ta][i][8 * cg]) =
-                  make_float4(f8[0], f8[1], f8[2], f8[3]);
-              *reinterpret_cast<float4*>(&s_fac[ta][i][8 * cg + 4]) =
-                  make_float4(f8[4], f8[5], f8[6], f8[7]);
+              float* fr = fac + (ta * 3 + i) * kD + 8 * cg;
+              *reinterpret_cast<float4*>(fr) = make_float4(f8[0], f8[1], f8[2], f8[3]);
+              *reinterpret_cast<float4*>(fr + 4) = make_float4(f8[4], f8[5], f8[6], f8[7]);
             }
           }
           if (ta == 0) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) s_gamma[s][8 * cg + u] = exp2f(GC[u]);
+            for (int u = 0; u < 8; ++u) s_gamma[s][8 * cg + u] = ex2_fast(GC[u]);
           }
         }
         __syncwarp();
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int r = row0 + m, rl = 4 * r4 + m;
-          float kf[8], qf[8], x[8], y[8];
-          unpack8(rk[m], kf);
-          unpack8(rq[m], qf);
+          const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
+          const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
+          uint32_t okp[4], oqp[4], okt[4], oqt[4], okh[4], okb[4];
+          uint64_t kh[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float e1 = exp2f(G[m][u] - Ra[u]);
-            x[u] = kf[u] * e1;
-            y[u] = qf[u] * e1;
+          for (int w = 0; w < 4; ++w) {
+            const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
+            float dx, dy;
+            f2_unpack(f2_sub(f2_pack(G[m][2 * w], G[m][2 * w + 1]), Rp[w]), dx, dy);
+            const uint64_t e1 = f2_pack(ex2_fast(dx), ex2_fast(dy));    // e^{G - R_ta} <= 1
+            const uint64_t ei = f2_pack(ex2_fast(-dx), ex2_fast(-dy));  // e^{R_ta - G} < e^80
+            const uint64_t k1 = f2_mul(kp, e1), q1 = f2_mul(qp, e1);
+            okp[w] = f2_to_bf16x2(k1);
+            oqp[w] = f2_to_bf16x2(q1);
+            okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
+            oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
+            kh[w] = f2_mul(kp, ei);
+            okh[w] = f2_to_bf16x2(kh[w]);
+            okb[w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
           }
-          st_tile8(smem + kOffKQ, 32 * ta + rl, 8 * cg, 128, x);
-          st_tile8(smem + kOffKQ, 32 * ta + 16 + rl, 8 * cg, 128, y);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) { x[u] *= eR[u]; y[u] *= eR[u]; }
-          if (ok_e) st_tile8(qt, r, 8 * cg, 64, y);
-          st_tile8(smem + kOffKT, r, 8 * cg, 64, x);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            x[u] = kf[u] * exp2f(Ra[u] - G[m][u]);
-            y[u] = x[u] * eC[u];
+          auto st4 = [&](uint32_t off_tile, int row, int rows, const uint32_t (&v)[4]) {
+            *reinterpret_cast<uint4*>(smem + off_tile + sw128_off(row, 8 * cg, rows)) =
+                make_uint4(v[0], v[1], v[2], v[3]);
+          };
+          st4(kOffKQ, 32 * ta + rl, 128, okp);
+          st4(kOffKQ, 32 * ta + 16 + rl, 128, oqp);
+          st4(kOffKT, r, 64, okt);
+          st4(kOffKH, khat_row0(ta) + r, 160, okh);
+          if (ok_raw) {
+            *reinterpret_cast<uint4*>(qt + sw128_off(r, 8 * cg, 64)) =
+                make_uint4(oqt[0], oqt[1], oqt[2], oqt[3]);
+            *reinterpret_cast<uint4*>(kb + sw128_off(r, 8 * cg, 64)) =
+                make_uint4(okb[0], okb[1], okb[2], okb[3]);
           }
-          if (ok_e) st_tile8(kb, r, 8 * cg, 64, y);
-          st_tile8(smem + kOffKH, khat_row0(ta) + r, 8 * cg, 160, x);
 #pragma unroll
           for (int i = 0; i < 3; ++i) {
             if (ta + 1 + i < 4) {
-              const float4 f0 = *reinterpret_cast<const float4*>(&s_fac[ta][i][8 * cg]);
-              const float4 f1 = *reinterpret_cast<const float4*>(&s_fac[ta][i][8 * cg + 4]);
-              y[0] = x[0] * f0.x; y[1] = x[1] * f0.y; y[2] = x[2] * f0.z; y[3] = x[3] * f0.w;
-              y[4] = x[4] * f1.x; y[5] = x[5] * f1.y; y[6] = x[6] * f1.z; y[7] = x[7] * f1.w;
-              st_tile8(smem + kOffKH, khat_row0(ta + 1 + i) + r, 8 * cg, 160, y);
+              const float* fr = fac + (ta * 3 + i) * kD + 8 * cg;
+              const float4 f0 = *reinterpret_cast<const float4*>(fr);
+              const float4 f1 = *reinterpret_cast<const float4*>(fr + 4);
+              const uint64_t fp[4] = {f2_pack(f0.x, f0.y), f2_pack(f0.z, f0.w),
+                                      f2_pack(f1.x, f1.y), f2_pack(f1.z, f1.w)};
+              uint32_t ox[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[w], fp[w]));
+              st4(kOffKH, khat_row0(ta + 1 + i) + r, 160, ox);
             }
           }
         }
       }
-      if (c + 1 < n_chunks) load_chunk(c + 1);
+      if (c + 1 < n_chunks) load_beta(c + 1);
       fence_async_smem();
       named_bar(2, kPrepThreads);
+      KDA_MARK(9);
 
       // ---- P3: every masked intra-chunk product in one MMA.
       if (leader && !s_abort) {
@@ -505,7 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
         umma_commit(&s_bars[kBarAP]);
       }
       const bool ok_ap = sync.wait(kBarAP, c & 1);
+      KDA_MARK(10);
       tc_fence_after();
+      // Prefetch the next chunk's raw tiles: AP has read [K';Q'], and the
+      // Qtil / Kbar slot of chunk c + 1 is free once the state pass of chunk
+      // c - 1 has finished its last MMA.
+      if (loader && c + 1 < n_chunks && ok_ap) {
+        const bool ok_e = c < 1 || sync.wait(kBarEmpty0 + ((c + 1) & 1), ((c - 1) >> 1) & 1);
+        if (ok_e) issue_raw(c + 1);
+      }
 
       // ---- P4: A (x beta, strictly lower; fp32) and P (lower inclusive; bf16).
       if (pw < 4 && ok_ap) {
@@ -532,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
             for (int u = 0; u < 16; ++u) v[u] = 0.f;
           }
           if (isP) {
-            if (ok_e) {
+            if (ok_raw) {
 #pragma unroll
               for (int h8 = 0; h8 < 2; ++h8) {
                 float f8[8];
@@ -552,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       tc_fence_before();
       named_bar(2, kPrepThreads);
 
+      KDA_MARK(11);
       // ---- P5: T = (I + A)^-1 in fp32; T' = T diag(beta) as bf16.
       if (p < 64) {
         const int blk = p >> 4, jj = p & 15;
@@ -617,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       fence_async_smem();
       named_bar(2, kPrepThreads);
 
+      KDA_MARK(12);
       // ---- P6: W^T = Ktil^T T'^T and U0^T = V^T T'^T (U0 goes where the state
       // pass accumulates U, once it has read the previous chunk's U).
       const bool ok_u = c < 1 || sync.wait(kBarUFree, (c - 1) & 1);
@@ -637,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       // -W^T may overwrite the shared tile once the state pass's first MMA of
       // the previous chunk is done.
       const bool ok_m1 = c < 1 || sync.wait(kBarMMA1, (c - 1) & 1);
+      KDA_MARK(13);
       tc_fence_after();
 
       // ---- P7: -W^T (rows = key channel, K = token) as an MN-major B operand.
@@ -660,7 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
       tc_fence_before();
       named_bar(2, kPrepThreads);
       if (leader && !s_abort) mbar_arrive(&s_bars[kBarFull0 + s]);
+      KDA_MARK(14);
     }
+#ifdef KDA_PHASE_PROFILE
+    if (blockIdx.x == 0 && blockIdx.y == 0 && p == 0)
+      for (int i = 8; i < 16; ++i) kda_phase_clocks[i] = prof_acc[i];
+#endif
   }
 
   tc_fence_before();
@@ -669,10 +787,44 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(LaunchArgs args) 
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// [T, H, 128] bf16 viewed as a 3-D tensor (channel, head, token); one box is
+// 64 channels x 1 head x 64 tokens, 128B-swizzled, zero-filled past T.
+bool make_token_map(CUtensorMap* map, const void* base, int heads, long long tokens) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(heads) * kD * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kC)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool chunk_tc_supported(const LaunchArgs& a) {
-  return a.dtype == KDA_BF16 && a.dk == kD && a.dv == kD && a.chunk == kC;
+  return a.dtype == KDA_BF16 && a.dk == kD && a.dv == kD && a.chunk == kC &&
+         a.total_tokens < (1ll << 31);
 }
 
 cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream) {
@@ -681,9 +833,25 @@ cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
+  CUtensorMap maps[4] = {};
+  if (a.total_tokens > 0) {
+    const void* bases[4] = {a.q, a.k, a.v, a.g};
+    for (int i = 0; i < 4; ++i)
+      if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
+        return cudaErrorInvalidValue;
+  }
   dim3 grid(a.n_seqs, a.heads);
-  chunk_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  chunk_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }
+
+#ifdef KDA_PHASE_PROFILE
+// Copies the phase totals of the last profiled launch to the host (build with
+// -DKDA_PHASE_PROFILE only).
+extern "C" KDA_API int kda_debug_phase_clocks(unsigned long long* host) {
+  return static_cast<int>(
+      cudaMemcpyFromSymbol(host, kda_phase_clocks, sizeof(unsigned long long) * 32));
+}
+#endif
 
 }  // namespace kda
