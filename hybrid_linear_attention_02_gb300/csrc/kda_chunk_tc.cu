@@ -20,7 +20,7 @@
 // the serial state pass, and the two run concurrently on different warps:
 //   prep  (warps 4..11) for chunk c+1:  cumulative decay, scaled operand tiles,
 //         AP = [K';Q'] x Khat^T (one M=128 N=160 K=128 MMA), A and P rows,
-//         T = (I + A)^-1 in fp32, W^T = Ktil^T T'^T and U0^T = V^T T'^T
+//         T = (I + A)^-1 in fp32 (block Neumann form), W^T = Ktil^T T'^T and U0^T = V^T T'^T
 //         (T' = T diag(beta)), -W^T to shared memory.
 //   state (warps 0..3) for chunk c:  U^T = U0^T + S^T(-W)^T, O^T = S^T Qtil^T;
 //         S <- Diag(e^{G_C}) S (fp32, in TMEM);  U^T -> bf16 in TMEM;
@@ -32,9 +32,10 @@
 // pass consumes).  Every wait is bounded; on expiry the CTA stops issuing
 // work, reports KDA_ERR_TIMEOUT and exits.
 // Raw q, k, v, g tiles of the next chunk arrive by TMA into tiles that are
-// dead at that point (k and v into the [K';Q'] tile once the masked-product
-// MMA has read it, q and g into the Qtil / Kbar slot the next chunk will
-// overwrite in place), so the prefetch costs no extra shared memory.
+// dead at that point (k into the [K';Q'] tile once the masked-product MMA has
+// read it, v into the V tile once U0 is done, q and g into the Qtil / Kbar
+// slot the next chunk overwrites in place), so the prefetch costs no extra
+// shared memory.
 //
 // Building with -DKDA_PHASE_PROFILE records per-phase SM-clock totals of
 // CTA (0, 0) in the device array kda_phase_clocks (instrumentation only).
@@ -54,6 +55,13 @@ constexpr int kD = 128;
 constexpr int kStateThreads = 128;                  // warps 0..3
 constexpr int kPrepThreads = 256;                   // warps 4..11
 constexpr int kThreads = kStateThreads + kPrepThreads;
+// Register split: the block launches with 168 per thread (384 x 168 = 64512);
+// the state warpgroup gives up 80 per thread and the two prep warpgroups take
+// 40 more each (128 x 88 + 256 x 208 = 64512).
+constexpr int kStateRegs = 88;
+constexpr int kPrepRegs = 208;
+static_assert(kStateThreads * kStateRegs + kPrepThreads * kPrepRegs <= kThreads * 168,
+              "register split fits the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory tiles (byte offsets from a 1024-aligned base); bf16 tiles use
@@ -69,21 +77,26 @@ constexpr uint32_t kOffWT = kOffKB + 32768;    // -W^T                        12
 constexpr uint32_t kOffP = kOffWT + 16384;     // P, 2 slots                   64 x 64
 constexpr uint32_t kOffO = kOffP + 16384;      // O staging (row-major bf16)   64 x 128
 constexpr uint32_t kTileBytes = kOffO + 16384;
-// Raw tiles of the next chunk (TMA destinations, same swizzled layout).
-constexpr uint32_t kOffRawK = kOffKQ;          // 64 x 128, dead once AP is done
-constexpr uint32_t kOffRawV = kOffKQ + 16384;  // 64 x 128
-// (raw q and g land in the Qtil and Kbar slot of their chunk.)
-// Per-chunk scan sums and Khat factors live in the T' tile until P5 writes it.
-constexpr uint32_t kOffTileTot = kOffTB;       // fp32 [4][128]
-constexpr uint32_t kOffFac = kOffTB + 2048;    // fp32 [4][3][128]
-static_assert(2048 + 4 * 3 * 128 * 4 <= 8192, "scan sums and factors fit in the T' tile");
+// Raw tiles of the next chunk (TMA destinations, same swizzled layout): k in
+// the [K';Q'] tile once AP has read it, v straight into the V tile, q and g in
+// the Qtil and Kbar slot of their chunk (overwritten in place).
+constexpr uint32_t kOffRawK = kOffKQ;          // 64 x 128
+// Per-chunk tile sums and per-(tile, channel) factors live in the T' tile
+// until P5 writes it; the Khat block factors in the chunk's P slot until P4.
+constexpr uint32_t kOffTileTot = kOffTB;              // fp32 [4][128]
+constexpr uint32_t kOffTabR = kOffTB + 2048;          // fp32 [2][4][128]
+static_assert(2048 + 2 * 4 * 128 * 4 <= 8192, "tile sums and factors fit in the T' tile");
+static_assert(6 * 128 * 4 <= 8192, "Khat factors fit in a P slot");
 constexpr uint32_t kSmemBytes = kTileBytes + 1024;
 // fp32 work matrices of the inverse reuse the Khat tile once AP is done.
 constexpr int kLdA = 68;                                 // 16-byte aligned rows
-constexpr uint32_t kOffA = kOffKH;                       // A  64 x 68
-constexpr uint32_t kOffT = kOffA + 64 * kLdA * 4;        // T  64 x 68
-constexpr uint32_t kOffX = kOffT + 64 * kLdA * 4;        // X  3 x 16 x 20
-static_assert(kOffX + 3 * 16 * 20 * 4 <= kOffKH + 40960, "inverse scratch fits");
+constexpr uint32_t kOffA = kOffKH;                       // A     64 x 68
+constexpr int kLdB = 20;                                 // 16 x 16 blocks, 16-byte rows
+constexpr uint32_t kOffD = kOffA + 64 * kLdA * 4;        // D     4 x 16 x 20
+constexpr uint32_t kOffN = kOffD + 4 * 16 * kLdB * 4;    // N     6 x 16 x 20
+constexpr uint32_t kOffN2 = kOffN + 6 * 16 * kLdB * 4;   // N^2   3 x 16 x 20
+constexpr uint32_t kOffN3 = kOffN2 + 3 * 16 * kLdB * 4;  // N^3   16 x 20
+static_assert(kOffN3 + 16 * kLdB * 4 <= kOffKH + 40960, "inverse scratch fits");
 
 // TMEM columns (512 allocated).
 constexpr uint32_t kColAP = 0;     // 160 fp32: AP;  W^T reuses columns 0..63
@@ -96,7 +109,7 @@ constexpr uint32_t kColUT = 480;   // 32: bf16 U^T, A operand
 constexpr uint32_t kTmemCols = 512;
 
 enum { kBarAP = 0, kBarWU, kBarFull0, kBarFull1, kBarEmpty0, kBarEmpty1, kBarMMA1, kBarUFree,
-       kBarMMA2, kBarRaw, kNumBars };
+       kBarMMA2, kBarRaw, kBarRawV, kNumBars };
 
 #ifdef KDA_PHASE_PROFILE
 __device__ unsigned long long kda_phase_clocks[32];
@@ -144,14 +157,13 @@ struct Sync {
     if (*abort) return false;
     if (mbar_try_wait(&bars[b], parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(&bars[b], parity)) return true;
-      if ((it & 255u) == 0) {
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > 2000000000ull) {
-          *abort = 1;
-          return false;
-        }
+    for (;;) {
+      // Suspended until the phase completes (or 20 us pass), not spinning.
+      if (mbar_try_wait_sleep(&bars[b], parity, 20000u)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 2000000000ull) {
+        *abort = 1;
+        return false;
       }
     }
   }
@@ -200,11 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = s_tmem;
   Sync sync{s_bars, &s_abort};
 #ifdef KDA_PHASE_PROFILE
-  unsigned long long prof_acc[16] = {}, prof_t = clock64();
+  unsigned long long prof_acc[24] = {}, prof_t = clock64();
 #endif
 
   if (tid < kStateThreads) {
     // =============================== state pass ===============================
+    regs_dec<kStateRegs>();
     const int j = tid;                                   // TMEM lane = value column
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     const long long soff = (static_cast<long long>(n) * H + h) * kD * kD;
@@ -229,11 +242,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     named_bar(1, kStateThreads);
 
+    // Outputs of chunk cc leave from the staging tile as 16-byte rows.
+    auto store_out = [&](int cc) {
+      const long long c0 = t0 + static_cast<long long>(cc) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      __nv_bfloat16* dst = gout + (c0 * H + h) * kD;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = j + kStateThreads * i, r = e >> 4, ch = e & 15;
+        if (r < L)
+          *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H * kD + 8 * ch) =
+              *reinterpret_cast<const uint4*>(smem + kOffO + r * 256 + ch * 16);
+      }
+    };
+    bool prev_ok = false;
+
 #pragma unroll 1
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
-      const long long c0 = t0 + static_cast<long long>(c) * kC;
-      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool ok_full = sync.wait(kBarFull0 + s, (c >> 1) & 1);
       KDA_MARK(0);
       tc_fence_after();
@@ -252,23 +278,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s_bars[kBarMMA1]);
       }
       KDA_MARK(1);
+      // The previous chunk's outputs leave while MMA1 runs.
+      if (c > 0 && prev_ok) store_out(c - 1);
       // Decay the fp32 state in place: S <- Diag(e^{G_C}) S (MMA1 does not read it).
       if (ok_full) {
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float v[32];
-          tmem_ld32(tbase + lane_base + kColS + 32 * cb, v);
+        for (int cb = 0; cb < 8; ++cb) {
+          float v[16];
+          tmem_ld16(tbase + lane_base + kColS + 16 * cb, v);
           tmem_ld_wait();
-          uint32_t f[32];
+          uint32_t f[16];
 #pragma unroll
-          for (int u = 0; u < 32; u += 4) {
-            const float4 gm = *reinterpret_cast<const float4*>(&s_gamma[s][32 * cb + u]);
+          for (int u = 0; u < 16; u += 4) {
+            const float4 gm = *reinterpret_cast<const float4*>(&s_gamma[s][16 * cb + u]);
             f[u] = __float_as_uint(v[u] * gm.x);
             f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
             f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
             f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
           }
-          tmem_st32(tbase + lane_base + kColS + 32 * cb, f);
+          tmem_st16(tbase + lane_base + kColS + 16 * cb, f);
         }
       }
       const bool ok1 = sync.wait(kBarMMA1, c & 1);
@@ -310,9 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok2 = sync.wait(kBarMMA2, c & 1);
       KDA_MARK(4);
       tc_fence_after();
-      float o0[32], o1[32];
       if (ok2) {
-        // New state -> bf16 operand copy; O^T -> registers.
+        // New state -> bf16 operand copy; O^T column j -> row-major staging.
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float v[32];
@@ -323,39 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
           tmem_st16(tbase + lane_base + kColSB + 16 * cb, b);
         }
-        tmem_ld32(tbase + lane_base + kColO, o0);
-        tmem_ld32(tbase + lane_base + kColO + 32, o1);
-        tmem_ld_wait();
+        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kOffO) + j;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kColO + 32 * half, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int r = 0; r < 32; ++r) so[(32 * half + r) * kD] = __float2bfloat16_rn(v[r]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       named_bar(1, kStateThreads);
+      prev_ok = ok2;
       KDA_MARK(5);
-      // O^T column j -> row-major staging, then 16-byte rows to global memory.
-      if (ok2) {
-        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kOffO) + j;
-#pragma unroll
-        for (int r = 0; r < 32; ++r) so[r * kD] = __float2bfloat16_rn(o0[r]);
-#pragma unroll
-        for (int r = 0; r < 32; ++r) so[(32 + r) * kD] = __float2bfloat16_rn(o1[r]);
-      }
-      named_bar(1, kStateThreads);
-      if (ok2) {
-        __nv_bfloat16* dst = gout + (c0 * H + h) * kD;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = j + kStateThreads * i, r = e >> 4, ch = e & 15;
-          if (r < L)
-            *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H * kD + 8 * ch) =
-                *reinterpret_cast<const uint4*>(smem + kOffO + r * 256 + ch * 16);
-        }
-      }
-      KDA_MARK(6);
     }
+    if (n_chunks > 0 && prev_ok) store_out(n_chunks - 1);
 #ifdef KDA_PHASE_PROFILE
     if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
       for (int i = 0; i < 8; ++i) kda_phase_clocks[i] = prof_acc[i];
-      kda_phase_clocks[24] = n_chunks;
+      kda_phase_clocks[28] = n_chunks;
     }
 #endif
     if (!s_abort && args.final_state) {
@@ -370,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================== prep ==================================
+    regs_inc<kPrepRegs>();
     const int p = tid - kStateThreads;          // 0..255
     const int pw = p >> 5;                      // prep warp 0..7
     const int ta = pw & 3;                      // this warp's 16-token row tile
@@ -380,28 +396,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool loader = p == 128;               // issues the raw-tile TMA loads
     const __nv_bfloat16* __restrict__ gb = static_cast<const __nv_bfloat16*>(args.beta);
     float* Am = reinterpret_cast<float*>(smem + kOffA);
-    float* Tm = reinterpret_cast<float*>(smem + kOffT);
-    float* Xm = reinterpret_cast<float*>(smem + kOffX);
+    float* Dm = reinterpret_cast<float*>(smem + kOffD);      // [4][16][kLdB]  T_aa
+    float* Nm = reinterpret_cast<float*>(smem + kOffN);      // [6][16][kLdB]  T_aa A_ab
+    float* N2m = reinterpret_cast<float*>(smem + kOffN2);    // [3][16][kLdB]
+    float* N3m = reinterpret_cast<float*>(smem + kOffN3);    // [16][kLdB]
     float* tile_tot = reinterpret_cast<float*>(smem + kOffTileTot);  // [4][128]
-    float* fac = reinterpret_cast<float*>(smem + kOffFac);           // [4][3][128]
+    float* tabR = reinterpret_cast<float*>(smem + kOffTabR);  // e^{R_a}, e^{G_C - R_a}: [2][4][128]
 
     auto chunk_len = [&](int c) {
       const long long rem = t1 - (t0 + static_cast<long long>(c) * kC);
       return static_cast<int>(rem < kC ? rem : kC);
     };
-    // Raw q, k, v, g of chunk c: two 64-channel boxes each, by TMA.
+    // Raw k, q, g of chunk c (two 64-channel boxes each), by TMA.
     auto issue_raw = [&](int c) {
       const int s = c & 1;
       const int c0 = static_cast<int>(t0 + static_cast<long long>(c) * kC);
       uint64_t* bar = &s_bars[kBarRaw];
-      mbar_arrive_expect_tx(bar, 4 * 16384);
+      mbar_arrive_expect_tx(bar, 3 * 16384);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         tma_load_3d(smem + kOffRawK + hf * 8192, &tm_k, 64 * hf, h, c0, bar);
-        tma_load_3d(smem + kOffRawV + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
         tma_load_3d(smem + kOffQT + s * 16384 + hf * 8192, &tm_q, 64 * hf, h, c0, bar);
         tma_load_3d(smem + kOffKB + s * 16384 + hf * 8192, &tm_g, 64 * hf, h, c0, bar);
       }
+    };
+    // Raw v of chunk c straight into the V operand tile.
+    auto issue_raw_v = [&](int c) {
+      const int c0 = static_cast<int>(t0 + static_cast<long long>(c) * kC);
+      uint64_t* bar = &s_bars[kBarRawV];
+      mbar_arrive_expect_tx(bar, 16384);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(smem + kOffV + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
     };
     // beta of chunk c: the 16 threads of channel group 0 hold 4 rows each.
     float rb[4];
@@ -421,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
         issue_raw(0);
+        issue_raw_v(0);
       }
       load_beta(0);
     }
@@ -429,26 +456,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
       const int L = chunk_len(c);
+      // beta of this chunk to shared memory; the next chunk's load is in flight
+      // for the whole iteration.
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        if (cg == 0) s_beta[row0 + m] = rb[m];
+      if (c + 1 < n_chunks) load_beta(c + 1);
       const bool ok_raw = sync.wait(kBarRaw, c & 1);
       KDA_MARK(8);
       // Raw rows of this chunk (rows past the end of the sequence read as 0).
-      uint4 rq[4], rk[4], rgt[4], rv[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int r = row0 + m;
-        const uint32_t off = sw128_off(r, 8 * cg, 64);
-        if (r < L && ok_raw) {
-          rgt[m] = *reinterpret_cast<const uint4*>(smem + kOffKB + s * 16384 + off);
-          rq[m] = *reinterpret_cast<const uint4*>(smem + kOffQT + s * 16384 + off);
-          rk[m] = *reinterpret_cast<const uint4*>(smem + kOffRawK + off);
-          rv[m] = *reinterpret_cast<const uint4*>(smem + kOffRawV + off);
-        } else {
-          rgt[m] = rq[m] = rk[m] = rv[m] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // ---- P1: cumulative decay (log2 units) along the chunk, per channel.
+      uint4 rq[4], rk[4];
       float G[4][8];
       {
+        uint4 rgt[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int r = row0 + m;
+          const uint32_t off = sw128_off(r, 8 * cg, 64);
+          if (r < L && ok_raw) {
+            rgt[m] = *reinterpret_cast<const uint4*>(smem + kOffKB + s * 16384 + off);
+            rq[m] = *reinterpret_cast<const uint4*>(smem + kOffQT + s * 16384 + off);
+            rk[m] = *reinterpret_cast<const uint4*>(smem + kOffRawK + off);
+          } else {
+            rgt[m] = rq[m] = rk[m] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        // ---- P1: decay accumulated from the start of this 16-token tile
+        // (log2 units): G = cumsum(g) - R_ta, the exponent e1 and ei need.
         float gf[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -457,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 8; ++u) G[m][u] = (m ? G[m - 1][u] : 0.f) + gf[u] * kLog2e;
         }
       }
-      // Scan the four 4-row groups of this tile (lanes 8 apart), then across tiles.
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         float tot = G[3][u];
@@ -470,85 +503,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 0; m < 4; ++m) G[m][u] += excl;
         if (r4 == 3) tile_tot[ta * kD + 8 * cg + u] = tot;
       }
-      // Tile sums are visible, and every raw k / v read is done before the
+      // Tile sums are visible, and every raw k read is done before the
       // [K';Q'] tile is rewritten.
       named_bar(2, kPrepThreads);
-      float R[4][8], GC[8];
-      {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // ---- Per-(tile, channel) factors, once per chunk (thread p <-> channel p):
+      // e^{R_a}, e^{G_C - R_a}, the Khat block factors e^{R_{a2} - R_a}
+      // (a2 > a) and e^{G_C}.  Split layout: entry c of a 128-vector sits at
+      // (c & 4 ? 64 : 0) + 4 (c >> 3) + (c & 3), so the 16-byte reads of the
+      // row loop are conflict-free.
+      float* facs = reinterpret_cast<float*>(smem + kOffP + s * 8192);  // [6][128]
+      if (p < kD) {
+        const int cc = p;
+        const int sc = (cc & 4 ? 64 : 0) + 4 * (cc >> 3) + (cc & 3);
+        float tt[4], R[4], acc = 0.f;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) R[a][u] = acc[u];
-          const float4 t0v = *reinterpret_cast<const float4*>(&tile_tot[a * kD + 8 * cg]);
-          const float4 t1v = *reinterpret_cast<const float4*>(&tile_tot[a * kD + 8 * cg + 4]);
-          acc[0] += t0v.x; acc[1] += t0v.y; acc[2] += t0v.z; acc[3] += t0v.w;
-          acc[4] += t1v.x; acc[5] += t1v.y; acc[6] += t1v.z; acc[7] += t1v.w;
+          tt[a] = tile_tot[a * kD + cc];
+          R[a] = acc;
+          acc += tt[a];
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) GC[u] = acc[u];
+        for (int a = 0; a < 4; ++a) {
+          tabR[a * kD + sc] = ex2_fast(R[a]);
+          tabR[(4 + a) * kD + sc] = ex2_fast(acc - R[a]);
+        }
+        // factor rows: (a, a2) = (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        facs[0 * kD + sc] = ex2_fast(R[1] - R[0]);
+        facs[1 * kD + sc] = ex2_fast(R[2] - R[0]);
+        facs[2 * kD + sc] = ex2_fast(R[3] - R[0]);
+        facs[3 * kD + sc] = ex2_fast(R[2] - R[1]);
+        facs[4 * kD + sc] = ex2_fast(R[3] - R[1]);
+        facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
+        s_gamma[s][cc] = ex2_fast(acc);
       }
-      float Ra[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        Ra[u] = ta == 0 ? R[0][u] : ta == 1 ? R[1][u] : ta == 2 ? R[2][u] : R[3][u];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) G[m][u] += Ra[u];
-      }
+      named_bar(2, kPrepThreads);
+      KDA_MARK(15);
 
       // ---- P2: scaled operand tiles (packed fp32 pairs, one rounding each).
       {
         uint8_t* qt = smem + kOffQT + s * 16384;
         uint8_t* kb = smem + kOffKB + s * 16384;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int r = row0 + m;
-          *reinterpret_cast<uint4*>(smem + kOffV + sw128_off(r, 8 * cg, 64)) = rv[m];
-          if (cg == 0) s_beta[r] = rb[m];
-        }
-        uint64_t eR[4], eC[4], Rp[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          eR[w] = f2_pack(ex2_fast(Ra[2 * w]), ex2_fast(Ra[2 * w + 1]));
-          eC[w] = f2_pack(ex2_fast(GC[2 * w] - Ra[2 * w]), ex2_fast(GC[2 * w + 1] - Ra[2 * w + 1]));
-          Rp[w] = f2_pack(Ra[2 * w], Ra[2 * w + 1]);
-        }
-        // Khat factors for the later key blocks, e^{R_{a2} - R_ta} <= 1, shared
-        // by the warp (all its lanes are in tile ta).
-        if (r4 == 0) {
-#pragma unroll
-          for (int i = 0; i < 3; ++i) {
-            const int a2 = ta + 1 + i;
-            if (a2 < 4) {
-              float f8[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const float ra2 = a2 == 1 ? R[1][u] : a2 == 2 ? R[2][u] : R[3][u];
-                f8[u] = ex2_fast(ra2 - Ra[u]);
-              }
-              float* fr = fac + (ta * 3 + i) * kD + 8 * cg;
-              *reinterpret_cast<float4*>(fr) = make_float4(f8[0], f8[1], f8[2], f8[3]);
-              *reinterpret_cast<float4*>(fr + 4) = make_float4(f8[4], f8[5], f8[6], f8[7]);
-            }
-          }
-          if (ta == 0) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) s_gamma[s][8 * cg + u] = ex2_fast(GC[u]);
-          }
-        }
-        __syncwarp();
+        const int sc0 = 4 * cg;  // split-layout index of channels 8cg..8cg+3 (+64: 8cg+4..)
+        auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
+          const float4 lo = *reinterpret_cast<const float4*>(t + sc0);
+          const float4 hi = *reinterpret_cast<const float4*>(t + 64 + sc0);
+          o[0] = f2_pack(lo.x, lo.y);
+          o[1] = f2_pack(lo.z, lo.w);
+          o[2] = f2_pack(hi.x, hi.y);
+          o[3] = f2_pack(hi.z, hi.w);
+        };
+        uint64_t eR[4], eC[4];
+        ld8(tabR + ta * kD, eR);
+        ld8(tabR + (4 + ta) * kD, eC);
+        auto st4 = [&](uint32_t off_tile, int row, int rows, const uint32_t (&v)[4]) {
+          *reinterpret_cast<uint4*>(smem + off_tile + sw128_off(row, 8 * cg, rows)) =
+              make_uint4(v[0], v[1], v[2], v[3]);
+        };
+        uint64_t kh[4][4];   // Khat rows of this thread (fp32 pairs), for the later blocks
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int r = row0 + m, rl = 4 * r4 + m;
           const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
           const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
           uint32_t okp[4], oqp[4], okt[4], oqt[4], okh[4], okb[4];
-          uint64_t kh[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
-            float dx, dy;
-            f2_unpack(f2_sub(f2_pack(G[m][2 * w], G[m][2 * w + 1]), Rp[w]), dx, dy);
+            const float dx = G[m][2 * w], dy = G[m][2 * w + 1];
             const uint64_t e1 = f2_pack(ex2_fast(dx), ex2_fast(dy));    // e^{G - R_ta} <= 1
             const uint64_t ei = f2_pack(ex2_fast(-dx), ex2_fast(-dy));  // e^{R_ta - G} < e^80
             const uint64_t k1 = f2_mul(kp, e1), q1 = f2_mul(qp, e1);
@@ -556,14 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             oqp[w] = f2_to_bf16x2(q1);
             okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
             oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
-            kh[w] = f2_mul(kp, ei);
-            okh[w] = f2_to_bf16x2(kh[w]);
-            okb[w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
+            kh[m][w] = f2_mul(kp, ei);
+            okh[w] = f2_to_bf16x2(kh[m][w]);
+            okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
           }
-          auto st4 = [&](uint32_t off_tile, int row, int rows, const uint32_t (&v)[4]) {
-            *reinterpret_cast<uint4*>(smem + off_tile + sw128_off(row, 8 * cg, rows)) =
-                make_uint4(v[0], v[1], v[2], v[3]);
-          };
           st4(kOffKQ, 32 * ta + rl, 128, okp);
           st4(kOffKQ, 32 * ta + 16 + rl, 128, oqp);
           st4(kOffKT, r, 64, okt);
@@ -574,23 +591,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(kb + sw128_off(r, 8 * cg, 64)) =
                 make_uint4(okb[0], okb[1], okb[2], okb[3]);
           }
+        }
+        // Later key blocks a2 > ta: Khat e^{R_a2 - R_ta}.
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
-            if (ta + 1 + i < 4) {
-              const float* fr = fac + (ta * 3 + i) * kD + 8 * cg;
-              const float4 f0 = *reinterpret_cast<const float4*>(fr);
-              const float4 f1 = *reinterpret_cast<const float4*>(fr + 4);
-              const uint64_t fp[4] = {f2_pack(f0.x, f0.y), f2_pack(f0.z, f0.w),
-                                      f2_pack(f1.x, f1.y), f2_pack(f1.z, f1.w)};
+        for (int i = 0; i < 3; ++i) {
+          const int a2 = ta + 1 + i;
+          if (a2 < 4) {
+            const int frow = ta == 0 ? a2 - 1 : ta == 1 ? a2 + 1 : 5;
+            uint64_t f[4];
+            ld8(facs + frow * kD, f);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
               uint32_t ox[4];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[w], fp[w]));
-              st4(kOffKH, khat_row0(ta + 1 + i) + r, 160, ox);
+              for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[m][w], f[w]));
+              st4(kOffKH, khat_row0(a2) + row0 + m, 160, ox);
             }
           }
         }
       }
-      if (c + 1 < n_chunks) load_beta(c + 1);
       fence_async_smem();
       named_bar(2, kPrepThreads);
       KDA_MARK(9);
@@ -609,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok_ap = sync.wait(kBarAP, c & 1);
       KDA_MARK(10);
       tc_fence_after();
-      // Prefetch the next chunk's raw tiles: AP has read [K';Q'], and the
+      // Prefetch the next chunk's raw k, q, g: AP has read [K';Q'], and the
       // Qtil / Kbar slot of chunk c + 1 is free once the state pass of chunk
       // c - 1 has finished its last MMA.
       if (loader && c + 1 < n_chunks && ok_ap) {
@@ -642,14 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 16; ++u) v[u] = 0.f;
           }
           if (isP) {
-            if (ok_raw) {
 #pragma unroll
-              for (int h8 = 0; h8 < 2; ++h8) {
-                float f8[8];
+            for (int h8 = 0; h8 < 2; ++h8) {
+              float f8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
-                st_tile8(ptile, r, 16 * blk + 8 * h8, 64, f8);
-              }
+              for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
+              st_tile8(ptile, r, 16 * blk + 8 * h8, 64, f8);
             }
           } else {
 #pragma unroll
@@ -661,69 +678,180 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       named_bar(2, kPrepThreads);
-
       KDA_MARK(11);
-      // ---- P5: T = (I + A)^-1 in fp32; T' = T diag(beta) as bf16.
+
+      // ---- P5: T = (I + A)^-1 in fp32, written as T' = T diag(beta) in bf16.
+      // With D = blockdiag of the inverted 16 x 16 diagonal blocks and
+      // N = D (strictly block-lower part of A), T = (I - N + N^2 - N^3) D.
+      // Off-diagonal block pairs (a, b), a > b, are numbered
+      // (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5.  Block products are
+      // 16 x 16 x 16, one 4 x 4 output tile per thread.
       if (p < 64) {
+        // D_bb by forward substitution, one column per thread; the block's
+        // rows are loaded first so the substitution runs from registers.
         const int blk = p >> 4, jj = p & 15;
         const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
+        float ar[16][16];
+#pragma unroll
+        for (int rr = 1; rr < 16; ++rr)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (4 * q < rr) {
+              const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
+              ar[rr][4 * q] = v.x; ar[rr][4 * q + 1] = v.y;
+              ar[rr][4 * q + 2] = v.z; ar[rr][4 * q + 3] = v.w;
+            }
+          }
         float x[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
-          float acc = 0.f;
+          float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < rr; ++i) acc = fmaf(Ab[rr * kLdA + i], x[i], acc);
-          x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -acc);
+          for (int i = 0; i < rr; ++i) {
+            if (i & 1) acc1 = fmaf(ar[rr][i], x[i], acc1);
+            else acc0 = fmaf(ar[rr][i], x[i], acc0);
+          }
+          x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -(acc0 + acc1));
         }
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * kLdA + 16 * blk + jj] = x[rr];
+        for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = x[rr];
+      } else {
+        // Zero the blocks of T' strictly above the diagonal (192 vectors).
+        for (int e = p - 64; e < 192; e += kPrepThreads - 64) {
+          const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+          const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
+          const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
+          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          st_tile8(smem + kOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
+        }
       }
       named_bar(2, kPrepThreads);
-#pragma unroll 1
-      for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        const int bi = p >> 6, b = bi, a = b + d, rr = (p >> 2) & 15, q = p & 3;
-        if (bi < nb) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int cc = b; cc < a; ++cc) {
-            const float* arow = Am + (16 * a + rr) * kLdA + 16 * cc;
-            const float* tcol = Tm + (16 * cc) * kLdA + 16 * b + 4 * q;
+      KDA_MARK(16);
+      // acc[i][j] += X[4 i4 + i][k] Y[k][4 j4 + j], k = 0..15, X rows xstride
+      // apart, Y rows ystride apart (Y rows 16-byte aligned).
+      // acc[i][j] += X[4 i4 + i][k] Y[k][4 j4 + j], k = 0..15; both operands are
+      // loaded (16-byte rows) before the FMAs.
+      auto tile16 = [&](const float* X, int xs, const float* Y, int ys, int i4, int j4,
+                        float (&acc)[4][4]) {
+        float4 yv[16], xv[4][4];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const float av = arow[u];
-              const float4 tv = *reinterpret_cast<const float4*>(tcol + u * kLdA);
-              acc.x = fmaf(av, tv.x, acc.x); acc.y = fmaf(av, tv.y, acc.y);
-              acc.z = fmaf(av, tv.z, acc.z); acc.w = fmaf(av, tv.w, acc.w);
-            }
+        for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float4*>(Y + k * ys + 4 * j4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            xv[i][q] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 xq = xv[i][k >> 2];
+            const float xk = (k & 3) == 0 ? xq.x : (k & 3) == 1 ? xq.y : (k & 3) == 2 ? xq.z : xq.w;
+            acc[i][0] = fmaf(xk, yv[k].x, acc[i][0]);
+            acc[i][1] = fmaf(xk, yv[k].y, acc[i][1]);
+            acc[i][2] = fmaf(xk, yv[k].z, acc[i][2]);
+            acc[i][3] = fmaf(xk, yv[k].w, acc[i][3]);
           }
-          *reinterpret_cast<float4*>(&Xm[(bi * 16 + rr) * 20 + 4 * q]) = acc;
         }
-        named_bar(2, kPrepThreads);
-        if (bi < nb) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float* trow = Tm + (16 * a + rr) * kLdA + 16 * a;
+      };
+      auto store_tile = [&](float* Z, int i4, int j4, const float (&acc)[4][4]) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float tv = trow[u];
-            const float4 xv = *reinterpret_cast<const float4*>(&Xm[(bi * 16 + u) * 20 + 4 * q]);
-            acc.x = fmaf(tv, xv.x, acc.x); acc.y = fmaf(tv, xv.y, acc.y);
-            acc.z = fmaf(tv, xv.z, acc.z); acc.w = fmaf(tv, xv.w, acc.w);
-          }
-          *reinterpret_cast<float4*>(&Tm[(16 * a + rr) * kLdA + 16 * b + 4 * q]) =
-              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        named_bar(2, kPrepThreads);
-      }
-#pragma unroll
-      for (int e = p; e < 64 * 8; e += kPrepThreads) {
-        const int r = e >> 3, i0 = (e & 7) * 8;
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(Z + (4 * i4 + i) * kLdB + 4 * j4) =
+              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      };
+      const int tq = p & 15, i4 = tq >> 2, j4 = tq & 3;
+      // Step 1: N_ab = D_aa A_ab (96 threads); diagonal blocks of T' (128 threads).
+      if (p < 96) {
+        const int blk = p >> 4;
+        const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
+        const int b = blk - (a * (a - 1)) / 2;
+        float acc[4][4] = {};
+        tile16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, i4, j4, acc);
+        store_tile(Nm + blk * 16 * kLdB, i4, j4, acc);
+      } else if (p >= 128) {
+        const int e = p - 128, a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
         float f8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u;
-          f8[u] = (i >> 4) <= (r >> 4) ? Tm[r * kLdA + i] * s_beta[i] : 0.f;
+          const int cc = 8 * h8 + u;
+          f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
         }
-        st_tile8(smem + kOffTB, r, i0, 64, f8);
+        st_tile8(smem + kOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
+      }
+      named_bar(2, kPrepThreads);
+      KDA_MARK(17);
+      // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
+      if (p < 48) {
+        const int k2 = p >> 4;
+        float acc[4][4] = {};
+        const int xa = k2 == 0 ? 2 : k2 == 1 ? 5 : 4, ya = k2 == 0 ? 0 : k2 == 1 ? 2 : 0;
+        tile16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, i4, j4, acc);
+        if (k2 == 2) tile16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, i4, j4, acc);
+        store_tile(N2m + k2 * 16 * kLdB, i4, j4, acc);
+      }
+      named_bar(2, kPrepThreads);
+      KDA_MARK(18);
+      // Step 3: N^3 block (3,0) = N32 (N^2)_20 (16 threads), and M = -N + N^2
+      // in place of N for blocks (1,0) (2,0) (2,1) (3,1); N32, which the N^3
+      // threads read, is negated in step 4 and M_30 is finished there too.
+      if (p < 16) {
+        float acc[4][4] = {};
+        tile16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, i4, j4, acc);
+        store_tile(N3m, i4, j4, acc);
+      } else if (p >= 32) {
+        for (int e = p - 32; e < 4 * 64; e += kPrepThreads - 32) {
+          const int bsel = e >> 6;                          // blocks 0, 1, 2, 4
+          const int blk = bsel < 3 ? bsel : 4;
+          const int k2 = blk == 1 ? 0 : blk == 4 ? 1 : -1;
+          const int row = (e >> 2) & 15, q = e & 3;
+          float4* nv = reinterpret_cast<float4*>(Nm + (blk * 16 + row) * kLdB + 4 * q);
+          float4 m = *nv;
+          m.x = -m.x; m.y = -m.y; m.z = -m.z; m.w = -m.w;
+          if (k2 >= 0) {
+            const float4 n2 = *reinterpret_cast<const float4*>(N2m + (k2 * 16 + row) * kLdB + 4 * q);
+            m.x += n2.x; m.y += n2.y; m.z += n2.z; m.w += n2.w;
+          }
+          *nv = m;
+        }
+      }
+      named_bar(2, kPrepThreads);
+      KDA_MARK(19);
+      // Step 4: T_ab = M_ab D_bb, times beta, into T' (M_30 = -N30 + N^2_30 - N^3_30).
+      if (p < 96) {
+        const int blk = p >> 4;
+        const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
+        const int b = blk - (a * (a - 1)) / 2;
+        if (blk == 3) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = 4 * i4 + i;
+            float4* nv = reinterpret_cast<float4*>(Nm + (3 * 16 + row) * kLdB + 4 * j4);
+            const float4 n2 = *reinterpret_cast<const float4*>(N2m + (2 * 16 + row) * kLdB + 4 * j4);
+            const float4 n3 = *reinterpret_cast<const float4*>(N3m + row * kLdB + 4 * j4);
+            float4 m = *nv;
+            m.x = n2.x - m.x - n3.x; m.y = n2.y - m.y - n3.y;
+            m.z = n2.z - m.z - n3.z; m.w = n2.w - m.w - n3.w;
+            *nv = m;
+          }
+          __syncwarp(0x0000FFFFu << (16 * (lane >> 4)));
+        }
+        float acc[4][4] = {};
+        tile16(Nm + blk * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, i4, j4, acc);
+        if (blk == 5) {   // M_32 = -N_32
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jq = 0; jq < 4; ++jq) acc[i][jq] = -acc[i][jq];
+        }
+        const float4 bv = *reinterpret_cast<const float4*>(&s_beta[16 * b + 4 * j4]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint2 pk = make_uint2(pack2(acc[i][0] * bv.x, acc[i][1] * bv.y),
+                                      pack2(acc[i][2] * bv.z, acc[i][3] * bv.w));
+          *reinterpret_cast<uint2*>(smem + kOffTB +
+                                    sw128_off(16 * a + 4 * i4 + i, 16 * b + 4 * j4, 64)) = pk;
+        }
       }
       fence_async_smem();
       named_bar(2, kPrepThreads);
@@ -732,7 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P6: W^T = Ktil^T T'^T and U0^T = V^T T'^T (U0 goes where the state
       // pass accumulates U, once it has read the previous chunk's U).
       const bool ok_u = c < 1 || sync.wait(kBarUFree, (c - 1) & 1);
-      if (leader && ok_u && !s_abort) {
+      const bool ok_v = sync.wait(kBarRawV, c & 1);
+      if (leader && ok_u && ok_v && !s_abort) {
         tc_fence_after();
         const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
         const uint32_t aKT = smem_u32(smem + kOffKT), aV = smem_u32(smem + kOffV),
@@ -746,6 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s_bars[kBarWU]);
       }
       const bool ok_wu = sync.wait(kBarWU, c & 1);
+      // The V tile is free: fetch the next chunk's v.
+      if (loader && c + 1 < n_chunks && ok_wu) issue_raw_v(c + 1);
       // -W^T may overwrite the shared tile once the state pass's first MMA of
       // the previous chunk is done.
       const bool ok_m1 = c < 1 || sync.wait(kBarMMA1, (c - 1) & 1);
@@ -777,7 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #ifdef KDA_PHASE_PROFILE
     if (blockIdx.x == 0 && blockIdx.y == 0 && p == 0)
-      for (int i = 8; i < 16; ++i) kda_phase_clocks[i] = prof_acc[i];
+      for (int i = 8; i < 24; ++i) kda_phase_clocks[i] = prof_acc[i];
+    if (blockIdx.x == 0 && blockIdx.y == 0 && p == 0) kda_phase_clocks[28] = n_chunks;
 #endif
   }
 
