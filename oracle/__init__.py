@@ -50,6 +50,9 @@ def _load():
             lib.kda_oracle_prefill.argtypes = [vp, vp, vp, vp, vp, ip, dp, dp, ip, ip, ip, ip,
                                                dp, dp, ip]
             lib.kda_oracle_prefill.restype = ip
+            lib.kda_oracle_prefill_ckpt.argtypes = [vp, vp, vp, vp, vp, ip, dp, dp, ip, ip, ip,
+                                                    ip, dp, dp, dp, dp, ctypes.c_longlong, ip]
+            lib.kda_oracle_prefill_ckpt.restype = ip
             lib.kda_oracle_decode.argtypes = [vp, vp, vp, vp, vp, ip, dp, ip, ip, ip, ip, dp, ip]
             lib.kda_oracle_decode.restype = ip
             lib.kda_oracle_default_threads.restype = ip
@@ -104,12 +107,23 @@ def _state_f64(s, shape):
     return s
 
 
-def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0):
+def checkpoint_offsets(cu_seqlens, interval: int):
+    """Row offsets of each sequence's checkpoints: sequence n owns
+    floor(len_n / interval) rows starting at offsets[n]."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    counts = (cu[1:] - cu[:-1]) // int(interval)
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+
+
+def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0,
+            ckpt_interval: int = 0):
     """Token-by-token fp64 KDA over packed sequences.
 
     q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; init_state: [N, H, dk, dv]
     or None (zeros); cu_seqlens: [N+1] offsets or None (one sequence).
-    Returns (out [T, H, dv] fp64, final_state [N, H, dk, dv] fp64).
+    Returns (out [T, H, dv] fp64, final_state [N, H, dk, dv] fp64), plus the
+    checkpoints [n_ckpt, H, dk, dv] (state after every ckpt_interval tokens of
+    each sequence, rows laid out by checkpoint_offsets) when ckpt_interval > 0.
     """
     arrs = [_as_host(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"))]
     codes = {c for _, c in arrs}
@@ -136,13 +150,20 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0
     s0 = _state_f64(init_state, (N, H, dk, dv))
     out = np.zeros((T, H, dv), dtype=np.float64)
     fin = np.zeros((N, H, dk, dv), dtype=np.float64)
-    rc = _load().kda_oracle_prefill(
+    ck = offs = None
+    if ckpt_interval:
+        offs = checkpoint_offsets(cu, ckpt_interval)
+        ck = np.zeros((int(offs[-1]), H, dk, dv), dtype=np.float64)
+    rc = _load().kda_oracle_prefill_ckpt(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, ga.ctypes.data, ba.ctypes.data, dt,
         None if s0 is None else s0.ctypes.data, cu.ctypes.data, N, H, dk, dv,
-        out.ctypes.data, fin.ctypes.data, int(threads))
+        out.ctypes.data, fin.ctypes.data, None if ck is None else ck.ctypes.data,
+        None if offs is None else offs.ctypes.data, int(ckpt_interval), int(threads))
     if rc < 0:
         raise RuntimeError(f"kda_oracle_prefill failed ({rc})")
     prefill.last_threads = rc
+    if ckpt_interval:
+        return out, fin, ck
     return out, fin
 
 

@@ -57,6 +57,9 @@ typedef struct {
   int n_seqs, heads, dk, dv;
   double* out;              /* [T_total, H, dv] */
   double* final_state;      /* nullable */
+  double* checkpoints;      /* nullable: [n_ckpt, H, dk, dv] */
+  const long long* ckpt_offsets; /* [n_seqs + 1] when checkpoints != NULL */
+  long long ckpt_interval;  /* tokens between checkpoints */
   int next_job;             /* shared work counter */
 } orc_job_t;
 
@@ -98,6 +101,13 @@ static void orc_run_pair(const orc_job_t* J, int n, int h, double* S, double* kk
     for (int c = 0; c < dk; ++c)
       for (int j = 0; j < dv; ++j) u[j] += S[c * dv + j] * qq[c];
     memcpy(J->out + rv, u, sizeof(double) * dv);
+
+    /* Prefix-cache checkpoint: the state after every ckpt_interval tokens. */
+    const long long done = t - J->cu_seqlens[n] + 1;
+    if (J->checkpoints && done % J->ckpt_interval == 0) {
+      const long long row = J->ckpt_offsets[n] + done / J->ckpt_interval - 1;
+      memcpy(J->checkpoints + (row * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+    }
   }
   if (J->final_state) memcpy(J->final_state + state_off, S, sizeof(double) * dk * dv);
 }
@@ -128,20 +138,27 @@ int kda_oracle_default_threads(void) {
 }
 
 /*
- * Prefill over packed sequences.  Returns the number of threads used, or a
- * negative value on bad arguments / allocation failure.
+ * Prefill over packed sequences, optionally also writing the state after every
+ * ckpt_interval tokens of each sequence (the prefix-cache checkpoints of the
+ * paper review's serving description): checkpoint k of sequence n (state after
+ * (k+1) * ckpt_interval tokens) is row ckpt_offsets[n] + k of `checkpoints`.
+ * Returns the number of threads used, or a negative value on bad arguments /
+ * allocation failure.
  */
-int kda_oracle_prefill(const void* q, const void* k, const void* v, const void* g,
-                       const void* beta, int dtype, const double* init_state,
-                       const long long* cu_seqlens, int n_seqs, int heads, int dk, int dv,
-                       double* out, double* final_state, int n_threads) {
+int kda_oracle_prefill_ckpt(const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, int dtype, const double* init_state,
+                            const long long* cu_seqlens, int n_seqs, int heads, int dk, int dv,
+                            double* out, double* final_state, double* checkpoints,
+                            const long long* ckpt_offsets, long long ckpt_interval,
+                            int n_threads) {
   if (!q || !k || !v || !g || !beta || !cu_seqlens || !out) return -1;
   if (n_seqs < 0 || heads <= 0 || dk <= 0 || dv <= 0) return -1;
   if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F64) return -1;
   for (int n = 0; n < n_seqs; ++n)
     if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+  if (checkpoints && (!ckpt_offsets || ckpt_interval <= 0)) return -1;
   orc_job_t J = {q, k, v, g, beta, dtype, init_state, cu_seqlens, n_seqs, heads, dk, dv,
-                 out, final_state, 0};
+                 out, final_state, checkpoints, ckpt_offsets, ckpt_interval, 0};
   const int n_jobs = n_seqs * heads;
   if (n_threads <= 0) n_threads = kda_oracle_default_threads();
   if (n_threads > n_jobs) n_threads = n_jobs > 0 ? n_jobs : 1;
@@ -159,6 +176,15 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, const void* 
   }
   free(th);
   return failed ? -2 : (started ? started : 1);
+}
+
+/* Prefill over packed sequences without checkpoints. */
+int kda_oracle_prefill(const void* q, const void* k, const void* v, const void* g,
+                       const void* beta, int dtype, const double* init_state,
+                       const long long* cu_seqlens, int n_seqs, int heads, int dk, int dv,
+                       double* out, double* final_state, int n_threads) {
+  return kda_oracle_prefill_ckpt(q, k, v, g, beta, dtype, init_state, cu_seqlens, n_seqs, heads,
+                                 dk, dv, out, final_state, NULL, NULL, 0, n_threads);
 }
 
 /*

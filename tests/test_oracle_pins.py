@@ -264,3 +264,27 @@ def test_generator_recipe_shapes_and_norms():
     assert float((nrm - 1).abs().max()) < 2e-2
     b = d["beta"].float()
     assert float(b.min()) > 0 and float(b.max()) < 1
+
+
+def test_checkpoints_equal_prefix_final_states():
+    """A checkpoint after j * interval tokens is the final state of the prefix
+    [start, start + j * interval) of its sequence, with the same initial state."""
+    rng = np.random.default_rng(20)
+    lens, interval = [20, 7, 16, 0, 33], 8
+    T, H, dk, dv = sum(lens), 2, 5, 4
+    q, k, v, g, beta = _rand_case(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    cu = np.cumsum([0] + lens)
+    out, fin, ck = oracle.prefill(q, k, v, g, beta, init_state=S0, cu_seqlens=cu,
+                                  ckpt_interval=interval)
+    offs = oracle.checkpoint_offsets(cu, interval)
+    assert list(np.diff(offs)) == [n // interval for n in lens]
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        for j in range(1, (b - a) // interval + 1):
+            e = a + j * interval
+            _, f = oracle.prefill(q[a:e], k[a:e], v[a:e], g[a:e], beta[a:e],
+                                  init_state=S0[n:n + 1])
+            np.testing.assert_array_equal(ck[offs[n] + j - 1], f[0])
+    # outputs are unchanged by asking for checkpoints
+    o2, f2 = oracle.prefill(q, k, v, g, beta, init_state=S0, cu_seqlens=cu)
+    assert np.array_equal(o2, out) and np.array_equal(f2, fin)
