@@ -278,7 +278,35 @@ def run_gpu(args):
     barrier()
     e2e_ms = max_over_ranks(start.elapsed_time(end)) / e2e_steps
     e2e_value = job_throughput(world, T, e2e_ms) / 1e6
-    del host_in, dev_in, host_out, host_fin, d, args_pf, out, fin
+    del host_in, dev_in, host_out, host_fin
+
+    # ------- prefill that also writes prefix-cache checkpoints every 512 tokens -------
+    ck_int = 512
+    ck_offs = torch.tensor(kda.checkpoint_offsets([T], ck_int), dtype=torch.int32, device=dev)
+    ck_buf = torch.empty((T // ck_int, H, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def ckpt_step():
+        kda.chunk_fwd(*args_pf, d["init_state"], None, chunk=w.chunk, out=out, final_state=fin,
+                      ckpt_interval=ck_int, ckpt_offsets=ck_offs, checkpoints=ck_buf)
+
+    for _ in range(3):
+        ckpt_step()
+    barrier()
+    ck_steps = max(1, min(args.steps, 20))
+    start.record(stream)
+    for _ in range(ck_steps):
+        ckpt_step()
+    end.record(stream)
+    barrier()
+    ck_ms = max_over_ranks(start.elapsed_time(end)) / ck_steps
+    ck_bytes = alg_bytes + ck_buf.numel() * 4
+    ckpt = {"interval": ck_int, "value": job_throughput(world, T, ck_ms) / 1e6,
+            "unit": "Mtok/s", "ms_per_step": ck_ms, "steps": ck_steps,
+            "overhead_vs_plain": ck_ms / ms_step - 1.0,
+            "algorithmic_bytes_per_launch": ck_bytes,
+            "achieved_gbs": ck_bytes / (ck_ms * 1e-3) / 1e9,
+            "frac": ck_bytes / (ck_ms * 1e-3) / 1e9 / hbm_peak}
+    del d, args_pf, out, fin, ck_buf, ck_offs
     torch.cuda.empty_cache()
     if args.only == "prefill":
         return
@@ -344,6 +372,7 @@ def run_gpu(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * 1,
             "clocks": clocks,
+            "prefill_checkpoints": ckpt,
             "decode": {"workload": DECODE, "value": job_throughput(world, N, dec_ms),
                        "unit": "tok/s", "ms_per_step": dec_ms, "steps": wd.decode_steps,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,

@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
+__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libkda.so"
@@ -68,6 +68,9 @@ def load():
             lib.kda_status_string.argtypes = [ip]
             lib.kda_status_string.restype = ctypes.c_char_p
             lib.kda_version.restype = ip
+            lib.kda_chunk_fwd_checkpoints.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp,
+                                                      vp, sz, vp, vp, vp, vp, ip]
+            lib.kda_chunk_fwd_checkpoints.restype = ip
             lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
             lib.kda_chunk_fwd_algorithm.restype = ip
             _lib = lib
@@ -115,15 +118,31 @@ def algorithm(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=6
     return {0: "recurrent", 1: "tcgen05"}[rc]
 
 
+def checkpoint_offsets(lengths, interval: int) -> list:
+    """Checkpoint row offsets for host-side sequence lengths: sequence n owns
+    floor(len_n / interval) rows starting at offsets[n]."""
+    offs = [0]
+    for n in lengths:
+        offs.append(offs[-1] + int(n) // int(interval))
+    return offs
+
+
 def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 64, *,
               n_seqs: int | None = None, out=None, final_state=None,
-              output_final_state: bool = True, workspace=None, dev_status=None, stream=None):
+              output_final_state: bool = True, workspace=None, dev_status=None, stream=None,
+              ckpt_interval: int = 0, ckpt_offsets=None, checkpoints=None):
     """Chunkwise KDA prefill over packed sequences (``kda_chunk_fwd``).
 
     q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H] (fp32 or bf16, one dtype,
     on one CUDA device).  init_state: [N, H, dk, dv] fp32 or None (zeros).
     cu_seqlens: int32 [N+1] on the device, or None for ``n_seqs`` (default 1)
     equal-length sequences.  Returns (out [T, H, dv], final_state or None).
+
+    With ckpt_interval > 0 (a multiple of 64) it calls
+    ``kda_chunk_fwd_checkpoints`` and returns (out, final_state, checkpoints):
+    the state after every ckpt_interval tokens of each sequence, rows laid out
+    by ckpt_offsets (int32 [N+1] on the device; computed from cu_seqlens when
+    not given, which reads the lengths back to the host).
     """
     lib = load()
     if q.dim() != 3:
@@ -158,6 +177,25 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 6
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if ckpt_interval:
+        if ckpt_offsets is None:
+            lens = ([T // N] * N if cu_seqlens is None
+                    else (cu_seqlens[1:] - cu_seqlens[:-1]).tolist())
+            ckpt_offsets = torch.tensor(checkpoint_offsets(lens, ckpt_interval),
+                                        dtype=torch.int32, device=dev)
+        _check_input("ckpt_offsets", ckpt_offsets, (N + 1,), torch.int32, dev)
+        if checkpoints is None:
+            n_ck = int(ckpt_offsets[-1].item())
+            checkpoints = torch.empty((max(n_ck, 1), H, dk, dv), dtype=torch.float32, device=dev)
+        with torch.cuda.device(dev):
+            rc = lib.kda_chunk_fwd_checkpoints(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                _ptr(cu_seqlens), _ptr(out), _ptr(final_state), int(chunk), ctypes.byref(d),
+                _ptr(workspace), ws_bytes, _ptr(dev_status), _stream_handle(stream),
+                _ptr(checkpoints), _ptr(ckpt_offsets), int(ckpt_interval))
+        if rc != 0:
+            raise KDAError(rc, "kda_chunk_fwd_checkpoints")
+        return out, final_state, checkpoints
     with torch.cuda.device(dev):
         rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
                                _ptr(cu_seqlens), _ptr(out), _ptr(final_state), int(chunk),

@@ -79,15 +79,26 @@ int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk) {
   return kda::chunk_tc_supported(a) ? KDA_ALGO_TCGEN05 : KDA_ALGO_RECURRENT;
 }
 
-int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
-                  const float* init_state, const int* cu_seqlens, void* out, float* final_state,
-                  int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
-                  int* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// kda_chunk_fwd with optional prefix-cache checkpoints (ckpt == nullptr: none).
+int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                   const float* init_state, const int* cu_seqlens, void* out, float* final_state,
+                   int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                   int* dev_status, void* stream, float* ckpt, const int* ckpt_offsets,
+                   int ckpt_interval) {
   int rc = check_dims(dims);
   if (rc != KDA_OK) return rc;
   if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
   rc = check_io_pointers(q, k, v, g, beta, out, dims);
   if (rc != KDA_OK) return rc;
+  if (ckpt) {
+    if (!ckpt_offsets || ckpt_interval <= 0) return KDA_ERR_INVALID;
+    if (ckpt_interval % 64 != 0) return KDA_ERR_UNSUPPORTED;
+    if (!aligned(ckpt, 16)) return KDA_ERR_ALIGNMENT;
+  }
   const int N = dims->n_seqs;
   if (N == 0 || dims->heads == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
   long long seq_len = 0;
@@ -113,6 +124,9 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, co
   a.dev_status = dev_status;
   a.n_seqs = N; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
   a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
+  a.ckpt = ckpt;
+  a.ckpt_offsets = ckpt ? ckpt_offsets : nullptr;
+  a.ckpt_interval = ckpt ? ckpt_interval : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (need > 0 && cu_seqlens) {
@@ -126,6 +140,30 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, co
   else
     e = kda::launch_recurrent(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                  const float* init_state, const int* cu_seqlens, void* out, float* final_state,
+                  int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                  int* dev_status, void* stream) {
+  return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
+                        workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, 0);
+}
+
+int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const float* init_state, const int* cu_seqlens,
+                              void* out, float* final_state, int chunk, const kda_dims* dims,
+                              void* workspace, size_t workspace_bytes, int* dev_status,
+                              void* stream, float* checkpoints, const int* ckpt_offsets,
+                              int ckpt_interval) {
+  if (!checkpoints) return KDA_ERR_INVALID;
+  return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
+                        workspace, workspace_bytes, dev_status, stream, checkpoints, ckpt_offsets,
+                        ckpt_interval);
 }
 
 int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,

@@ -339,12 +339,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       KDA_MARK(4);
       tc_fence_after();
       if (ok2) {
+        // Prefix-cache checkpoint after this chunk (full chunks whose end is a
+        // multiple of the checkpoint interval).
+        const long long done = static_cast<long long>(c + 1) * kC;
+        float* ck = nullptr;
+        if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
+          const long long row = args.ckpt_offsets[n] + done / args.ckpt_interval - 1;
+          ck = args.ckpt + (row * H + h) * kD * kD + j;
+        }
         // New state -> bf16 operand copy; O^T column j -> row-major staging.
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float v[32];
           tmem_ld32(tbase + lane_base + kColS + 32 * cb, v);
           tmem_ld_wait();
+          if (ck) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) __stcs(ck + (32 * cb + u) * kD, v[u]);
+          }
           uint32_t b[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);

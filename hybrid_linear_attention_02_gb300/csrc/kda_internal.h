@@ -21,6 +21,9 @@ struct LaunchArgs {
   int* dev_status;          // nullable
   int n_seqs, heads, dk, dv, dtype, chunk;
   long long total_tokens;
+  float* ckpt;              // nullable: state after every ckpt_interval tokens
+  const int* ckpt_offsets;  // [n_seqs + 1] first checkpoint row of each sequence
+  int ckpt_interval;        // tokens between checkpoints (multiple of 64) or 0
 };
 
 // fp32 CUDA-core kernel that walks the recurrence token by token with the

@@ -49,7 +49,9 @@ __device__ __forceinline__ void store_out4<__nv_bfloat16>(__nv_bfloat16* p, long
   *reinterpret_cast<uint2*>(p + i) = pk;
 }
 
-template <int DK, int DV, typename T>
+// kCkpt: also write the prefix-cache checkpoints (a separate instantiation,
+// so the prefill and decode code without them carries no extra test).
+template <int DK, int DV, typename T, bool kCkpt>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
   constexpr int CG = DV / 4;       // float4 column groups
   constexpr int RG = kThreads / CG;  // row groups
@@ -92,61 +94,81 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
     for (int m = 0; m < RPT; ++m) S[m] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  for (long long t = t0; t < t1; ++t) {
-    const int b = static_cast<int>((t - t0) & 1);
-    const long long rk = (t * a.heads + h) * DK, rv = (t * a.heads + h) * DV;
-    for (int c = tid; c < DK; c += kThreads) {
-      s_q[b][c] = load_in(q, rk + c);
-      s_k[b][c] = load_in(k, rk + c);
-      s_a[b][c] = expf(load_in(g, rk + c));
-    }
-    for (int j = tid; j < DV; j += kThreads) s_v[b][j] = load_in(v, rv + j);
-    if (tid == 0) s_b[b] = load_in(beta, t * a.heads + h);
-    __syncthreads();
+  // Tokens [s0, s1) of the sequence, one at a time.
+  auto run = [&](long long s0, long long s1) {
+    for (long long t = s0; t < s1; ++t) {
+      const int b = static_cast<int>((t - t0) & 1);
+      const long long rk = (t * a.heads + h) * DK, rv = (t * a.heads + h) * DV;
+      for (int c = tid; c < DK; c += kThreads) {
+        s_q[b][c] = load_in(q, rk + c);
+        s_k[b][c] = load_in(k, rk + c);
+        s_a[b][c] = expf(load_in(g, rk + c));
+      }
+      for (int j = tid; j < DV; j += kThreads) s_v[b][j] = load_in(v, rv + j);
+      if (tid == 0) s_b[b] = load_in(beta, t * a.heads + h);
+      __syncthreads();
 
-    float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pp = pu;
-    float pqk = 0.f;
+      float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pp = pu;
+      float pqk = 0.f;
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const int c = rg + RG * m;
-      const float al = s_a[b][c], kc = s_k[b][c], qc = s_q[b][c];
-      S[m].x *= al; S[m].y *= al; S[m].z *= al; S[m].w *= al;
-      pu.x = fmaf(S[m].x, kc, pu.x); pu.y = fmaf(S[m].y, kc, pu.y);
-      pu.z = fmaf(S[m].z, kc, pu.z); pu.w = fmaf(S[m].w, kc, pu.w);
-      pp.x = fmaf(S[m].x, qc, pp.x); pp.y = fmaf(S[m].y, qc, pp.y);
-      pp.z = fmaf(S[m].z, qc, pp.z); pp.w = fmaf(S[m].w, qc, pp.w);
-      pqk = fmaf(qc, kc, pqk);
-    }
-    *reinterpret_cast<float4*>(&s_ru[b][rg][4 * cg]) = pu;
-    *reinterpret_cast<float4*>(&s_rp[b][rg][4 * cg]) = pp;
-    if (cg == 0) s_rqk[b][rg] = pqk;
-    __syncthreads();
+      for (int m = 0; m < RPT; ++m) {
+        const int c = rg + RG * m;
+        const float al = s_a[b][c], kc = s_k[b][c], qc = s_q[b][c];
+        S[m].x *= al; S[m].y *= al; S[m].z *= al; S[m].w *= al;
+        pu.x = fmaf(S[m].x, kc, pu.x); pu.y = fmaf(S[m].y, kc, pu.y);
+        pu.z = fmaf(S[m].z, kc, pu.z); pu.w = fmaf(S[m].w, kc, pu.w);
+        pp.x = fmaf(S[m].x, qc, pp.x); pp.y = fmaf(S[m].y, qc, pp.y);
+        pp.z = fmaf(S[m].z, qc, pp.z); pp.w = fmaf(S[m].w, qc, pp.w);
+        pqk = fmaf(qc, kc, pqk);
+      }
+      *reinterpret_cast<float4*>(&s_ru[b][rg][4 * cg]) = pu;
+      *reinterpret_cast<float4*>(&s_rp[b][rg][4 * cg]) = pp;
+      if (cg == 0) s_rqk[b][rg] = pqk;
+      __syncthreads();
 
-    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), p = u;
-    float qk = 0.f;
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f), p = u;
+      float qk = 0.f;
 #pragma unroll
-    for (int r = 0; r < RG; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(&s_ru[b][r][4 * cg]);
-      const float4 y = *reinterpret_cast<const float4*>(&s_rp[b][r][4 * cg]);
-      u.x += x.x; u.y += x.y; u.z += x.z; u.w += x.w;
-      p.x += y.x; p.y += y.y; p.z += y.z; p.w += y.w;
-      qk += s_rqk[b][r];
-    }
-    const float bt = s_b[b];
-    const float4 vv = *reinterpret_cast<const float4*>(&s_v[b][4 * cg]);
-    const float4 d = make_float4(bt * (vv.x - u.x), bt * (vv.y - u.y), bt * (vv.z - u.z),
-                                 bt * (vv.w - u.w));
+      for (int r = 0; r < RG; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(&s_ru[b][r][4 * cg]);
+        const float4 y = *reinterpret_cast<const float4*>(&s_rp[b][r][4 * cg]);
+        u.x += x.x; u.y += x.y; u.z += x.z; u.w += x.w;
+        p.x += y.x; p.y += y.y; p.z += y.z; p.w += y.w;
+        qk += s_rqk[b][r];
+      }
+      const float bt = s_b[b];
+      const float4 vv = *reinterpret_cast<const float4*>(&s_v[b][4 * cg]);
+      const float4 d = make_float4(bt * (vv.x - u.x), bt * (vv.y - u.y), bt * (vv.z - u.z),
+                                   bt * (vv.w - u.w));
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const float kc = s_k[b][rg + RG * m];
-      S[m].x = fmaf(kc, d.x, S[m].x); S[m].y = fmaf(kc, d.y, S[m].y);
-      S[m].z = fmaf(kc, d.z, S[m].z); S[m].w = fmaf(kc, d.w, S[m].w);
+      for (int m = 0; m < RPT; ++m) {
+        const float kc = s_k[b][rg + RG * m];
+        S[m].x = fmaf(kc, d.x, S[m].x); S[m].y = fmaf(kc, d.y, S[m].y);
+        S[m].z = fmaf(kc, d.z, S[m].z); S[m].w = fmaf(kc, d.w, S[m].w);
+      }
+      if (rg == 0) {
+        const float4 o = make_float4(fmaf(qk, d.x, p.x), fmaf(qk, d.y, p.y), fmaf(qk, d.z, p.z),
+                                     fmaf(qk, d.w, p.w));
+        store_out4(out, rv + 4 * cg, o);
+      }
     }
-    if (rg == 0) {
-      const float4 o = make_float4(fmaf(qk, d.x, p.x), fmaf(qk, d.y, p.y), fmaf(qk, d.z, p.z),
-                                   fmaf(qk, d.w, p.w));
-      store_out4(out, rv + 4 * cg, o);
+  };
+
+  if constexpr (kCkpt) {
+    // Segments of ckpt_interval tokens; after each full one, its checkpoint.
+    const long long seg = a.ckpt_interval;
+    for (long long s0 = t0; s0 < t1; s0 += seg) {
+      const long long s1 = s0 + seg < t1 ? s0 + seg : t1;
+      run(s0, s1);
+      if (s1 - s0 == seg) {
+        const long long row = a.ckpt_offsets[n] + (s1 - t0) / seg - 1;
+        float4* dst = reinterpret_cast<float4*>(a.ckpt + (row * a.heads + h) * DK * DV);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) __stcs(dst + (rg + RG * m) * CG + cg, S[m]);
+      }
     }
+  } else {
+    run(t0, t1);
   }
 
   if (a.final_state) {
@@ -159,10 +181,18 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
 template <int DK, int DV>
 cudaError_t launch_dims(const LaunchArgs& a, cudaStream_t s) {
   dim3 grid(a.n_seqs, a.heads);
-  if (a.dtype == KDA_F32)
-    recurrent_kernel<DK, DV, float><<<grid, kThreads, 0, s>>>(a);
-  else
-    recurrent_kernel<DK, DV, __nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
+  const bool ck = a.ckpt != nullptr;
+  if (a.dtype == KDA_F32) {
+    if (ck)
+      recurrent_kernel<DK, DV, float, true><<<grid, kThreads, 0, s>>>(a);
+    else
+      recurrent_kernel<DK, DV, float, false><<<grid, kThreads, 0, s>>>(a);
+  } else {
+    if (ck)
+      recurrent_kernel<DK, DV, __nv_bfloat16, true><<<grid, kThreads, 0, s>>>(a);
+    else
+      recurrent_kernel<DK, DV, __nv_bfloat16, false><<<grid, kThreads, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -106,6 +106,32 @@ KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const voi
                   int* dev_status, void* stream);
 
 /*
+ * kda_chunk_fwd that also writes prefix-cache checkpoints: the fp32 state of
+ * every (sequence, head) after each `ckpt_interval` tokens of the sequence.
+ * The serving description of the Kimi K3 architecture-atlas entry keeps KDA
+ * state checkpoints at 512-token hash boundaries beside the MLA KV pages
+ * ("KDA-aware prefix cache", also in the paper review's section
+ * "Infrastructure: how to actually run trillion-scale").
+ *
+ *   checkpoints   fp32 [n_ckpt, H, dk, dv]: checkpoint j of sequence n (the
+ *                 state after (j+1) * ckpt_interval tokens of it) is row
+ *                 ckpt_offsets[n] + j.  A sequence of length L has
+ *                 floor(L / ckpt_interval) checkpoints; the last one equals
+ *                 final_state when L is a multiple of the interval.
+ *   ckpt_offsets  device int32 [N + 1]: ckpt_offsets[n+1] - ckpt_offsets[n] =
+ *                 floor(len_n / ckpt_interval), ckpt_offsets[0] = 0.
+ *   ckpt_interval tokens between checkpoints: a positive multiple of 64.
+ * Everything else, including results, is as kda_chunk_fwd.
+ */
+KDA_API int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v,
+                                      const void* g, const void* beta, const float* init_state,
+                                      const int* cu_seqlens, void* out, float* final_state,
+                                      int chunk, const kda_dims* dims, void* workspace,
+                                      size_t workspace_bytes, int* dev_status, void* stream,
+                                      float* checkpoints, const int* ckpt_offsets,
+                                      int ckpt_interval);
+
+/*
  * One recurrent decode step (the "dedicated kernels for KDA decode" of the
  * section "Infrastructure: how to actually run trillion-scale"; the state is
  * the fixed-size d_k x d_v cache object per head).  Every one of the N

@@ -71,6 +71,22 @@ def test_host_validation_prefill(lib):
     assert _prefill(lib, _dims(n=0, t=0)) == 0
 
 
+def test_host_validation_checkpoints(lib):
+    d = _dims(n=1, t=128)
+
+    def call(ck=FAKE, offs=FAKE, interval=64):
+        return lib.kda_chunk_fwd_checkpoints(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                             64, ctypes.byref(d), None, 0, None, None, ck, offs,
+                                             interval)
+
+    assert call(ck=None) == -1              # checkpoint buffer is required
+    assert call(offs=None) == -1            # so are the offsets
+    assert call(interval=0) == -1           # interval must be positive
+    assert call(interval=-64) == -1
+    assert call(interval=100) == -2         # and a multiple of 64
+    assert call(ck=MISALIGNED) == -5
+
+
 def test_host_validation_decode(lib):
     d = _dims(n=4, t=5)
     assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d),
