@@ -248,9 +248,15 @@ def run_gpu(args):
     value = job_throughput(world, T, ms_step) / 1e6
     alg_bytes = prefill_bytes(T, H, w.dk, w.dv)
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-    tc = kda.algorithm(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk) == "tcgen05"
-    traffic = kernel_traffic("kda_chunk_tc.cu" if tc else "kda_recurrent.cu",
-                             "chunk_fwd_prefill_T8192_H96.md")
+    algo = kda.algorithm(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk)
+    tc = algo.startswith("tcgen05")
+    # The split path is two kernels per call (one window of chunks at this size).
+    kname, kfile, kprof, launches = {
+        "tcgen05_split": ("kda_chunk_split (chunk_prep_kernel + chunk_state_kernel)",
+                          "kda_chunk_split.cu", "chunk_split_prefill_T8192_H96.md", 2),
+        "tcgen05": ("kda_chunk_tc", "kda_chunk_tc.cu", "chunk_fwd_prefill_T8192_H96.md", 1),
+    }.get(algo, ("kda_recurrent", "kda_recurrent.cu", "chunk_fwd_prefill_T8192_H96.md", 1))
+    traffic = kernel_traffic(kfile, kprof)
 
     # ---------------- e2e through the public API with host buffers ----------------
     host_in = [x.cpu().pin_memory() for x in args_pf + [d["init_state"]]]
@@ -364,13 +370,13 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic,
-                         "kernel": "kda_chunk_tc" if tc else "kda_recurrent",
+                         "kernel": kname,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "kernel_ms": kern_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * 1,
+            "gpu_launches": args.steps * launches,
             "clocks": clocks,
             "prefill_checkpoints": ckpt,
             "decode": {"workload": DECODE, "value": job_throughput(world, N, dec_ms),

@@ -115,7 +115,7 @@ def algorithm(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=6
     rc = int(load().kda_chunk_fwd_algorithm(ctypes.byref(d), int(chunk)))
     if rc < 0:
         raise KDAError(rc, "kda_chunk_fwd_algorithm")
-    return {0: "recurrent", 1: "tcgen05"}[rc]
+    return {0: "recurrent", 1: "tcgen05", 2: "tcgen05_split"}[rc]
 
 
 def checkpoint_offsets(lengths, interval: int) -> list:

@@ -2,6 +2,8 @@
 // runs on the host before any CUDA call, so an invalid call returns without
 // touching the device.
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "kda_internal.h"
 
@@ -43,6 +45,33 @@ int check_io_pointers(const void* q, const void* k, const void* v, const void* g
   return KDA_OK;
 }
 
+size_t align_up(size_t b) { return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign; }
+
+enum class Path { kRecurrent, kFused, kSplit };
+
+// Which prefill kernels run for these dims (split only with room for its
+// records in the workspace; KDA_CHUNK_PATH=fused|split overrides the default).
+Path choose_path(const kda_dims* d, int chunk) {
+  LaunchArgs a{};
+  a.n_seqs = d->n_seqs; a.heads = d->heads; a.dk = d->dk; a.dv = d->dv;
+  a.dtype = d->dtype; a.chunk = chunk; a.total_tokens = d->total_tokens;
+  if (!kda::chunk_tc_supported(a)) return Path::kRecurrent;
+  if (d->n_seqs > kda::kSplitMaxSeqs) return Path::kFused;
+  const char* env = getenv("KDA_CHUNK_PATH");
+  if (env && strcmp(env, "fused") == 0) return Path::kFused;
+  if (env && strcmp(env, "split") == 0) return Path::kSplit;
+  return static_cast<long long>(d->n_seqs) * d->heads <= kda::kSplitMaxPairs ? Path::kSplit
+                                                                              : Path::kFused;
+}
+
+// Split-path workspace after the order array: the carried state, then records.
+size_t split_state_bytes(const kda_dims* d) {
+  return align_up(static_cast<size_t>(d->n_seqs) * d->heads * d->dk * d->dv * sizeof(float));
+}
+size_t split_workspace_bytes(const kda_dims* d) {
+  return split_state_bytes(d) + kda::split_record_bytes(d->n_seqs, d->total_tokens, d->heads);
+}
+
 }  // namespace
 
 extern "C" {
@@ -64,19 +93,22 @@ const char* kda_status_string(int status) {
 }
 
 size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk) {
-  (void)chunk;
   if (check_dims(dims) != KDA_OK) return 0;
-  return order_bytes(dims->n_seqs);
+  size_t b = order_bytes(dims->n_seqs);
+  if (dims->n_seqs > 0 && dims->heads > 0 && choose_path(dims, chunk) == Path::kSplit)
+    b += split_workspace_bytes(dims);
+  return b;
 }
 
 int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk) {
   const int rc = check_dims(dims);
   if (rc != KDA_OK) return rc;
   if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
-  LaunchArgs a{};
-  a.n_seqs = dims->n_seqs; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
-  a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
-  return kda::chunk_tc_supported(a) ? KDA_ALGO_TCGEN05 : KDA_ALGO_RECURRENT;
+  switch (choose_path(dims, chunk)) {
+    case Path::kSplit: return KDA_ALGO_TCGEN05_SPLIT;
+    case Path::kFused: return KDA_ALGO_TCGEN05;
+    default: return KDA_ALGO_RECURRENT;
+  }
 }
 
 }  // extern "C"
@@ -135,10 +167,25 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
     a.order = order;
   }
   cudaError_t e;
-  if (kda::chunk_tc_supported(a))
+  const Path path = choose_path(dims, chunk);
+  // The split form needs room for at least one record per pair after the
+  // order array and the carried states; less room than the full size only
+  // means more (smaller) windows.
+  const size_t split_min = need + split_state_bytes(dims) +
+                           static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;
+  if (path == Path::kSplit && workspace && workspace_bytes >= split_min) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace) + need;
+    float* run = reinterpret_cast<float*>(ws);
+    uint8_t* rec = ws + split_state_bytes(dims);
+    size_t rec_bytes = workspace_bytes - need - split_state_bytes(dims);
+    const size_t full = kda::split_record_bytes(N, dims->total_tokens, dims->heads);
+    if (rec_bytes > full) rec_bytes = full;
+    e = kda::launch_chunk_split(a, rec, rec_bytes, final_state ? final_state : run, s);
+  } else if (path != Path::kRecurrent) {
     e = kda::launch_chunk_tc(a, s);
-  else
+  } else {
     e = kda::launch_recurrent(a, s);
+  }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

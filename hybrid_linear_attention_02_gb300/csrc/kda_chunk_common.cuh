@@ -1,0 +1,72 @@
+// Device helpers and constants shared by the chunkwise tensor-core kernels
+// (the fused kernel and the split prep / state kernels), plus the host helper
+// that describes a [T, H, 128] bf16 tensor to TMA.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "kda_sm100.cuh"
+
+namespace kda {
+
+constexpr int kC = 64;    // chunk length (tokens)
+constexpr int kD = 128;   // dk = dv
+constexpr float kLog2e = 1.4426950408889634f;
+
+// [T, H, 128] bf16 viewed as a 3-D tensor (channel, head, token); one box is
+// 64 channels x 1 head x 64 tokens, 128B-swizzled, zero-filled past T.
+bool make_token_map(CUtensorMap* map, const void* base, int heads, long long tokens);
+
+namespace chunk {
+
+using namespace sm100;
+
+__device__ __forceinline__ int khat_row0(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_tile8(uint8_t* tile, int row, int col, int rows,
+                                         const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
+      make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// Shared by all roles: a wait that also gives up once any thread has given up.
+struct Sync {
+  uint64_t* bars;
+  volatile int* abort;
+  __device__ __forceinline__ bool wait(int b, uint32_t parity) {
+    if (*abort) return false;
+    if (mbar_try_wait(&bars[b], parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      // Suspended until the phase completes (or 20 us pass), not spinning.
+      if (mbar_try_wait_sleep(&bars[b], parity, 20000u)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 2000000000ull) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+};
+
+}  // namespace chunk
+}  // namespace kda

@@ -1,0 +1,1009 @@
+// bf16 chunkwise KDA on tcgen05 tensor cores (dk = dv = 128, chunk C = 64),
+// split into a parallel preparation kernel and a serial state kernel.
+//
+// Same chunkwise form as the fused kernel (written out from the recurrence of
+// "[Paper Review] Kimi K3: Open Frontier Intelligence", section "Kimi Delta
+// Attention (KDA)"; G = in-chunk cumulative log-decay, T = (I + A)^-1):
+//   A  = strictly_lower(diag(beta) (k e^G)(k e^-G)^T)
+//   W  = T diag(beta) (k e^G),  U = T diag(beta) V - W S0
+//   O  = (q e^G) S0 + lower_incl((q e^G)(k e^-G)^T) U
+//   S_C = Diag(e^{G_C}) S0 + (k e^{G_C - G})^T U
+// Everything but the last three lines' products with S0 and U is independent
+// of the state.  With few (sequence, head) pairs, one CTA per pair leaves most
+// SMs idle while each CTA's preparation chain is the bound, so here:
+//
+//  chunk_prep_kernel: persistent, two CTAs per SM, one chunk of one head per
+//    iteration, over every chunk of every pair at once.  It runs the
+//    state-independent chain (cumulative decay, scaled operand tiles, the
+//    masked products A and P in one MMA, T by block-Neumann inversion,
+//    W^T = Ktil^T T'^T by MMA) and writes one 66,048-byte record per chunk:
+//    the byte images of the operand tiles the state pass reads (-W^T, Qtil,
+//    Kbar, P, T' = T diag(beta)) and e^{G_C}.
+//  chunk_state_kernel: one CTA per pair walks its chunks in order; a producer
+//    warp streams records (1-D bulk copies) and v tiles (TMA) into a two-slot
+//    ring, four warps run the state pass with the fp32 state resident in TMEM:
+//      U^T = V^T T'^T + S^T (-W)^T,  O^T = S^T Qtil^T     (MMA)
+//      S^T += U^T Kbar,  O^T += U^T P^T                    (MMA)
+//    and fold the next chunk's decay Diag(e^{G_C}) into the pass that makes
+//    the bf16 operand copy of the new state.
+//
+// Records of a window of chunk indices [cw0, cw1) (per sequence) are laid out
+// [sequence][head][chunk]; a long input runs as several windows with the
+// state carried between them, which bounds the record buffer.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "kda_internal.h"
+#include "kda_sm100.cuh"
+#include "kda_chunk_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+using namespace chunk;
+
+// ---- one chunk record: shared-memory operand images, 1024-aligned tiles.
+constexpr uint32_t kRecW = 0;        // -W^T  128 x 64, rows = key channel (MN-major B)
+constexpr uint32_t kRecQ = 16384;    // Qtil   64 x 128 (K-major B)
+constexpr uint32_t kRecK = 32768;    // Kbar   64 x 128 (MN-major B)
+constexpr uint32_t kRecP = 49152;    // P      64 x 64  (K-major B)
+constexpr uint32_t kRecT = 57344;    // T'     64 x 64  (K-major B)
+constexpr uint32_t kRecG = 65536;    // e^{G_C}, fp32 [128]
+constexpr uint32_t kRecBytes = 66048;
+constexpr uint32_t kRecSlot = 66560; // slot stride in shared memory (1024-aligned)
+static_assert(kRecBytes == kSplitRecordBytes, "record size seen by the host");
+
+// ---------------------------------------------------------------- prep kernel
+constexpr int kPThreads = 256;
+constexpr uint32_t kPOffKQ = 0;        // [K';Q'] 128 x 128; raw k at 0, raw q at 16384
+constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W^T
+constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128; raw g before P2
+constexpr uint32_t kPOffTB = 90112;    // T' 64 x 64; tile sums and e^{R_a} tables in P1/P2
+constexpr uint32_t kPTiles = 98304;
+constexpr uint32_t kPSmem = kPTiles + 1024;
+constexpr uint32_t kPOffTileTot = kPOffTB;          // fp32 [4][128]
+constexpr uint32_t kPOffTabR = kPOffTB + 2048;      // fp32 [2][4][128]
+constexpr int kLdA = 68;
+constexpr uint32_t kPOffA = kPOffKH;                       // A   64 x 68 fp32
+constexpr int kLdB = 20;
+constexpr uint32_t kPOffD = kPOffA + 64 * kLdA * 4;        // D   4 x 16 x 20
+constexpr uint32_t kPOffN = kPOffD + 4 * 16 * kLdB * 4;    // N   6 x 16 x 20
+constexpr uint32_t kPOffN2 = kPOffN + 6 * 16 * kLdB * 4;   // N^2 3 x 16 x 20
+constexpr uint32_t kPOffN3 = kPOffN2 + 3 * 16 * kLdB * 4;  // N^3 16 x 20
+static_assert(kPOffN3 + 16 * kLdB * 4 <= kPOffKH + 40960, "inverse scratch fits");
+constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W^T reuses 0..63
+enum { kPBarAP = 0, kPBarW, kPBarRaw, kPNumBars };
+
+// ---------------------------------------------------------------- state kernel
+constexpr int kSThreads = 160;             // warps 0..3 state pass, warp 4 producer
+constexpr uint32_t kSOffRec = 0;           // 2 record slots
+constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
+constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging, row-major bf16 64 x 128
+constexpr uint32_t kSTiles = kSOffO + 16384;
+constexpr uint32_t kSSmem = kSTiles + 1024;
+constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (lane = value column, column = key row)
+constexpr uint32_t kSColSB = 128;  // 64: bf16 S^T, A operand
+constexpr uint32_t kSColUT = 192;  // 32: bf16 U^T, A operand
+constexpr uint32_t kSColU = 224;   // 64 fp32: U^T
+constexpr uint32_t kSColO = 288;   // 64 fp32: O^T
+constexpr uint32_t kSTmemCols = 512;
+enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSNumBars };
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                    ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ void seq_bounds(const LaunchArgs& a, int n, long long& t0,
+                                           long long& t1) {
+  if (a.cu_seqlens) {
+    t0 = a.cu_seqlens[n];
+    t1 = a.cu_seqlens[n + 1];
+  } else {
+    t0 = static_cast<long long>(n) * a.seq_len;
+    t1 = t0 + a.seq_len;
+  }
+}
+
+// cum[n] = H x (chunks of sequences m < n inside the window), n = 0..N; the
+// records of sequence n start at cum[n].  Every thread of the block calls it.
+__device__ void window_prefix(const LaunchArgs& a, const SplitWindow& w, int* cum) {
+  const int N = a.n_seqs, H = a.heads;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    long long t0, t1;
+    seq_bounds(a, i, t0, t1);
+    const long long nc = (t1 - t0 + kC - 1) / kC;
+    const long long lo = nc < w.cw0 ? nc : w.cw0, hi = nc < w.cw1 ? nc : w.cw1;
+    cum[i + 1] = H * static_cast<int>(hi - lo);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < N; base += 32) {
+      const int i = base + lane;
+      int x = i < N ? cum[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (i < N) cum[i + 1] = carry + x;
+      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) cum[0] = 0;
+  }
+  __syncthreads();
+}
+
+struct Item {
+  int n, h, c;          // sequence, head, chunk index within the sequence
+  long long t0, t1;     // sequence token range
+};
+
+__device__ __forceinline__ Item decode_item(const LaunchArgs& a, const SplitWindow& w,
+                                            const int* cum, int it) {
+  int lo = 0, hi = a.n_seqs;  // cum[lo] <= it < cum[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cum[mid] <= it) lo = mid;
+    else hi = mid;
+  }
+  Item r;
+  r.n = lo;
+  const int nck = (cum[lo + 1] - cum[lo]) / a.heads;
+  const int local = it - cum[lo];
+  r.h = local / nck;
+  r.c = w.cw0 + local % nck;
+  seq_bounds(a, lo, r.t0, r.t1);
+  return r;
+}
+
+// 8 floats -> bf16 at (row, col) of a 128B-swizzled tile image in global memory.
+__device__ __forceinline__ void st_gtile8(uint8_t* tile, int row, int col, int rows,
+                                          const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
+      make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kPThreads, 2)
+    chunk_prep_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(16) float facs[6 * kD];   // Khat block factors e^{R_a2 - R_a}
+  __shared__ __align__(16) float s_beta[kC];
+  __shared__ int s_cum[kSplitMaxSeqs + 1];
+  __shared__ uint64_t s_bars[kPNumBars];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int p = threadIdx.x, pw = p >> 5, lane = p & 31;
+  const int H = args.heads;
+  window_prefix(args, win, s_cum);
+  const int n_items = s_cum[args.n_seqs];
+  if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform over the block
+
+  if (pw == 0) {
+    tmem_alloc(&s_tmem, kPTmemCols);
+    tmem_relinquish();
+  }
+  if (p == 0) {
+    for (int b = 0; b < kPNumBars; ++b) mbar_init(&s_bars[b], 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+  Sync sync{s_bars, &s_abort};
+
+  const int ta = pw & 3;                      // this warp's 16-token row tile
+  const int cg = 8 * (pw >> 2) + (lane & 7);  // channels 8 cg .. 8 cg + 7
+  const int r4 = lane >> 3;                   // rows 16 ta + 4 r4 + m, m = 0..3
+  const int row0 = 16 * ta + 4 * r4;
+  const bool leader = p == 0;                 // issues MMAs and bulk stores
+  const bool loader = p == 128;               // issues the raw-tile TMA loads
+  const __nv_bfloat16* __restrict__ gb = static_cast<const __nv_bfloat16*>(args.beta);
+  float* Am = reinterpret_cast<float*>(smem + kPOffA);
+  float* Dm = reinterpret_cast<float*>(smem + kPOffD);
+  float* Nm = reinterpret_cast<float*>(smem + kPOffN);
+  float* N2m = reinterpret_cast<float*>(smem + kPOffN2);
+  float* N3m = reinterpret_cast<float*>(smem + kPOffN3);
+  float* tile_tot = reinterpret_cast<float*>(smem + kPOffTileTot);
+  float* tabR = reinterpret_cast<float*>(smem + kPOffTabR);
+
+  // Raw k, q (into the [K';Q'] tile) and g (into the Ktil tile), two boxes each.
+  auto issue_raw = [&](const Item& x) {
+    const int c0 = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
+    uint64_t* bar = &s_bars[kPBarRaw];
+    mbar_arrive_expect_tx(bar, 3 * 16384);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      tma_load_3d(smem + kPOffKQ + hf * 8192, &tm_k, 64 * hf, x.h, c0, bar);
+      tma_load_3d(smem + kPOffKQ + 16384 + hf * 8192, &tm_q, 64 * hf, x.h, c0, bar);
+      tma_load_3d(smem + kPOffKT + hf * 8192, &tm_g, 64 * hf, x.h, c0, bar);
+    }
+  };
+  float rb[4];
+  auto load_beta = [&](const Item& x) {
+    const long long c0 = x.t0 + static_cast<long long>(x.c) * kC;
+    const long long rem = x.t1 - c0;
+    const int L = static_cast<int>(rem < kC ? rem : kC);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int r = row0 + m;
+      rb[m] = (cg == 0 && r < L) ? __bfloat162float(gb[(c0 + r) * H + x.h]) : 0.f;
+    }
+  };
+
+  Item cur = decode_item(args, win, s_cum, blockIdx.x);
+  if (loader) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_g);
+    issue_raw(cur);
+  }
+  load_beta(cur);
+
+  uint32_t k_iter = 0;
+#pragma unroll 1
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k_iter) {
+    const uint32_t par = k_iter & 1;
+    const long long c0 = cur.t0 + static_cast<long long>(cur.c) * kC;
+    const int L = static_cast<int>(cur.t1 - c0 < kC ? cur.t1 - c0 : kC);
+    uint8_t* rec = win.rec + static_cast<size_t>(it) * kRecBytes;
+    const int it_next = it + static_cast<int>(gridDim.x);
+    Item nxt = cur;
+    if (it_next < n_items) nxt = decode_item(args, win, s_cum, it_next);
+
+    // The previous item's bulk stores have read T' and -W^T out of shared
+    // memory before this item rewrites those tiles.
+    if (leader) bulk_wait_read_all();
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (cg == 0) s_beta[row0 + m] = rb[m];
+    if (it_next < n_items) load_beta(nxt);
+    named_bar(2, kPThreads);
+    const bool ok_raw = sync.wait(kPBarRaw, par);
+
+    uint4 rq[4], rk[4];
+    float G[4][8];
+    {
+      uint4 rgt[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int r = row0 + m;
+        const uint32_t off = sw128_off(r, 8 * cg, 64);
+        if (r < L && ok_raw) {
+          rgt[m] = *reinterpret_cast<const uint4*>(smem + kPOffKT + off);
+          rq[m] = *reinterpret_cast<const uint4*>(smem + kPOffKQ + 16384 + off);
+          rk[m] = *reinterpret_cast<const uint4*>(smem + kPOffKQ + off);
+        } else {
+          rgt[m] = rq[m] = rk[m] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // ---- P1: decay accumulated from the start of this 16-token tile (log2 units).
+      float gf[8];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        unpack8(rgt[m], gf);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) G[m][u] = (m ? G[m - 1][u] : 0.f) + gf[u] * kLog2e;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float tot = G[3][u];
+      float y = __shfl_up_sync(0xFFFFFFFFu, tot, 8);
+      if (r4 >= 1) tot += y;
+      y = __shfl_up_sync(0xFFFFFFFFu, tot, 16);
+      if (r4 >= 2) tot += y;
+      const float excl = tot - G[3][u];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) G[m][u] += excl;
+      if (r4 == 3) tile_tot[ta * kD + 8 * cg + u] = tot;
+    }
+    // Tile sums are visible, and every raw read is done before the tiles are rewritten.
+    named_bar(2, kPThreads);
+    // ---- Per-(tile, channel) factors, thread p <-> channel p; split layout as in
+    // the fused kernel, so the 16-byte reads below are conflict-free.
+    if (p < kD) {
+      const int cc = p;
+      const int sc = (cc & 4 ? 64 : 0) + 4 * (cc >> 3) + (cc & 3);
+      float tt[4], R[4], acc = 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        tt[a] = tile_tot[a * kD + cc];
+        R[a] = acc;
+        acc += tt[a];
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        tabR[a * kD + sc] = ex2_fast(R[a]);
+        tabR[(4 + a) * kD + sc] = ex2_fast(acc - R[a]);
+      }
+      facs[0 * kD + sc] = ex2_fast(R[1] - R[0]);
+      facs[1 * kD + sc] = ex2_fast(R[2] - R[0]);
+      facs[2 * kD + sc] = ex2_fast(R[3] - R[0]);
+      facs[3 * kD + sc] = ex2_fast(R[2] - R[1]);
+      facs[4 * kD + sc] = ex2_fast(R[3] - R[1]);
+      facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
+      reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
+    }
+    named_bar(2, kPThreads);
+
+    // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
+    {
+      const int sc0 = 4 * cg;
+      auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
+        const float4 lo = *reinterpret_cast<const float4*>(t + sc0);
+        const float4 hi = *reinterpret_cast<const float4*>(t + 64 + sc0);
+        o[0] = f2_pack(lo.x, lo.y);
+        o[1] = f2_pack(lo.z, lo.w);
+        o[2] = f2_pack(hi.x, hi.y);
+        o[3] = f2_pack(hi.z, hi.w);
+      };
+      uint64_t eR[4], eC[4];
+      ld8(tabR + ta * kD, eR);
+      ld8(tabR + (4 + ta) * kD, eC);
+      auto st4 = [&](uint8_t* base, int row, int rows, const uint32_t (&v)[4]) {
+        *reinterpret_cast<uint4*>(base + sw128_off(row, 8 * cg, rows)) =
+            make_uint4(v[0], v[1], v[2], v[3]);
+      };
+      uint64_t kh[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int r = row0 + m, rl = 4 * r4 + m;
+        const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
+        const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
+        uint32_t okp[4], oqp[4], okt[4], oqt[4], okh[4], okb[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
+          const float dx = G[m][2 * w], dy = G[m][2 * w + 1];
+          const uint64_t e1 = f2_pack(ex2_fast(dx), ex2_fast(dy));
+          const uint64_t ei = f2_pack(ex2_fast(-dx), ex2_fast(-dy));
+          const uint64_t k1 = f2_mul(kp, e1), q1 = f2_mul(qp, e1);
+          okp[w] = f2_to_bf16x2(k1);
+          oqp[w] = f2_to_bf16x2(q1);
+          okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
+          oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
+          kh[m][w] = f2_mul(kp, ei);
+          okh[w] = f2_to_bf16x2(kh[m][w]);
+          okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
+        }
+        st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
+        st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
+        st4(smem + kPOffKT, r, 64, okt);
+        st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
+        st4(rec + kRecQ, r, 64, oqt);
+        st4(rec + kRecK, r, 64, okb);
+      }
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        const int a2 = ta + 1 + i;
+        if (a2 < 4) {
+          const int frow = ta == 0 ? a2 - 1 : ta == 1 ? a2 + 1 : 5;
+          uint64_t f[4];
+          ld8(facs + frow * kD, f);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t ox[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[m][w], f[w]));
+            st4(smem + kPOffKH, khat_row0(a2) + row0 + m, 160, ox);
+          }
+        }
+      }
+    }
+    fence_async_smem();
+    named_bar(2, kPThreads);
+
+    // ---- P3: every masked intra-chunk product in one MMA (M=128, N=160, K=128).
+    if (leader && !s_abort) {
+      tc_fence_after();
+      const uint32_t idesc = umma_idesc_bf16(128, 160, 0, 0);
+      const uint32_t aK = smem_u32(smem + kPOffKQ), bK = smem_u32(smem + kPOffKH);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        umma_bf16(tbase, umma_desc(aK + (t >> 2) * 128 * 128 + (t & 3) * 32, 16, 1024),
+                  umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
+      umma_commit(&s_bars[kPBarAP]);
+    }
+    const bool ok_ap = sync.wait(kPBarAP, par);
+    tc_fence_after();
+
+    // ---- P4: A (x beta, strictly lower; fp32, shared) and P (lower inclusive;
+    // bf16, straight to the record).
+    if (pw < 4 && ok_ap) {
+      const int a = pw, rl = lane & 15, r = 16 * a + rl;
+      const bool isP = lane >= 16;
+      const float br = s_beta[r];
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float v[16];
+        if (blk <= a) {
+          tmem_ld16(tbase + (static_cast<uint32_t>(32 * pw) << 16) + khat_row0(a) + 16 * blk, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int i = 16 * blk + u;
+            v[u] = isP ? (i <= r ? v[u] : 0.f) : (i < r ? br * v[u] : 0.f);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) v[u] = 0.f;
+        }
+        if (isP) {
+#pragma unroll
+          for (int h8 = 0; h8 < 2; ++h8) {
+            float f8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
+            st_gtile8(rec + kRecP, r, 16 * blk + 8 * h8, 64, f8);
+          }
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<float4*>(&Am[r * kLdA + 16 * blk + 4 * q4]) =
+                make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+    named_bar(2, kPThreads);
+
+    // ---- P5: T = (I + A)^-1 = (I - N + N^2 - N^3) D in fp32, written as
+    // T' = T diag(beta) in bf16 (same block scheme as the fused kernel).
+    if (p < 64) {
+      const int blk = p >> 4, jj = p & 15;
+      const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
+      float ar[16][16];
+#pragma unroll
+      for (int rr = 1; rr < 16; ++rr)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (4 * q < rr) {
+            const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
+            ar[rr][4 * q] = v.x; ar[rr][4 * q + 1] = v.y;
+            ar[rr][4 * q + 2] = v.z; ar[rr][4 * q + 3] = v.w;
+          }
+        }
+      float x[16];
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < rr; ++i) {
+          if (i & 1) acc1 = fmaf(ar[rr][i], x[i], acc1);
+          else acc0 = fmaf(ar[rr][i], x[i], acc0);
+        }
+        x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -(acc0 + acc1));
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = x[rr];
+    } else {
+      for (int e = p - 64; e < 192; e += kPThreads - 64) {
+        const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+        const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
+        const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st_tile8(smem + kPOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
+      }
+    }
+    named_bar(2, kPThreads);
+    auto tile16 = [&](const float* X, int xs, const float* Y, int ys, int i4, int j4,
+                      float (&acc)[4][4]) {
+      float4 yv[16], xv[4][4];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float4*>(Y + k * ys + 4 * j4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          xv[i][q] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 xq = xv[i][k >> 2];
+          const float xk = (k & 3) == 0 ? xq.x : (k & 3) == 1 ? xq.y : (k & 3) == 2 ? xq.z : xq.w;
+          acc[i][0] = fmaf(xk, yv[k].x, acc[i][0]);
+          acc[i][1] = fmaf(xk, yv[k].y, acc[i][1]);
+          acc[i][2] = fmaf(xk, yv[k].z, acc[i][2]);
+          acc[i][3] = fmaf(xk, yv[k].w, acc[i][3]);
+        }
+      }
+    };
+    auto store_tile = [&](float* Z, int i4, int j4, const float (&acc)[4][4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(Z + (4 * i4 + i) * kLdB + 4 * j4) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    };
+    const int tq = p & 15, i4 = tq >> 2, j4 = tq & 3;
+    // Step 1: N_ab = D_aa A_ab; diagonal blocks of T'.
+    if (p < 96) {
+      const int blk = p >> 4;
+      const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
+      const int b = blk - (a * (a - 1)) / 2;
+      float acc[4][4] = {};
+      tile16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, i4, j4, acc);
+      store_tile(Nm + blk * 16 * kLdB, i4, j4, acc);
+    } else if (p >= 128) {
+      const int e = p - 128, a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+      float f8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int cc = 8 * h8 + u;
+        f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
+      }
+      st_tile8(smem + kPOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
+    }
+    named_bar(2, kPThreads);
+    // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
+    if (p < 48) {
+      const int k2 = p >> 4;
+      float acc[4][4] = {};
+      const int xa = k2 == 0 ? 2 : k2 == 1 ? 5 : 4, ya = k2 == 0 ? 0 : k2 == 1 ? 2 : 0;
+      tile16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, i4, j4, acc);
+      if (k2 == 2) tile16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, i4, j4, acc);
+      store_tile(N2m + k2 * 16 * kLdB, i4, j4, acc);
+    }
+    named_bar(2, kPThreads);
+    // Step 3: N^3 block (3,0); M = -N + N^2 in place for (1,0) (2,0) (2,1) (3,1).
+    if (p < 16) {
+      float acc[4][4] = {};
+      tile16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, i4, j4, acc);
+      store_tile(N3m, i4, j4, acc);
+    } else if (p >= 32) {
+      for (int e = p - 32; e < 4 * 64; e += kPThreads - 32) {
+        const int bsel = e >> 6;
+        const int blk = bsel < 3 ? bsel : 4;
+        const int k2 = blk == 1 ? 0 : blk == 4 ? 1 : -1;
+        const int row = (e >> 2) & 15, q = e & 3;
+        float4* nv = reinterpret_cast<float4*>(Nm + (blk * 16 + row) * kLdB + 4 * q);
+        float4 m = *nv;
+        m.x = -m.x; m.y = -m.y; m.z = -m.z; m.w = -m.w;
+        if (k2 >= 0) {
+          const float4 n2 = *reinterpret_cast<const float4*>(N2m + (k2 * 16 + row) * kLdB + 4 * q);
+          m.x += n2.x; m.y += n2.y; m.z += n2.z; m.w += n2.w;
+        }
+        *nv = m;
+      }
+    }
+    named_bar(2, kPThreads);
+    // Step 4: T_ab = M_ab D_bb, times beta, into T' (M_30 = -N30 + N^2_30 - N^3_30).
+    if (p < 96) {
+      const int blk = p >> 4;
+      const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
+      const int b = blk - (a * (a - 1)) / 2;
+      if (blk == 3) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = 4 * i4 + i;
+          float4* nv = reinterpret_cast<float4*>(Nm + (3 * 16 + row) * kLdB + 4 * j4);
+          const float4 n2 = *reinterpret_cast<const float4*>(N2m + (2 * 16 + row) * kLdB + 4 * j4);
+          const float4 n3 = *reinterpret_cast<const float4*>(N3m + row * kLdB + 4 * j4);
+          float4 m = *nv;
+          m.x = n2.x - m.x - n3.x; m.y = n2.y - m.y - n3.y;
+          m.z = n2.z - m.z - n3.z; m.w = n2.w - m.w - n3.w;
+          *nv = m;
+        }
+        __syncwarp(0x0000FFFFu << (16 * (lane >> 4)));
+      }
+      float acc[4][4] = {};
+      tile16(Nm + blk * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, i4, j4, acc);
+      if (blk == 5) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jq = 0; jq < 4; ++jq) acc[i][jq] = -acc[i][jq];
+      }
+      const float4 bv = *reinterpret_cast<const float4*>(&s_beta[16 * b + 4 * j4]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint2 pk = make_uint2(pack2(acc[i][0] * bv.x, acc[i][1] * bv.y),
+                                    pack2(acc[i][2] * bv.z, acc[i][3] * bv.w));
+        *reinterpret_cast<uint2*>(smem + kPOffTB +
+                                  sw128_off(16 * a + 4 * i4 + i, 16 * b + 4 * j4, 64)) = pk;
+      }
+    }
+    fence_async_smem();
+    named_bar(2, kPThreads);
+
+    // ---- P6: W^T = Ktil^T T'^T (M=128, N=64, K=64), into TMEM columns 0..63.
+    if (leader && !s_abort) {
+      tc_fence_after();
+      const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
+      const uint32_t aKT = smem_u32(smem + kPOffKT), bT = smem_u32(smem + kPOffTB);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        umma_bf16(tbase, umma_desc(aKT + t * 2048, 64 * 128, 1024),
+                  umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
+      umma_commit(&s_bars[kPBarW]);
+    }
+    const bool ok_w = sync.wait(kPBarW, par);
+    tc_fence_after();
+    // [K';Q'] and Ktil are dead: the next item's raw tiles may land.
+    if (loader && ok_w && it_next < n_items) issue_raw(nxt);
+
+    // ---- P7: -W^T (rows = key channel, columns = token) staged where Khat was.
+    if (pw < 4 && ok_w) {
+      const int cc = 32 * pw + lane;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float w[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * pw) << 16) + 32 * half, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float f8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) f8[u] = -w[8 * q8 + u];
+          st_tile8(smem + kPOffKH, cc, 32 * half + 8 * q8, 128, f8);
+        }
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    named_bar(2, kPThreads);
+    if (leader && !s_abort) {
+      bulk_store(rec + kRecW, smem + kPOffKH, 16384);
+      bulk_store(rec + kRecT, smem + kPOffTB, 8192);
+      bulk_commit();
+    }
+    cur = nxt;
+  }
+  if (leader) bulk_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && p == 0 && args.dev_status) atomicExch(args.dev_status, KDA_ERR_TIMEOUT);
+  if (pw == 0) tmem_dealloc(tbase, kPTmemCols);
+}
+
+__global__ void __launch_bounds__(kSThreads, 1)
+    chunk_state_kernel(LaunchArgs args, SplitWindow win,
+                       const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ int s_cum[kSplitMaxSeqs + 1];
+  __shared__ uint64_t s_bars[kSNumBars];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = args.heads;
+  const int h = blockIdx.y;
+  const int n = args.order ? args.order[blockIdx.x] : static_cast<int>(blockIdx.x);
+  window_prefix(args, win, s_cum);
+  long long t0, t1;
+  seq_bounds(args, n, t0, t1);
+  const int nck = (s_cum[n + 1] - s_cum[n]) / H;     // chunks of this pair in the window
+  const int rbase = s_cum[n] + h * nck;
+  const long long soff = (static_cast<long long>(n) * H + h) * kD * kD;
+  const float* src = win.first ? args.init_state : win.s_run;
+  float* dst = win.last ? args.final_state : win.s_run;
+
+  if (nck == 0) {
+    // No chunk of this pair in the window: carry its state through.
+    if (dst && dst != src) {
+      float4* d4 = reinterpret_cast<float4*>(dst + soff);
+      const float4* s4 = reinterpret_cast<const float4*>(src + soff);
+      for (int e = tid; e < kD * kD / 4; e += kSThreads)
+        d4[e] = src ? s4[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kSTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < kSNumBars; ++b) mbar_init(&s_bars[b], 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+  Sync sync{s_bars, &s_abort};
+
+  if (warp == 4) {
+    // ================================ producer ================================
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+#pragma unroll 1
+      for (int c = 0; c < nck; ++c) {
+        const int s = c & 1;
+        if (c >= 2 && !sync.wait(kSBarEmpty0 + s, ((c - 2) >> 1) & 1)) break;
+        uint64_t* bar = &s_bars[kSBarFull0 + s];
+        mbar_arrive_expect_tx(bar, kRecBytes + 16384);
+        const uint8_t* rec = win.rec + static_cast<size_t>(rbase + c) * kRecBytes;
+        uint8_t* slot = smem + kSOffRec + s * kRecSlot;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bulk_load(slot + 16384 * i, rec + 16384 * i, 16384, bar);
+        bulk_load(slot + kRecG, rec + kRecG, kRecBytes - kRecG, bar);
+        const int c0 = static_cast<int>(t0 + static_cast<long long>(win.cw0 + c) * kC);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(smem + kSOffV + s * 16384 + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
+      }
+    }
+  } else {
+    // =============================== state pass ===============================
+    const int j = tid;                                  // TMEM lane = value column
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
+
+    // S^T[j][c] = S[c][j]: fp32 copy (decayed below) and bf16 operand copy.
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t f[32], b[16];
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        f[u] = __float_as_uint(src ? __ldcs(src + soff + (32 * cb + u) * kD + j) : 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        b[u] = pack2(__uint_as_float(f[2 * u]), __uint_as_float(f[2 * u + 1]));
+      tmem_st32(tbase + lane_base + kSColS + 32 * cb, f);
+      tmem_st16(tbase + lane_base + kSColSB + 16 * cb, b);
+    }
+    tmem_st_wait();
+    // The fp32 state carries the first chunk's decay before its first update.
+    bool ok = sync.wait(kSBarFull0, 0);
+    if (ok) {
+      const float* gam = reinterpret_cast<const float*>(smem + kSOffRec + kRecG);
+#pragma unroll 1
+      for (int cb = 0; cb < 8; ++cb) {
+        float v[16];
+        tmem_ld16(tbase + lane_base + kSColS + 16 * cb, v);
+        tmem_ld_wait();
+        uint32_t f[16];
+#pragma unroll
+        for (int u = 0; u < 16; u += 4) {
+          const float4 gm = *reinterpret_cast<const float4*>(&gam[16 * cb + u]);
+          f[u] = __float_as_uint(v[u] * gm.x);
+          f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
+          f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
+          f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
+        }
+        tmem_st16(tbase + lane_base + kSColS + 16 * cb, f);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    named_bar(1, 128);
+
+    // U^T = V^T T'^T for the chunk in slot s (state-independent).
+    auto issue_mma0 = [&](int s) {
+      const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
+      const uint32_t aV = smem_u32(smem + kSOffV + s * 16384);
+      const uint32_t bT = smem_u32(smem + kSOffRec + s * kRecSlot + kRecT);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        umma_bf16(tbase + kSColU, umma_desc(aV + t * 2048, 64 * 128, 1024),
+                  umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
+    };
+    auto store_out = [&](int cl) {
+      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      __nv_bfloat16* dsto = gout + (c0 * H + h) * kD;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = j + 128 * i, r = e >> 4, ch = e & 15;
+        if (r < L)
+          *reinterpret_cast<uint4*>(dsto + static_cast<long long>(r) * H * kD + 8 * ch) =
+              *reinterpret_cast<const uint4*>(smem + kSOffO + r * 256 + ch * 16);
+      }
+    };
+    if (j == 0 && ok) {
+      tc_fence_after();
+      issue_mma0(0);
+    }
+    bool prev_ok = false;
+
+#pragma unroll 1
+    for (int c = 0; c < nck; ++c) {
+      const int s = c & 1;
+      uint8_t* slot = smem + kSOffRec + s * kRecSlot;
+      if (j == 0 && ok && !s_abort) {
+        tc_fence_after();
+        // U^T += S^T (-W)^T ;  O^T = S^T Qtil^T      (K = dk = 128)
+        const uint32_t iU = umma_idesc_bf16(128, 64, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
+        const uint32_t bW = smem_u32(slot + kRecW), bQ = smem_u32(slot + kRecQ);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t aS = tbase + kSColSB + 8 * t;
+          umma_bf16_tmem_a(tbase + kSColU, aS, umma_desc(bW + t * 2048, 128 * 128, 1024), iU, 1);
+          umma_bf16_tmem_a(tbase + kSColO, aS,
+                           umma_desc(bQ + (t >> 2) * 64 * 128 + (t & 3) * 32, 16, 1024), iO,
+                           t > 0);
+        }
+        umma_commit(&s_bars[kSBarMMA1]);
+      }
+      // The previous chunk's outputs leave while MMA1 runs.
+      if (c > 0 && prev_ok) store_out(c - 1);
+      const bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
+      tc_fence_after();
+      if (ok1) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kSColU + 32 * half, v);
+          tmem_ld_wait();
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          tmem_st16(tbase + lane_base + kSColUT + 16 * half, b);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar(1, 128);
+      const bool has_next = c + 1 < nck;
+      if (j == 0 && ok1 && !s_abort) {
+        tc_fence_after();
+        // S^T += U^T Kbar (K = 64 tokens) ;  O^T += U^T P^T
+        const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
+        const uint32_t bK = smem_u32(slot + kRecK), bP = smem_u32(slot + kRecP);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t aU = tbase + kSColUT + 8 * t;
+          umma_bf16_tmem_a(tbase + kSColS, aU, umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
+          umma_bf16_tmem_a(tbase + kSColO, aU, umma_desc(bP + t * 32, 16, 1024), iO, 1);
+        }
+        umma_commit(&s_bars[kSBarEmpty0 + s]);
+        umma_commit(&s_bars[kSBarMMA2]);
+        // The next chunk's U^T = V^T T'^T queues behind MMA2 (U^T is free).
+        if (has_next && sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1)) {
+          tc_fence_after();
+          issue_mma0(s ^ 1);
+        }
+      }
+      const bool ok_next = !has_next || sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1);
+      const bool ok2 = ok1 && sync.wait(kSBarMMA2, c & 1);
+      tc_fence_after();
+      if (ok2) {
+        const long long done = static_cast<long long>(win.cw0 + c + 1) * kC;
+        float* ck = nullptr;
+        if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
+          const long long row = args.ckpt_offsets[n] + done / args.ckpt_interval - 1;
+          ck = args.ckpt + (row * H + h) * kD * kD + j;
+        }
+        const bool decay = has_next && ok_next;
+        const float* gam =
+            reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot + kRecG);
+        // New state -> bf16 operand copy, and (for the next chunk) the decayed
+        // fp32 state; O^T column j -> row-major staging.
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kSColS + 32 * cb, v);
+          tmem_ld_wait();
+          if (ck) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) __stcs(ck + (32 * cb + u) * kD, v[u]);
+          }
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          tmem_st16(tbase + lane_base + kSColSB + 16 * cb, b);
+          if (decay) {
+            uint32_t f[32];
+#pragma unroll
+            for (int u = 0; u < 32; u += 4) {
+              const float4 gm = *reinterpret_cast<const float4*>(&gam[32 * cb + u]);
+              f[u] = __float_as_uint(v[u] * gm.x);
+              f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
+              f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
+              f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
+            }
+            tmem_st32(tbase + lane_base + kSColS + 32 * cb, f);
+          }
+        }
+        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kSOffO) + j;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(tbase + lane_base + kSColO + 32 * half, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int r = 0; r < 32; ++r) so[(32 * half + r) * kD] = __float2bfloat16_rn(v[r]);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar(1, 128);
+      prev_ok = ok2;
+      ok = ok2 && ok_next;
+    }
+    if (prev_ok) store_out(nck - 1);
+    if (!s_abort && dst) {
+      // After the last chunk the fp32 state carries no further decay.
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+        tmem_ld32(tbase + lane_base + kSColS + 32 * cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) __stcs(dst + soff + (32 * cb + u) * kD + j, v[u]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && tid == 0 && args.dev_status) atomicExch(args.dev_status, KDA_ERR_TIMEOUT);
+  if (warp == 0) tmem_dealloc(tbase, kSTmemCols);
+}
+
+}  // namespace
+
+size_t split_record_bytes(int n_seqs, long long total_tokens, int heads) {
+  const long long pairs = static_cast<long long>(n_seqs) * heads;
+  const long long bound = static_cast<long long>(heads) * (total_tokens / kC + n_seqs);
+  const long long budget = static_cast<long long>(kSplitRecordBudget / kRecBytes);
+  long long items = bound < budget ? bound : budget;
+  if (items < pairs) items = pairs;
+  return static_cast<size_t>(items) * kRecBytes;
+}
+
+cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
+                               float* run_state, cudaStream_t stream) {
+  if (a.n_seqs == 0 || a.heads == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kPSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSSmem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  CUtensorMap maps[4] = {};
+  if (a.total_tokens > 0) {
+    const void* bases[4] = {a.q, a.k, a.v, a.g};
+    for (int i = 0; i < 4; ++i)
+      if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
+        return cudaErrorInvalidValue;
+  }
+  const long long pairs = static_cast<long long>(a.n_seqs) * a.heads;
+  const long long cap_items = static_cast<long long>(record_bytes / kRecBytes);
+  if (cap_items < pairs) return cudaErrorInvalidValue;
+  const long long max_chunks = (a.total_tokens + kC - 1) / kC;   // of any one sequence
+  const long long wc = cap_items / pairs;                          // chunks per window
+  const long long item_bound_all = static_cast<long long>(a.heads) * (a.total_tokens / kC + a.n_seqs);
+  for (long long cw0 = 0;; cw0 += wc) {
+    SplitWindow w{};
+    w.rec = records;
+    w.cw0 = static_cast<int>(cw0);
+    w.cw1 = static_cast<int>(cw0 + wc < max_chunks ? cw0 + wc : max_chunks);
+    w.first = cw0 == 0;
+    w.last = cw0 + wc >= max_chunks;
+    w.s_run = run_state;
+    long long items = pairs * (w.cw1 - w.cw0);
+    if (items > item_bound_all) items = item_bound_all;
+    const long long grid_p = items < 2ll * sms ? items : 2ll * sms;
+    if (grid_p > 0) {
+      chunk_prep_kernel<<<static_cast<unsigned>(grid_p), kPThreads, kPSmem, stream>>>(
+          a, w, maps[0], maps[1], maps[3]);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    dim3 grid_s(a.n_seqs, a.heads);
+    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, stream>>>(a, w, maps[2]);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (w.last) break;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace kda

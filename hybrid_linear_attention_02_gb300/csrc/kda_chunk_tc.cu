@@ -44,14 +44,14 @@
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
+#include "kda_chunk_common.cuh"
 
 namespace kda {
 namespace {
 
 using namespace sm100;
+using namespace chunk;
 
-constexpr int kC = 64;
-constexpr int kD = 128;
 constexpr int kStateThreads = 128;                  // warps 0..3
 constexpr int kPrepThreads = 256;                   // warps 4..11
 constexpr int kThreads = kStateThreads + kPrepThreads;
@@ -62,7 +62,6 @@ constexpr int kStateRegs = 88;
 constexpr int kPrepRegs = 208;
 static_assert(kStateThreads * kStateRegs + kPrepThreads * kPrepRegs <= kThreads * 168,
               "register split fits the launch allocation");
-constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory tiles (byte offsets from a 1024-aligned base); bf16 tiles use
 // the 128B-swizzled layout of sw128_off().
@@ -122,52 +121,6 @@ __device__ unsigned long long kda_phase_clocks[32];
 #else
 #define KDA_MARK(i) ((void)0)
 #endif
-
-__device__ __forceinline__ int khat_row0(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
-
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void st_tile8(uint8_t* tile, int row, int col, int rows,
-                                         const float (&f)[8]) {
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
-      make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
-}
-
-// Shared by all roles: a wait that also gives up once any thread has given up.
-struct Sync {
-  uint64_t* bars;
-  volatile int* abort;
-  __device__ __forceinline__ bool wait(int b, uint32_t parity) {
-    if (*abort) return false;
-    if (mbar_try_wait(&bars[b], parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-      // Suspended until the phase completes (or 20 us pass), not spinning.
-      if (mbar_try_wait_sleep(&bars[b], parity, 20000u)) return true;
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > 2000000000ull) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-};
 
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(LaunchArgs args, const __grid_constant__ CUtensorMap tm_q,
@@ -931,10 +884,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+}  // namespace
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on libcuda).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -947,8 +901,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [T, H, 128] bf16 viewed as a 3-D tensor (channel, head, token); one box is
-// 64 channels x 1 head x 64 tokens, 128B-swizzled, zero-filled past T.
 bool make_token_map(CUtensorMap* map, const void* base, int heads, long long tokens) {
   const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
@@ -963,8 +915,6 @@ bool make_token_map(CUtensorMap* map, const void* base, int heads, long long tok
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool chunk_tc_supported(const LaunchArgs& a) {
   return a.dtype == KDA_BF16 && a.dk == kD && a.dv == kD && a.chunk == kC &&

@@ -39,4 +39,25 @@ cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,
 bool chunk_tc_supported(const LaunchArgs& a);
 cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream);
 
+// The same computation split into a parallel preparation kernel, which writes
+// one record per chunk, and a serial state kernel (for few sequence-head
+// pairs).  Records of a window of chunk indices [cw0, cw1) of every sequence;
+// the state is carried between windows in s_run.
+constexpr int kSplitMaxSeqs = 1024;              // sequences per call on this path
+constexpr long long kSplitMaxPairs = 304;        // default: sequence-head pairs up to this
+constexpr size_t kSplitRecordBytes = 66048;      // one chunk record
+constexpr size_t kSplitRecordBudget = 2ull << 30;  // record buffer cap (bytes)
+
+struct SplitWindow {
+  uint8_t* rec;
+  int cw0, cw1;
+  bool first, last;
+  float* s_run;        // state between windows (nullable with a single window)
+};
+
+// Record-buffer bytes the split path needs for these sizes.
+size_t split_record_bytes(int n_seqs, long long total_tokens, int heads);
+cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
+                               float* run_state, cudaStream_t stream);
+
 }  // namespace kda

@@ -95,9 +95,18 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  *   dev_status        optional device int, set non-zero by a kernel whose
  *                     bounded wait expired (KDA_ERR_TIMEOUT); never cleared.
  *   stream            cudaStream_t to enqueue on.
- * Paths: bf16 with dk = dv = 128 and chunk = 64 runs the tcgen05/TMA tensor-
- * core kernel (requires q, k, v, g, out 16-byte aligned); every other
- * supported case runs the fp32 CUDA-core kernel that walks the recurrence.
+ * Paths: bf16 with dk = dv = 128 and chunk = 64 runs on tcgen05 tensor cores
+ * (requires q, k, v, g, out 16-byte aligned); every other supported case runs
+ * the fp32 CUDA-core kernel that walks the recurrence.  On tensor cores, few
+ * (sequence, head) pairs (N x H <= 304, N <= 1024) run the split form, given
+ * a workspace of kda_chunk_fwd_workspace_size() bytes: a preparation kernel
+ * over every chunk at once, which writes a 66,048-byte record per chunk into
+ * the workspace (at most 2 GiB of records; longer inputs run in windows of
+ * chunks with the state carried between them), then a state kernel per pair.
+ * A smaller workspace that still holds the order array, N x H fp32 states and
+ * one record per pair runs the split form in more, smaller windows; below
+ * that, and otherwise, one fused kernel per pair runs.  The
+ * environment variable KDA_CHUNK_PATH=fused|split overrides the choice.
  * Inputs with g outside [-5, 0] are outside the tensor-core path's contract.
  */
 KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
@@ -150,7 +159,9 @@ KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const v
  * fragments a pool sized once at start-up.  The paper has no counterpart to
  * this entry point; it exists for those callers only.
  *
- * Arguments, layouts, paths and results are those of kda_chunk_fwd.  The only
+ * Arguments, layouts and results are those of kda_chunk_fwd; bf16 with
+ * dk = dv = 128 and chunk 64 always runs the fused tensor-core kernel (the
+ * split form needs a workspace for its records).  The only
  * scratch (the longest-first order of the packed sequences) lives in a fixed
  * device array inside libkda.so that holds KDA_NOALLOC_MAX_SEQS entries
  * (256 KiB); every GPU that loads the library keeps it until the process
@@ -172,11 +183,15 @@ KDA_API int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, c
                                   int chunk, const kda_dims* dims, int* dev_status,
                                   void* stream);
 
-typedef enum { KDA_ALGO_RECURRENT = 0, KDA_ALGO_TCGEN05 = 1 } kda_algo;
+typedef enum {
+  KDA_ALGO_RECURRENT = 0,       /* CUDA-core recurrence                          */
+  KDA_ALGO_TCGEN05 = 1,         /* fused tensor-core kernel, one CTA per pair    */
+  KDA_ALGO_TCGEN05_SPLIT = 2    /* tensor-core preparation + state kernels       */
+} kda_algo;
 
 /*
- * Which kernel kda_chunk_fwd runs for these dims and chunk size: the chunked
- * tcgen05 tensor-core kernel or the CUDA-core recurrence.  Returns a negative
+ * Which kernels kda_chunk_fwd runs for these dims and chunk size (given a
+ * workspace of kda_chunk_fwd_workspace_size() bytes).  Returns a negative
  * kda_status for dims kda_chunk_fwd would reject.
  */
 KDA_API int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk);

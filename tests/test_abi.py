@@ -98,11 +98,39 @@ def test_host_validation_decode(lib):
                                ctypes.byref(d), None, None) == -5
 
 
+REC = 66048          # one chunk record of the split tensor-core path
+
+
 def test_workspace_size(lib):
-    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(n=1)), 64) == 0
-    ws = lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(n=32, t=1000)), 64)
+    size = lambda d, c=64: lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), c)
+    algo = lambda d, c=64: lib.kda_chunk_fwd_algorithm(ctypes.byref(d), c)
+    # CUDA-core path (fp32): only the longest-first order of packed sequences.
+    assert algo(_dims(n=1, dtype=0)) == 0 and size(_dims(n=1, dtype=0)) == 0
+    ws = size(_dims(n=32, t=1000, dtype=0))
     assert ws >= 32 * 4 and ws % 256 == 0
-    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_dims(dk=7)), 64) == 0
+    # bf16, d = 128, few pairs: split path, carried states + a record per chunk.
+    d = _dims(n=1, t=8192, h=96)
+    assert algo(d) == 2
+    assert size(d) == 96 * 128 * 128 * 4 + 96 * (8192 // 64 + 1) * REC
+    # Long inputs: the record buffer is capped (2 GiB), the rest runs in windows.
+    d = _dims(n=1, t=1 << 20, h=32)
+    assert size(d) == 32 * 128 * 128 * 4 + ((2 << 30) // REC) * REC
+    # Many pairs: one fused kernel per pair, order array only.
+    d = _dims(n=32, t=270000, h=96)
+    assert algo(d) == 1 and size(d) == 256
+    # chunk 16 or 32 runs the CUDA-core path.
+    assert algo(_dims(n=1, t=8192, h=96), 32) == 0
+    assert size(_dims(dk=7)) == 0
+
+
+def test_path_override(lib, monkeypatch):
+    d = _dims(n=1, t=8192, h=96)
+    monkeypatch.setenv("KDA_CHUNK_PATH", "fused")
+    assert lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64) == 1
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), 64) == 0
+    monkeypatch.setenv("KDA_CHUNK_PATH", "split")
+    d = _dims(n=32, t=270000, h=96)
+    assert lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64) == 2
 
 
 def test_binding_rejects_cpu_tensors(lib):

@@ -13,6 +13,14 @@ DEV = torch.device("cuda:0")
 W = inputs.WORKLOADS
 
 
+@pytest.fixture(params=["split", "fused"])
+def tc_path(request, monkeypatch):
+    """Both tensor-core forms: the split preparation + state kernels (the
+    default for few sequence-head pairs) and the fused kernel."""
+    monkeypatch.setenv("KDA_CHUNK_PATH", request.param)
+    return request.param
+
+
 def _run(d, chunk=64):
     out, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
                              d["cu_seqlens"], chunk=chunk)
@@ -42,7 +50,7 @@ def test_oracle_scale_fp32_config():
 
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 @pytest.mark.parametrize("lengths", [[300], [0, 1, 63, 64, 65, 129, 200]])
-def test_bf16_ragged_and_varlen(lengths, chunk):
+def test_bf16_ragged_and_varlen(lengths, chunk, tc_path):
     w = W["prefill_T8192_H96_d128_bf16"]
     d = inputs.make_prefill(w, seed=1, device=DEV, lengths=lengths, heads=3)
     out, fin = _run(d, chunk)
@@ -61,14 +69,14 @@ def test_fp32_head_dims(dk, dv):
     assert_close(fin, rf, "f32", "final_state")
 
 
-def test_empty_sequence_passes_state_through():
+def test_empty_sequence_passes_state_through(tc_path):
     w = W["prefill_T8192_H96_d128_bf16"]
     d = inputs.make_prefill(w, seed=3, device=DEV, lengths=[0, 5, 0], heads=2)
     out, fin = _run(d)
     assert torch.equal(fin[0], d["init_state"][0]) and torch.equal(fin[2], d["init_state"][2])
 
 
-def test_final_state_may_alias_init_state():
+def test_final_state_may_alias_init_state(tc_path):
     w = W["prefill_T8192_H96_d128_bf16"]
     d = inputs.make_prefill(w, seed=4, device=DEV, lengths=[90], heads=2)
     ref_out, ref_fin = _run(d)
@@ -79,7 +87,7 @@ def test_final_state_may_alias_init_state():
     assert torch.equal(out, ref_out) and torch.equal(s, ref_fin)
 
 
-def test_deterministic():
+def test_deterministic(tc_path):
     w = W["prefill_T8192_H96_d128_bf16"]
     d = inputs.make_prefill(w, seed=5, device=DEV, lengths=[200, 77], heads=4)
     o1, f1 = _run(d)
@@ -87,7 +95,7 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
 
 
-def test_prefill_8k_full_size():
+def test_prefill_8k_full_size(tc_path):
     """H=96, T=8192, bf16, random initial state: every head checked."""
     w = W["prefill_T8192_H96_d128_bf16"]
     d = inputs.make_prefill(w, seed=0, device=DEV)
@@ -112,7 +120,9 @@ def test_varlen_32seq_full_size_sampled():
 
 def test_prefill_1m_full_size_sampled():
     """T = 1,048,576, H=32, saturated a in [-8, 8]: one head followed by the
-    oracle end to end (outputs and final state)."""
+    oracle end to end (outputs and final state).  The split path runs it in
+    windows of chunks (its record buffer is capped), carrying the state."""
+    assert kda.algorithm(1, 1 << 20, 32, 128, 128) == "tcgen05_split"
     w = W["prefill_T1M_H32_d128_bf16"]
     d = inputs.make_prefill(w, seed=0, device=DEV)
     out, fin = _run(d)
@@ -121,3 +131,25 @@ def test_prefill_1m_full_size_sampled():
     hs = torch.tensor(heads, device=DEV)
     assert_close(fin[:, hs], rf, "bf16", "final_state")
     assert_close(out[:, hs], ro, "bf16", "out")
+
+
+@pytest.mark.parametrize("with_final", [True, False])
+def test_split_windows_with_minimum_workspace(with_final):
+    """The split path with a workspace that holds one record per pair: one
+    chunk per window, the state carried between windows (in final_state, or
+    in the workspace when no final state is asked for)."""
+    w = W["prefill_T8192_H96_d128_bf16"]
+    lengths = [300, 70, 0, 129, 64]
+    d = inputs.make_prefill(w, seed=6, device=DEV, lengths=lengths, heads=3)
+    N, H = len(lengths), 3
+    order = (N * 4 + 255) // 256 * 256
+    ws = torch.empty(order + N * H * 128 * 128 * 4 + N * H * 66048, dtype=torch.uint8,
+                     device=DEV)
+    out, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                             d["cu_seqlens"], chunk=64, workspace=ws,
+                             output_final_state=with_final)
+    torch.cuda.synchronize()
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "out")
+    if with_final:
+        assert_close(fin, rf, "bf16", "final_state")
