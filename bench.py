@@ -314,37 +314,13 @@ def run_gpu(args):
             "frac": ck_bytes / (ck_ms * 1e-3) / 1e9 / hbm_peak}
     del d, args_pf, out, fin, ck_buf, ck_offs
     torch.cuda.empty_cache()
-    if args.only == "prefill":
-        return
-
-    # ---------------- decode ----------------
-    wd = inputs.WORKLOADS[DECODE]
-    N, Hd = wd.n_seqs, wd.heads
-    state = inputs.make_decode_state(wd, seed=rank, device=dev)
-    toks = [inputs.make_decode_tokens(wd, s, seed=rank, device=dev)
-            for s in range(wd.decode_steps)]
-    dout = torch.empty((N, Hd, wd.dv), dtype=wd.torch_dtype, device=dev)
-    for s in range(3):
-        kda.decode_step(*toks[s], state, out=dout)
-    barrier()
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(wd.decode_steps)]
-    start.record(stream)
-    for s in range(wd.decode_steps):
-        dev_ev[s][0].record(stream)
-        kda.decode_step(*toks[s], state, out=dout)
-        dev_ev[s][1].record(stream)
-    end.record(stream)
-    barrier()
-    dec_ms = max_over_ranks(start.elapsed_time(end)) / wd.decode_steps
-    dec_kern_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
-    dec_bytes = decode_bytes(N, Hd, wd.dk, wd.dv)
-    dec_gbs = dec_bytes / (dec_kern_ms * 1e-3) / 1e9
-    dec_traffic = kernel_traffic("kda_recurrent.cu", "decode_step_64x96.md")
-
+    decode = None
+    if args.only != "prefill":
+        decode = run_decode_leg(args, dev, rank, world, start, end, stream, barrier,
+                                max_over_ranks, hbm_peak)
     # ---------------- CPU baseline (oracle, rank 0, N=1 only) ----------------
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only != "prefill":
         import oracle
         ws = inputs.WORKLOADS[PREFILL]
         dc = inputs.make_prefill(ws, seed=0, device="cpu")
@@ -379,20 +355,54 @@ def run_gpu(args):
             "gpu_launches": args.steps * launches,
             "clocks": clocks,
             "prefill_checkpoints": ckpt,
-            "decode": {"workload": DECODE, "value": job_throughput(world, N, dec_ms),
-                       "unit": "tok/s", "ms_per_step": dec_ms, "steps": wd.decode_steps,
-                       "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
-                                    "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-                                    "algorithmic_bytes_per_launch": dec_bytes,
-                                    "kernel": "kda_recurrent (one token)",
-                                    "traffic": dec_traffic,
-                                    "kernel_ms": dec_kern_ms},
-                       "gpu_launches": wd.decode_steps},
+            "decode": decode,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_decode_leg(args, dev, rank, world, start, end, stream, barrier, max_over_ranks,
+                   hbm_peak):
+    """The decode workload: 64 consecutive steps over resident states."""
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    wd = inputs.WORKLOADS[DECODE]
+    N, Hd = wd.n_seqs, wd.heads
+    state = inputs.make_decode_state(wd, seed=rank, device=dev)
+    toks = [inputs.make_decode_tokens(wd, s, seed=rank, device=dev)
+            for s in range(wd.decode_steps)]
+    dout = torch.empty((N, Hd, wd.dv), dtype=wd.torch_dtype, device=dev)
+    for s in range(3):
+        kda.decode_step(*toks[s], state, out=dout)
+    barrier()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(wd.decode_steps)]
+    start.record(stream)
+    for s in range(wd.decode_steps):
+        dev_ev[s][0].record(stream)
+        kda.decode_step(*toks[s], state, out=dout)
+        dev_ev[s][1].record(stream)
+    end.record(stream)
+    barrier()
+    dec_ms = max_over_ranks(start.elapsed_time(end)) / wd.decode_steps
+    dec_kern_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = decode_bytes(N, Hd, wd.dk, wd.dv)
+    dec_gbs = dec_bytes / (dec_kern_ms * 1e-3) / 1e9
+    dec_traffic = kernel_traffic("kda_recurrent.cu", "decode_step_64x96.md")
+
+    return {"workload": DECODE, "value": job_throughput(world, N, dec_ms),
+            "unit": "tok/s", "ms_per_step": dec_ms, "steps": wd.decode_steps,
+            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+                         "algorithmic_bytes_per_launch": dec_bytes,
+                         "kernel": "kda_recurrent (one token)",
+                         "traffic": dec_traffic,
+                         "kernel_ms": dec_kern_ms},
+            "gpu_launches": wd.decode_steps}
 
 
 def run_decode_only(args, dev):

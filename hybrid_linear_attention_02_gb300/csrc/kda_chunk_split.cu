@@ -16,16 +16,21 @@
 //    iteration, over every chunk of every pair at once.  It runs the
 //    state-independent chain (cumulative decay, scaled operand tiles, the
 //    masked products A and P in one MMA, T by block-Neumann inversion,
-//    W^T = Ktil^T T'^T by MMA) and writes one 66,048-byte record per chunk:
-//    the byte images of the operand tiles the state pass reads (-W^T, Qtil,
-//    Kbar, P, T' = T diag(beta)) and e^{G_C}.
+//    W = T' Ktil by MMA) and writes one 66,048-byte record per chunk: the
+//    byte images of the operand tiles the state pass reads (Qtil, -W,
+//    Kbar^T, P, T' = T diag(beta)) and e^{G_C}.
 //  chunk_state_kernel: one CTA per pair walks its chunks in order; a producer
 //    warp streams records (1-D bulk copies) and v tiles (TMA) into a two-slot
-//    ring, four warps run the state pass with the fp32 state resident in TMEM:
-//      U^T = V^T T'^T + S^T (-W)^T,  O^T = S^T Qtil^T     (MMA)
-//      S^T += U^T Kbar,  O^T += U^T P^T                    (MMA)
-//    and fold the next chunk's decay Diag(e^{G_C}) into the pass that makes
-//    the bf16 operand copy of the new state.
+//    ring, one warp issues every MMA, and eight warps (two per TMEM lane
+//    quarter, each on half the columns) convert between the fp32 state
+//    resident in TMEM and the bf16 operands:
+//      U0^T = V^T T'^T                                     (MMA0, off the chain)
+//      [O^T | U^T] = S^T [Qtil; -W]^T,  U^T += U0^T         (MMA1, N = 128)
+//      [S^T | O^T] += U^T [Kbar^T; P]^T                     (MMA2, N = 192)
+//    The serial chain per chunk is MMA1 -> U^T to bf16 -> MMA2 -> S^T to
+//    bf16 (with the next chunk's decay Diag(e^{G_C}) applied to the fp32
+//    copy in the same pass); the previous chunk's output stores run while
+//    MMA1 executes.
 //
 // Records of a window of chunk indices [cw0, cw1) (per sequence) are laid out
 // [sequence][head][chunk]; a long input runs as several windows with the
@@ -44,11 +49,13 @@ using namespace sm100;
 using namespace chunk;
 
 // ---- one chunk record: shared-memory operand images, 1024-aligned tiles.
-constexpr uint32_t kRecW = 0;        // -W^T  128 x 64, rows = key channel (MN-major B)
-constexpr uint32_t kRecQ = 16384;    // Qtil   64 x 128 (K-major B)
-constexpr uint32_t kRecK = 32768;    // Kbar   64 x 128 (MN-major B)
-constexpr uint32_t kRecP = 49152;    // P      64 x 64  (K-major B)
-constexpr uint32_t kRecT = 57344;    // T'     64 x 64  (K-major B)
+// WQ: K-major B operand, N = 128 rows (rows 0..63 Qtil, rows 64..127 -W, one
+//     per token) by K = 128 key channels; two 16 KB channel panels.
+// KP: K-major B operand, N = 192 rows by K = 64 tokens: Kbar^T (rows 0..127,
+//     one per key channel), then P (rows 128..191, one per output token).
+constexpr uint32_t kRecWQ = 0;       // [Qtil; -W]        128 x 128
+constexpr uint32_t kRecKP = 32768;   // [Kbar^T; P]       192 x 64
+constexpr uint32_t kRecT = 57344;    // T' = T diag(beta) 64 x 64  (K-major B)
 constexpr uint32_t kRecG = 65536;    // e^{G_C}, fp32 [128]
 constexpr uint32_t kRecBytes = 66048;
 constexpr uint32_t kRecSlot = 66560; // slot stride in shared memory (1024-aligned)
@@ -57,10 +64,12 @@ static_assert(kRecBytes == kSplitRecordBytes, "record size seen by the host");
 // ---------------------------------------------------------------- prep kernel
 constexpr int kPThreads = 256;
 constexpr uint32_t kPOffKQ = 0;        // [K';Q'] 128 x 128; raw k at 0, raw q at 16384
-constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W^T
+constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W
 constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128; raw g before P2
-constexpr uint32_t kPOffTB = 90112;    // T' 64 x 64; tile sums and e^{R_a} tables in P1/P2
-constexpr uint32_t kPTiles = 98304;
+// TB: tile sums and e^{R_a} tables (P1/P2), then Kbar^T (P2..P4), then
+// [T'; 0] 128 x 64, the A operand of W = T' Ktil (rows 64..127 zero).
+constexpr uint32_t kPOffTB = 90112;
+constexpr uint32_t kPTiles = 106496;
 constexpr uint32_t kPSmem = kPTiles + 1024;
 constexpr uint32_t kPOffTileTot = kPOffTB;          // fp32 [4][128]
 constexpr uint32_t kPOffTabR = kPOffTB + 2048;      // fp32 [2][4][128]
@@ -72,23 +81,43 @@ constexpr uint32_t kPOffN = kPOffD + 4 * 16 * kLdB * 4;    // N   6 x 16 x 20
 constexpr uint32_t kPOffN2 = kPOffN + 6 * 16 * kLdB * 4;   // N^2 3 x 16 x 20
 constexpr uint32_t kPOffN3 = kPOffN2 + 3 * 16 * kLdB * 4;  // N^3 16 x 20
 static_assert(kPOffN3 + 16 * kLdB * 4 <= kPOffKH + 40960, "inverse scratch fits");
-constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W^T reuses 0..63
+constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W (lanes 0..63) reuses 0..127
 enum { kPBarAP = 0, kPBarW, kPBarRaw, kPNumBars };
 
 // ---------------------------------------------------------------- state kernel
-constexpr int kSThreads = 160;             // warps 0..3 state pass, warp 4 producer
+constexpr int kSStateWarps = 8;            // warps 0..7: state pass (TMEM <-> registers)
+constexpr int kSStateThreads = 32 * kSStateWarps;
+constexpr int kSProducerWarp = 8;          // records and v tiles into the ring
+constexpr int kSMmaWarp = 9;               // issues every MMA
+constexpr int kSThreads = 32 * 10;
 constexpr uint32_t kSOffRec = 0;           // 2 record slots
 constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
-constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging, row-major bf16 64 x 128
-constexpr uint32_t kSTiles = kSOffO + 16384;
+constexpr uint32_t kSTiles = kSOffV + 2 * 16384;
 constexpr uint32_t kSSmem = kSTiles + 1024;
 constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (lane = value column, column = key row)
-constexpr uint32_t kSColSB = 128;  // 64: bf16 S^T, A operand
-constexpr uint32_t kSColUT = 192;  // 32: bf16 U^T, A operand
-constexpr uint32_t kSColU = 224;   // 64 fp32: U^T
-constexpr uint32_t kSColO = 288;   // 64 fp32: O^T
+constexpr uint32_t kSColO = 128;   // 64 fp32: O^T  (MMA2 writes [S^T | O^T])
+constexpr uint32_t kSColU = 192;   // 64 fp32: U^T  (MMA1 writes [O^T | U^T])
+constexpr uint32_t kSColSB = 256;  // 64: bf16 S^T, A operand
+constexpr uint32_t kSColUT = 320;  // 32: bf16 U^T, A operand
+constexpr uint32_t kSColU0 = 352;  // 2 x 64 fp32: U0^T = V^T T'^T, by chunk parity
 constexpr uint32_t kSTmemCols = 512;
-enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSNumBars };
+enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSBarSB,
+       kSBarUT, kSNumBars };
+
+#ifdef KDA_PHASE_PROFILE
+// Per-phase SM-clock totals of two state-pass threads of CTA (0, 0)
+// (instrumentation builds only).
+__device__ unsigned long long kda_split_clocks[32];
+__device__ unsigned long long kda_prep_clocks[32];
+#define KDA_SMARK(i)                                  \
+  do {                                                \
+    const unsigned long long now_ = clock64();        \
+    prof_acc[i] += now_ - prof_t;                     \
+    prof_t = now_;                                    \
+  } while (0)
+#else
+#define KDA_SMARK(i) ((void)0)
+#endif
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -158,13 +187,6 @@ __device__ __forceinline__ Item decode_item(const LaunchArgs& a, const SplitWind
   r.c = w.cw0 + local % nck;
   seq_bounds(a, lo, r.t0, r.t1);
   return r;
-}
-
-// 8 floats -> bf16 at (row, col) of a 128B-swizzled tile image in global memory.
-__device__ __forceinline__ void st_gtile8(uint8_t* tile, int row, int col, int rows,
-                                          const float (&f)[8]) {
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
-      make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
 __global__ void __launch_bounds__(kPThreads, 2)
@@ -250,6 +272,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
   load_beta(cur);
 
   uint32_t k_iter = 0;
+#ifdef KDA_PHASE_PROFILE
+  unsigned long long prof_acc[16] = {}, prof_t = clock64();
+#endif
 #pragma unroll 1
   for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k_iter) {
     const uint32_t par = k_iter & 1;
@@ -268,7 +293,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
       if (cg == 0) s_beta[row0 + m] = rb[m];
     if (it_next < n_items) load_beta(nxt);
     named_bar(2, kPThreads);
+    KDA_SMARK(0);
     const bool ok_raw = sync.wait(kPBarRaw, par);
+    KDA_SMARK(1);
 
     uint4 rq[4], rk[4];
     float G[4][8];
@@ -309,6 +336,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     // Tile sums are visible, and every raw read is done before the tiles are rewritten.
     named_bar(2, kPThreads);
+    KDA_SMARK(2);
     // ---- Per-(tile, channel) factors, thread p <-> channel p; split layout as in
     // the fused kernel, so the 16-byte reads below are conflict-free.
     if (p < kD) {
@@ -335,6 +363,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
     }
     named_bar(2, kPThreads);
+    KDA_SMARK(3);
 
     // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
     {
@@ -355,12 +384,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
             make_uint4(v[0], v[1], v[2], v[3]);
       };
       uint64_t kh[4][4];
+      uint32_t okb[4][4];   // Kbar rows of this thread (bf16 pairs)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int r = row0 + m, rl = 4 * r4 + m;
         const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
         const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
-        uint32_t okp[4], oqp[4], okt[4], oqt[4], okh[4], okb[4];
+        uint32_t okp[4], oqp[4], okt[4], okh[4], oqt[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
@@ -374,14 +404,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
           oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
           kh[m][w] = f2_mul(kp, ei);
           okh[w] = f2_to_bf16x2(kh[m][w]);
-          okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
+          okb[m][w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
         }
         st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
         st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
         st4(smem + kPOffKT, r, 64, okt);
         st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
-        st4(rec + kRecQ, r, 64, oqt);
-        st4(rec + kRecK, r, 64, okb);
+        st4(rec + kRecWQ, r, 128, oqt);
       }
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
@@ -399,9 +428,26 @@ __global__ void __launch_bounds__(kPThreads, 2)
           }
         }
       }
+      // Kbar^T (row = key channel, 4 tokens row0 .. row0 + 3 per 8-byte
+      // piece) replaces the factor tables once every thread has read them.
+      named_bar(2, kPThreads);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t sel = e ? 0x7632u : 0x5410u;
+          *reinterpret_cast<uint2*>(smem + kPOffTB + sw128_off(8 * cg + 2 * w + e, row0, 128)) =
+              make_uint2(__byte_perm(okb[0][w], okb[1][w], sel),
+                         __byte_perm(okb[2][w], okb[3][w], sel));
+        }
     }
     fence_async_smem();
     named_bar(2, kPThreads);
+    if (leader && !s_abort) {
+      bulk_store(rec + kRecKP, smem + kPOffTB, 16384);
+      bulk_commit();
+    }
+    KDA_SMARK(4);
 
     // ---- P3: every masked intra-chunk product in one MMA (M=128, N=160, K=128).
     if (leader && !s_abort) {
@@ -416,6 +462,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     const bool ok_ap = sync.wait(kPBarAP, par);
     tc_fence_after();
+    KDA_SMARK(5);
 
     // ---- P4: A (x beta, strictly lower; fp32, shared) and P (lower inclusive;
     // bf16, straight to the record).
@@ -444,7 +491,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
             float f8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
-            st_gtile8(rec + kRecP, r, 16 * blk + 8 * h8, 64, f8);
+            st_tile8(rec + kRecKP, 128 + r, 16 * blk + 8 * h8, 192, f8);
           }
         } else {
 #pragma unroll
@@ -454,8 +501,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
       }
     }
+    // Kbar^T has left the TB tile before P5 writes T' there.
+    if (leader) bulk_wait_read_all();
     tc_fence_before();
     named_bar(2, kPThreads);
+    KDA_SMARK(6);
 
     // ---- P5: T = (I + A)^-1 = (I - N + N^2 - N^3) D in fp32, written as
     // T' = T diag(beta) in bf16 (same block scheme as the fused kernel).
@@ -494,8 +544,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         st_tile8(smem + kPOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
       }
+      // Rows 64..127 of the [T'; 0] operand.
+      for (int e = p - 64; e < 512; e += kPThreads - 64)
+        *reinterpret_cast<uint4*>(smem + kPOffTB + 8192 + 16 * e) = make_uint4(0, 0, 0, 0);
     }
     named_bar(2, kPThreads);
+    KDA_SMARK(7);
     auto tile16 = [&](const float* X, int xs, const float* Y, int ys, int i4, int j4,
                       float (&acc)[4][4]) {
       float4 yv[16], xv[4][4];
@@ -545,6 +599,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       st_tile8(smem + kPOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
     }
     named_bar(2, kPThreads);
+    KDA_SMARK(8);
     // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
     if (p < 48) {
       const int k2 = p >> 4;
@@ -555,6 +610,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       store_tile(N2m + k2 * 16 * kLdB, i4, j4, acc);
     }
     named_bar(2, kPThreads);
+    KDA_SMARK(9);
     // Step 3: N^3 block (3,0); M = -N + N^2 in place for (1,0) (2,0) (2,1) (3,1).
     if (p < 16) {
       float acc[4][4] = {};
@@ -577,6 +633,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       }
     }
     named_bar(2, kPThreads);
+    KDA_SMARK(10);
     // Step 4: T_ab = M_ab D_bb, times beta, into T' (M_30 = -N30 + N^2_30 - N^3_30).
     if (p < 96) {
       const int blk = p >> 4;
@@ -615,37 +672,41 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     fence_async_smem();
     named_bar(2, kPThreads);
+    KDA_SMARK(11);
 
-    // ---- P6: W^T = Ktil^T T'^T (M=128, N=64, K=64), into TMEM columns 0..63.
+    // ---- P6: [W; 0] = [T'; 0] Ktil (M=128, N=128, K=64): W rows in TMEM
+    // lanes 0..63, columns 0..127.
     if (leader && !s_abort) {
       tc_fence_after();
-      const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
-      const uint32_t aKT = smem_u32(smem + kPOffKT), bT = smem_u32(smem + kPOffTB);
+      const uint32_t idesc = umma_idesc_bf16(128, 128, 0, 1);
+      const uint32_t aT = smem_u32(smem + kPOffTB), bKT = smem_u32(smem + kPOffKT);
 #pragma unroll
       for (int t = 0; t < 4; ++t)
-        umma_bf16(tbase, umma_desc(aKT + t * 2048, 64 * 128, 1024),
-                  umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
+        umma_bf16(tbase, umma_desc(aT + t * 32, 16, 1024),
+                  umma_desc(bKT + t * 2048, 64 * 128, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarW]);
     }
     const bool ok_w = sync.wait(kPBarW, par);
     tc_fence_after();
+    KDA_SMARK(12);
     // [K';Q'] and Ktil are dead: the next item's raw tiles may land.
     if (loader && ok_w && it_next < n_items) issue_raw(nxt);
 
-    // ---- P7: -W^T (rows = key channel, columns = token) staged where Khat was.
-    if (pw < 4 && ok_w) {
-      const int cc = 32 * pw + lane;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+    // ---- P7: -W (row = token, column = key channel) staged where Khat was;
+    // its two 64-channel panels are rows 64..127 of the record's WQ panels.
+    if (pw < 2 && ok_w) {
+      const int t = 32 * pw + lane;
+#pragma unroll 1
+      for (int q32 = 0; q32 < 4; ++q32) {
         float w[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(32 * pw) << 16) + 32 * half, w);
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * pw) << 16) + 32 * q32, w);
         tmem_ld_wait();
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           float f8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) f8[u] = -w[8 * q8 + u];
-          st_tile8(smem + kPOffKH, cc, 32 * half + 8 * q8, 128, f8);
+          st_tile8(smem + kPOffKH, t, 32 * q32 + 8 * q8, 64, f8);
         }
       }
     }
@@ -653,12 +714,20 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_before();
     named_bar(2, kPThreads);
     if (leader && !s_abort) {
-      bulk_store(rec + kRecW, smem + kPOffKH, 16384);
+      bulk_store(rec + kRecWQ + 8192, smem + kPOffKH, 8192);
+      bulk_store(rec + kRecWQ + 16384 + 8192, smem + kPOffKH + 8192, 8192);
       bulk_store(rec + kRecT, smem + kPOffTB, 8192);
       bulk_commit();
     }
+    KDA_SMARK(13);
     cur = nxt;
   }
+#ifdef KDA_PHASE_PROFILE
+  if (blockIdx.x == 0 && (p == 0 || p == 160)) {
+    for (int i = 0; i < 14; ++i) kda_prep_clocks[(p ? 16 : 0) + i] = prof_acc[i];
+    if (p == 0) kda_prep_clocks[31] = k_iter;
+  }
+#endif
   if (leader) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
@@ -715,7 +784,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t tbase = s_tmem;
   Sync sync{s_bars, &s_abort};
 
-  if (warp == 4) {
+  if (warp == kSProducerWarp) {
     // ================================ producer ================================
     if (lane == 0) {
       prefetch_tmap(&tm_v);
@@ -736,204 +805,238 @@ __global__ void __launch_bounds__(kSThreads, 1)
           tma_load_3d(smem + kSOffV + s * 16384 + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
       }
     }
+  } else if (warp == kSMmaWarp) {
+    // ================================ MMA issue ===============================
+    if (lane == 0) {
+      // U0^T = V^T T'^T of the chunk in slot s, into U0 buffer s (state-independent).
+      auto issue_mma0 = [&](int s) {
+        const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
+        const uint32_t aV = smem_u32(smem + kSOffV + s * 16384);
+        const uint32_t bT = smem_u32(smem + kSOffRec + s * kRecSlot + kRecT);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          umma_bf16(tbase + kSColU0 + 64 * s, umma_desc(aV + t * 2048, 64 * 128, 1024),
+                    umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
+      };
+      bool ok = sync.wait(kSBarFull0, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_mma0(0);
+      }
+#pragma unroll 1
+      for (int c = 0; c < nck && ok; ++c) {
+        const int s = c & 1;
+        const uint8_t* slot = smem + kSOffRec + s * kRecSlot;
+        // [O^T | U^T] = S^T [Qtil^T | -W^T]      (M = 128, N = 128, K = dk = 128)
+        if (!sync.wait(kSBarSB, c & 1)) break;
+        tc_fence_after();
+        {
+          const uint32_t idesc = umma_idesc_bf16(128, 128, 0, 0);
+          const uint32_t bWQ = smem_u32(slot + kRecWQ);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            umma_bf16_tmem_a(tbase + kSColO, tbase + kSColSB + 8 * t,
+                             umma_desc(bWQ + (t >> 2) * 16384 + (t & 3) * 32, 16, 1024), idesc,
+                             t > 0);
+          umma_commit(&s_bars[kSBarMMA1]);
+        }
+        // [S^T | O^T] += U^T [Kbar^T; P]^T        (M = 128, N = 192, K = 64 tokens)
+        if (!sync.wait(kSBarUT, c & 1)) break;
+        tc_fence_after();
+        {
+          const uint32_t idesc = umma_idesc_bf16(128, 192, 0, 0);
+          const uint32_t bKP = smem_u32(slot + kRecKP);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            umma_bf16_tmem_a(tbase + kSColS, tbase + kSColUT + 8 * t,
+                             umma_desc(bKP + t * 32, 16, 1024), idesc, 1);
+          umma_commit(&s_bars[kSBarEmpty0 + s]);
+          umma_commit(&s_bars[kSBarMMA2]);
+        }
+        // The next chunk's U0^T runs while the state warps convert S^T.
+        if (c + 1 < nck) {
+          if (!sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1)) break;
+          tc_fence_after();
+          issue_mma0(s ^ 1);
+        }
+      }
+    }
   } else {
     // =============================== state pass ===============================
-    const int j = tid;                                  // TMEM lane = value column
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    // Warp w reads TMEM lanes 32 (w & 3) .. + 31 (value columns j) and the
+    // column half hf = w >> 2 of every TMEM matrix.
+    const int q = warp & 3, hf = warp >> 2;
+    const int j = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
 
-    // S^T[j][c] = S[c][j]: fp32 copy (decayed below) and bf16 operand copy.
+    // S^T[j][c] = S[c][j] for key rows c of this half: fp32 copy and bf16 copy.
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 0; cb < 2; ++cb) {
+      const int c0 = 64 * hf + 32 * cb;
       uint32_t f[32], b[16];
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        f[u] = __float_as_uint(src ? __ldcs(src + soff + (32 * cb + u) * kD + j) : 0.f);
+        f[u] = __float_as_uint(src ? __ldcs(src + soff + (c0 + u) * kD + j) : 0.f);
 #pragma unroll
       for (int u = 0; u < 16; ++u)
         b[u] = pack2(__uint_as_float(f[2 * u]), __uint_as_float(f[2 * u + 1]));
-      tmem_st32(tbase + lane_base + kSColS + 32 * cb, f);
-      tmem_st16(tbase + lane_base + kSColSB + 16 * cb, b);
+      tmem_st32(tbase + lane_base + kSColS + c0, f);
+      tmem_st16(tbase + lane_base + kSColSB + c0 / 2, b);
     }
-    tmem_st_wait();
-    // The fp32 state carries the first chunk's decay before its first update.
+    // Outputs of chunk cl held as O^T column j, rows 32 hf .. + 31, in `ov`:
+    // lane pairs swap values so each lane writes two adjacent columns of
+    // every other row (4-byte stores).
+    float ov[32];
+    auto emit_out = [&](int cl) {
+      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      const bool odd = lane & 1;
+      __nv_bfloat16* base = gout + (c0 * H + h) * kD + (j & ~1);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float a = ov[2 * k], b = ov[2 * k + 1];
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
+        const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+        const uint32_t pk = odd ? pack2(other, b) : pack2(a, other);
+        if (r < L) *reinterpret_cast<uint32_t*>(base + static_cast<long long>(r) * H * kD) = pk;
+      }
+    };
+
+    // The fp32 state carries the first chunk's decay Diag(e^{G_C}) before
+    // MMA2 adds onto it (later chunks get theirs in step E).
     bool ok = sync.wait(kSBarFull0, 0);
+    tmem_st_wait();
     if (ok) {
       const float* gam = reinterpret_cast<const float*>(smem + kSOffRec + kRecG);
 #pragma unroll 1
-      for (int cb = 0; cb < 8; ++cb) {
-        float v[16];
-        tmem_ld16(tbase + lane_base + kSColS + 16 * cb, v);
+      for (int cb = 0; cb < 2; ++cb) {
+        const int c0 = 64 * hf + 32 * cb;
+        float v[32];
+        tmem_ld32(tbase + lane_base + kSColS + c0, v);
         tmem_ld_wait();
-        uint32_t f[16];
+        uint32_t f[32];
 #pragma unroll
-        for (int u = 0; u < 16; u += 4) {
-          const float4 gm = *reinterpret_cast<const float4*>(&gam[16 * cb + u]);
+        for (int u = 0; u < 32; u += 4) {
+          const float4 gm = *reinterpret_cast<const float4*>(&gam[c0 + u]);
           f[u] = __float_as_uint(v[u] * gm.x);
           f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
           f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
           f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
         }
-        tmem_st16(tbase + lane_base + kSColS + 16 * cb, f);
+        tmem_st32(tbase + lane_base + kSColS + c0, f);
       }
     }
     tmem_st_wait();
     tc_fence_before();
-    named_bar(1, 128);
-
-    // U^T = V^T T'^T for the chunk in slot s (state-independent).
-    auto issue_mma0 = [&](int s) {
-      const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
-      const uint32_t aV = smem_u32(smem + kSOffV + s * 16384);
-      const uint32_t bT = smem_u32(smem + kSOffRec + s * kRecSlot + kRecT);
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        umma_bf16(tbase + kSColU, umma_desc(aV + t * 2048, 64 * 128, 1024),
-                  umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
-    };
-    auto store_out = [&](int cl) {
-      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
-      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
-      __nv_bfloat16* dsto = gout + (c0 * H + h) * kD;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = j + 128 * i, r = e >> 4, ch = e & 15;
-        if (r < L)
-          *reinterpret_cast<uint4*>(dsto + static_cast<long long>(r) * H * kD + 8 * ch) =
-              *reinterpret_cast<const uint4*>(smem + kSOffO + r * 256 + ch * 16);
-      }
-    };
-    if (j == 0 && ok) {
-      tc_fence_after();
-      issue_mma0(0);
-    }
+    named_bar(1, kSStateThreads);
+    if (tid == 0) mbar_arrive(&s_bars[kSBarSB]);
     bool prev_ok = false;
+#ifdef KDA_PHASE_PROFILE
+    unsigned long long prof_acc[10] = {}, prof_t = clock64();
+#endif
 
 #pragma unroll 1
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
-      uint8_t* slot = smem + kSOffRec + s * kRecSlot;
-      if (j == 0 && ok && !s_abort) {
-        tc_fence_after();
-        // U^T += S^T (-W)^T ;  O^T = S^T Qtil^T      (K = dk = 128)
-        const uint32_t iU = umma_idesc_bf16(128, 64, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
-        const uint32_t bW = smem_u32(slot + kRecW), bQ = smem_u32(slot + kRecQ);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint32_t aS = tbase + kSColSB + 8 * t;
-          umma_bf16_tmem_a(tbase + kSColU, aS, umma_desc(bW + t * 2048, 128 * 128, 1024), iU, 1);
-          umma_bf16_tmem_a(tbase + kSColO, aS,
-                           umma_desc(bQ + (t >> 2) * 64 * 128 + (t & 3) * 32, 16, 1024), iO,
-                           t > 0);
-        }
-        umma_commit(&s_bars[kSBarMMA1]);
-      }
-      // The previous chunk's outputs leave while MMA1 runs.
-      if (c > 0 && prev_ok) store_out(c - 1);
+      // (B) While MMA1 runs: the previous chunk's outputs.
+      if (__all_sync(0xFFFFFFFFu, c > 0 && prev_ok)) emit_out(c - 1);
+      KDA_SMARK(0);
+      // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
       const bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
       tc_fence_after();
+      KDA_SMARK(1);
       if (ok1) {
+        float v[32], w[32];
+        tmem_ld32(tbase + lane_base + kSColU + 32 * hf, v);
+        tmem_ld32(tbase + lane_base + kSColU0 + 64 * s + 32 * hf, w);
+        tmem_ld_wait();
+        uint32_t b[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld32(tbase + lane_base + kSColU + 32 * half, v);
-          tmem_ld_wait();
-          uint32_t b[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
-          tmem_st16(tbase + lane_base + kSColUT + 16 * half, b);
-        }
+        for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u] + w[2 * u], v[2 * u + 1] + w[2 * u + 1]);
+        tmem_st16(tbase + lane_base + kSColUT + 16 * hf, b);
       }
       tmem_st_wait();
       tc_fence_before();
-      named_bar(1, 128);
+      KDA_SMARK(2);
+      named_bar(1, kSStateThreads);
+      if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
+      KDA_SMARK(3);
+      KDA_SMARK(4);
+      // (E) Outputs to registers; new state -> bf16 operand copy (the serial
+      // step) and, for the next chunk, the decayed fp32 state; checkpoints;
+      // then hand the state to the next MMA1.
       const bool has_next = c + 1 < nck;
-      if (j == 0 && ok1 && !s_abort) {
-        tc_fence_after();
-        // S^T += U^T Kbar (K = 64 tokens) ;  O^T += U^T P^T
-        const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
-        const uint32_t bK = smem_u32(slot + kRecK), bP = smem_u32(slot + kRecP);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t aU = tbase + kSColUT + 8 * t;
-          umma_bf16_tmem_a(tbase + kSColS, aU, umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
-          umma_bf16_tmem_a(tbase + kSColO, aU, umma_desc(bP + t * 32, 16, 1024), iO, 1);
-        }
-        umma_commit(&s_bars[kSBarEmpty0 + s]);
-        umma_commit(&s_bars[kSBarMMA2]);
-        // The next chunk's U^T = V^T T'^T queues behind MMA2 (U^T is free).
-        if (has_next && sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1)) {
-          tc_fence_after();
-          issue_mma0(s ^ 1);
-        }
-      }
       const bool ok_next = !has_next || sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1);
       const bool ok2 = ok1 && sync.wait(kSBarMMA2, c & 1);
       tc_fence_after();
+      KDA_SMARK(5);
       if (ok2) {
+        const bool decay = has_next && ok_next;
+        const float* gam =
+            reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot + kRecG);
+        tmem_ld32(tbase + lane_base + kSColO + 32 * hf, ov);
         const long long done = static_cast<long long>(win.cw0 + c + 1) * kC;
         float* ck = nullptr;
         if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
           const long long row = args.ckpt_offsets[n] + done / args.ckpt_interval - 1;
           ck = args.ckpt + (row * H + h) * kD * kD + j;
         }
-        const bool decay = has_next && ok_next;
-        const float* gam =
-            reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot + kRecG);
-        // New state -> bf16 operand copy, and (for the next chunk) the decayed
-        // fp32 state; O^T column j -> row-major staging.
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < 2; ++cb) {
+          const int c0 = 64 * hf + 32 * cb;
           float v[32];
-          tmem_ld32(tbase + lane_base + kSColS + 32 * cb, v);
+          tmem_ld32(tbase + lane_base + kSColS + c0, v);
           tmem_ld_wait();
-          if (ck) {
-#pragma unroll
-            for (int u = 0; u < 32; ++u) __stcs(ck + (32 * cb + u) * kD, v[u]);
-          }
           uint32_t b[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
-          tmem_st16(tbase + lane_base + kSColSB + 16 * cb, b);
+          tmem_st16(tbase + lane_base + kSColSB + c0 / 2, b);
           if (decay) {
             uint32_t f[32];
 #pragma unroll
             for (int u = 0; u < 32; u += 4) {
-              const float4 gm = *reinterpret_cast<const float4*>(&gam[32 * cb + u]);
+              const float4 gm = *reinterpret_cast<const float4*>(&gam[c0 + u]);
               f[u] = __float_as_uint(v[u] * gm.x);
               f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
               f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
               f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
             }
-            tmem_st32(tbase + lane_base + kSColS + 32 * cb, f);
+            tmem_st32(tbase + lane_base + kSColS + c0, f);
+          }
+          if (ck) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) __stcs(ck + (c0 + u) * kD, v[u]);
           }
         }
-        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(smem + kSOffO) + j;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld32(tbase + lane_base + kSColO + 32 * half, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int r = 0; r < 32; ++r) so[(32 * half + r) * kD] = __float2bfloat16_rn(v[r]);
-        }
       }
+      KDA_SMARK(6);
       tmem_st_wait();
       tc_fence_before();
-      named_bar(1, 128);
+      KDA_SMARK(7);
+      named_bar(1, kSStateThreads);
+      if (tid == 0 && ok2 && ok_next && has_next) mbar_arrive(&s_bars[kSBarSB]);
+      KDA_SMARK(8);
       prev_ok = ok2;
       ok = ok2 && ok_next;
     }
-    if (prev_ok) store_out(nck - 1);
+#ifdef KDA_PHASE_PROFILE
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (tid == 0 || tid == 64)) {
+      for (int i = 0; i < 10; ++i) kda_split_clocks[(tid ? 10 : 0) + i] = prof_acc[i];
+      if (tid == 0) kda_split_clocks[30] = nck;
+    }
+#endif
+    if (__all_sync(0xFFFFFFFFu, prev_ok)) emit_out(nck - 1);
     if (!s_abort && dst) {
       // After the last chunk the fp32 state carries no further decay.
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
+        const int c0 = 64 * hf + 32 * cb;
         float v[32];
-        tmem_ld32(tbase + lane_base + kSColS + 32 * cb, v);
+        tmem_ld32(tbase + lane_base + kSColS + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) __stcs(dst + soff + (32 * cb + u) * kD + j, v[u]);
+        for (int u = 0; u < 32; ++u) __stcs(dst + soff + (c0 + u) * kD + j, v[u]);
       }
     }
   }
@@ -1005,5 +1108,14 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   }
   return cudaSuccess;
 }
+
+#ifdef KDA_PHASE_PROFILE
+extern "C" KDA_API int kda_debug_split_clocks(unsigned long long* host) {
+  cudaError_t e = cudaMemcpyFromSymbol(host, kda_split_clocks, sizeof(unsigned long long) * 32);
+  if (e == cudaSuccess)
+    e = cudaMemcpyFromSymbol(host + 32, kda_prep_clocks, sizeof(unsigned long long) * 32);
+  return static_cast<int>(e);
+}
+#endif
 
 }  // namespace kda
