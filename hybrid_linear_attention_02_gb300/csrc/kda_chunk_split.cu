@@ -92,7 +92,8 @@ constexpr int kSMmaWarp = 9;               // issues every MMA
 constexpr int kSThreads = 32 * 10;
 constexpr uint32_t kSOffRec = 0;           // 2 record slots
 constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
-constexpr uint32_t kSTiles = kSOffV + 2 * 16384;
+constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging 64 x 128 (TMA store image)
+constexpr uint32_t kSTiles = kSOffO + 16384;
 constexpr uint32_t kSSmem = kSTiles + 1024;
 constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (lane = value column, column = key row)
 constexpr uint32_t kSColO = 128;   // 64 fp32: O^T  (MMA2 writes [S^T | O^T])
@@ -285,9 +286,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
     Item nxt = cur;
     if (it_next < n_items) nxt = decode_item(args, win, s_cum, it_next);
 
-    // The previous item's bulk stores have read T' and -W^T out of shared
-    // memory before this item rewrites those tiles.
-    if (leader) bulk_wait_read_all();
+    // The previous item's T' store has read the TB tile before P1 rewrites
+    // it (its -W store, the newest bulk group, may still be reading Khat's
+    // tile until P2).
+    if (leader) bulk_wait_read_allbut1();
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
@@ -362,10 +364,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
       facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
       reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
     }
+    // The previous item's -W store has read Khat's tile before P2 rewrites it.
+    if (leader) bulk_wait_read_all();
     named_bar(2, kPThreads);
     KDA_SMARK(3);
 
-    // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
+    // ---- P2: scaled operand tiles; Qtil goes straight to the record.
     {
       const int sc0 = 4 * cg;
       auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
@@ -550,11 +554,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     named_bar(2, kPThreads);
     KDA_SMARK(7);
-    auto tile16 = [&](const float* X, int xs, const float* Y, int ys, int i4, int j4,
-                      float (&acc)[4][4]) {
-      float4 yv[16], xv[4][4];
+    // Block products, one warp per 16 x 16 x 16 product: lane (i4, j2) owns
+    // rows 4 i4 .. + 3 and columns 2 j2, 2 j2 + 1 of the output block.
+    //   acc[i][jj] += X[4 i4 + i][k] Y[k][2 j2 + jj],  k = 0..15.
+    const int i4 = lane >> 3, j2 = lane & 7;
+    auto prod16 = [&](const float* X, int xs, const float* Y, int ys, float (&acc)[4][2]) {
+      float2 yv[16];
+      float4 xv[4][4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float4*>(Y + k * ys + 4 * j4);
+      for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float2*>(Y + k * ys + 2 * j2);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -568,55 +576,59 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const float xk = (k & 3) == 0 ? xq.x : (k & 3) == 1 ? xq.y : (k & 3) == 2 ? xq.z : xq.w;
           acc[i][0] = fmaf(xk, yv[k].x, acc[i][0]);
           acc[i][1] = fmaf(xk, yv[k].y, acc[i][1]);
-          acc[i][2] = fmaf(xk, yv[k].z, acc[i][2]);
-          acc[i][3] = fmaf(xk, yv[k].w, acc[i][3]);
         }
       }
     };
-    auto store_tile = [&](float* Z, int i4, int j4, const float (&acc)[4][4]) {
+    auto store_blk = [&](float* Z, const float (&acc)[4][2]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4*>(Z + (4 * i4 + i) * kLdB + 4 * j4) =
-            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float2*>(Z + (4 * i4 + i) * kLdB + 2 * j2) =
+            make_float2(acc[i][0], acc[i][1]);
     };
-    const int tq = p & 15, i4 = tq >> 2, j4 = tq & 3;
-    // Step 1: N_ab = D_aa A_ab; diagonal blocks of T'.
-    if (p < 96) {
-      const int blk = p >> 4;
+    // Off-diagonal block pairs (a, b), a > b: (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5.
+    auto blk_a = [](int blk) { return blk < 1 ? 1 : blk < 3 ? 2 : 3; };
+    auto blk_b = [](int blk) {
       const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
-      const int b = blk - (a * (a - 1)) / 2;
-      float acc[4][4] = {};
-      tile16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, i4, j4, acc);
-      store_tile(Nm + blk * 16 * kLdB, i4, j4, acc);
-    } else if (p >= 128) {
-      const int e = p - 128, a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
-      float f8[8];
+      return blk - (a * (a - 1)) / 2;
+    };
+    // Step 1: N_ab = D_aa A_ab (warps 0..5); diagonal blocks of T' (warps 6, 7).
+    if (pw < 6) {
+      const int a = blk_a(pw), b = blk_b(pw);
+      float acc[4][2] = {};
+      prod16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, acc);
+      store_blk(Nm + pw * 16 * kLdB, acc);
+    } else {
+      for (int e = p - 192; e < 128; e += 64) {
+        const int a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+        float f8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int cc = 8 * h8 + u;
-        f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
+        for (int u = 0; u < 8; ++u) {
+          const int cc = 8 * h8 + u;
+          f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
+        }
+        st_tile8(smem + kPOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
       }
-      st_tile8(smem + kPOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
     }
     named_bar(2, kPThreads);
     KDA_SMARK(8);
     // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
-    if (p < 48) {
-      const int k2 = p >> 4;
-      float acc[4][4] = {};
-      const int xa = k2 == 0 ? 2 : k2 == 1 ? 5 : 4, ya = k2 == 0 ? 0 : k2 == 1 ? 2 : 0;
-      tile16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, i4, j4, acc);
-      if (k2 == 2) tile16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, i4, j4, acc);
-      store_tile(N2m + k2 * 16 * kLdB, i4, j4, acc);
+    if (pw < 3) {
+      float acc[4][2] = {};
+      const int xa = pw == 0 ? 2 : pw == 1 ? 5 : 4, ya = pw == 0 ? 0 : pw == 1 ? 2 : 0;
+      prod16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, acc);
+      if (pw == 2) prod16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, acc);
+      store_blk(N2m + pw * 16 * kLdB, acc);
     }
     named_bar(2, kPThreads);
     KDA_SMARK(9);
-    // Step 3: N^3 block (3,0); M = -N + N^2 in place for (1,0) (2,0) (2,1) (3,1).
-    if (p < 16) {
-      float acc[4][4] = {};
-      tile16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, i4, j4, acc);
-      store_tile(N3m, i4, j4, acc);
-    } else if (p >= 32) {
+    // Step 3: N^3 block (3,0) = N32 (N^2)_20 (warp 0), and M = -N + N^2 in
+    // place of N for blocks (1,0) (2,0) (2,1) (3,1) (warps 1..7); N32, which
+    // warp 0 reads, is negated in step 4 and M_30 is finished there too.
+    if (pw == 0) {
+      float acc[4][2] = {};
+      prod16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, acc);
+      store_blk(N3m, acc);
+    } else {
       for (int e = p - 32; e < 4 * 64; e += kPThreads - 32) {
         const int bsel = e >> 6;
         const int blk = bsel < 3 ? bsel : 4;
@@ -634,45 +646,42 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     named_bar(2, kPThreads);
     KDA_SMARK(10);
-    // Step 4: T_ab = M_ab D_bb, times beta, into T' (M_30 = -N30 + N^2_30 - N^3_30).
-    if (p < 96) {
-      const int blk = p >> 4;
-      const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
-      const int b = blk - (a * (a - 1)) / 2;
-      if (blk == 3) {
+    // Step 4: T_ab = M_ab D_bb, times beta, into T' (warps 0..5; M_30 =
+    // -N30 + N^2_30 - N^3_30 first, M_32 = -N_32).
+    if (pw < 6) {
+      const int a = blk_a(pw), b = blk_b(pw);
+      if (pw == 3) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = 4 * i4 + i;
-          float4* nv = reinterpret_cast<float4*>(Nm + (3 * 16 + row) * kLdB + 4 * j4);
-          const float4 n2 = *reinterpret_cast<const float4*>(N2m + (2 * 16 + row) * kLdB + 4 * j4);
-          const float4 n3 = *reinterpret_cast<const float4*>(N3m + row * kLdB + 4 * j4);
-          float4 m = *nv;
-          m.x = n2.x - m.x - n3.x; m.y = n2.y - m.y - n3.y;
-          m.z = n2.z - m.z - n3.z; m.w = n2.w - m.w - n3.w;
+          float2* nv = reinterpret_cast<float2*>(Nm + (3 * 16 + row) * kLdB + 2 * j2);
+          const float2 n2 = *reinterpret_cast<const float2*>(N2m + (2 * 16 + row) * kLdB + 2 * j2);
+          const float2 n3 = *reinterpret_cast<const float2*>(N3m + row * kLdB + 2 * j2);
+          float2 m = *nv;
+          m.x = n2.x - m.x - n3.x;
+          m.y = n2.y - m.y - n3.y;
           *nv = m;
         }
-        __syncwarp(0x0000FFFFu << (16 * (lane >> 4)));
+        __syncwarp();
       }
-      float acc[4][4] = {};
-      tile16(Nm + blk * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, i4, j4, acc);
-      if (blk == 5) {
+      float acc[4][2] = {};
+      prod16(Nm + pw * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, acc);
+      const float sg = pw == 5 ? -1.f : 1.f;
+      const float2 bv = *reinterpret_cast<const float2*>(&s_beta[16 * b + 2 * j2]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int jq = 0; jq < 4; ++jq) acc[i][jq] = -acc[i][jq];
-      }
-      const float4 bv = *reinterpret_cast<const float4*>(&s_beta[16 * b + 4 * j4]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint2 pk = make_uint2(pack2(acc[i][0] * bv.x, acc[i][1] * bv.y),
-                                    pack2(acc[i][2] * bv.z, acc[i][3] * bv.w));
-        *reinterpret_cast<uint2*>(smem + kPOffTB +
-                                  sw128_off(16 * a + 4 * i4 + i, 16 * b + 4 * j4, 64)) = pk;
-      }
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint32_t*>(smem + kPOffTB +
+                                     sw128_off(16 * a + 4 * i4 + i, 16 * b + 2 * j2, 64)) =
+            pack2(sg * acc[i][0] * bv.x, sg * acc[i][1] * bv.y);
     }
     fence_async_smem();
     named_bar(2, kPThreads);
     KDA_SMARK(11);
+    // T' is final: it leaves for the record now (it stays the A operand of W).
+    if (leader && !s_abort) {
+      bulk_store(rec + kRecT, smem + kPOffTB, 8192);
+      bulk_commit();
+    }
 
     // ---- P6: [W; 0] = [T'; 0] Ktil (M=128, N=128, K=64): W rows in TMEM
     // lanes 0..63, columns 0..127.
@@ -694,12 +703,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
 
     // ---- P7: -W (row = token, column = key channel) staged where Khat was;
     // its two 64-channel panels are rows 64..127 of the record's WQ panels.
-    if (pw < 2 && ok_w) {
-      const int t = 32 * pw + lane;
+    // Warps 0, 1 take channels 0..63 and warps 4, 5 channels 64..127 of
+    // TMEM lanes 0..63.
+    if ((pw & 3) < 2 && ok_w) {
+      const int t = 32 * (pw & 3) + lane;
 #pragma unroll 1
-      for (int q32 = 0; q32 < 4; ++q32) {
+      for (int q32 = 2 * (pw >> 2); q32 < 2 * (pw >> 2) + 2; ++q32) {
         float w[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(32 * pw) << 16) + 32 * q32, w);
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + 32 * q32, w);
         tmem_ld_wait();
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -716,7 +727,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (leader && !s_abort) {
       bulk_store(rec + kRecWQ + 8192, smem + kPOffKH, 8192);
       bulk_store(rec + kRecWQ + 16384 + 8192, smem + kPOffKH + 8192, 8192);
-      bulk_store(rec + kRecT, smem + kPOffTB, 8192);
       bulk_commit();
     }
     KDA_SMARK(13);
@@ -736,14 +746,17 @@ __global__ void __launch_bounds__(kPThreads, 2)
 }
 
 __global__ void __launch_bounds__(kSThreads, 1)
-    chunk_state_kernel(LaunchArgs args, SplitWindow win,
-                       const __grid_constant__ CUtensorMap tm_v) {
+    chunk_state_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ int s_cum[kSplitMaxSeqs + 1];
   __shared__ uint64_t s_bars[kSNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+#ifdef KDA_PHASE_PROFILE
+  __shared__ volatile unsigned long long s_ts[4];   // MMA1 / MMA2 issue, SB / UT hand-off
+#endif
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = args.heads;
@@ -830,6 +843,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // [O^T | U^T] = S^T [Qtil^T | -W^T]      (M = 128, N = 128, K = dk = 128)
         if (!sync.wait(kSBarSB, c & 1)) break;
         tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+        s_ts[0] = clock64();
+#endif
         {
           const uint32_t idesc = umma_idesc_bf16(128, 128, 0, 0);
           const uint32_t bWQ = smem_u32(slot + kRecWQ);
@@ -843,6 +859,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // [S^T | O^T] += U^T [Kbar^T; P]^T        (M = 128, N = 192, K = 64 tokens)
         if (!sync.wait(kSBarUT, c & 1)) break;
         tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+        s_ts[1] = clock64();
+#endif
         {
           const uint32_t idesc = umma_idesc_bf16(128, 192, 0, 0);
           const uint32_t bKP = smem_u32(slot + kRecKP);
@@ -884,22 +903,49 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tmem_st32(tbase + lane_base + kSColS + c0, f);
       tmem_st16(tbase + lane_base + kSColSB + c0 / 2, b);
     }
-    // Outputs of chunk cl held as O^T column j, rows 32 hf .. + 31, in `ov`:
-    // lane pairs swap values so each lane writes two adjacent columns of
-    // every other row (4-byte stores).
+    // Outputs of chunk cl, held as O^T column j, rows 32 hf .. + 31, in `ov`.
+    // Lane pairs swap values so each lane holds two adjacent columns of every
+    // other row.  A full chunk goes through the staging tile and one TMA
+    // store per 64-column half; a sequence's ragged last chunk is written
+    // row by row (the tile's tail rows belong to the next sequence).  Every
+    // state thread calls it (it holds barriers); `live` is false once a wait
+    // has failed.
     float ov[32];
-    auto emit_out = [&](int cl) {
+    auto emit_out = [&](int cl, bool live) {
       const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool odd = lane & 1;
-      __nv_bfloat16* base = gout + (c0 * H + h) * kD + (j & ~1);
+      uint32_t pk[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const float a = ov[2 * k], b = ov[2 * k + 1];
         const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
+        pk[k] = odd ? pack2(other, b) : pack2(a, other);
+      }
+      if (L < kC) {
+        __nv_bfloat16* base = gout + (c0 * H + h) * kD + (j & ~1);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+          if (live && r < L)
+            *reinterpret_cast<uint32_t*>(base + static_cast<long long>(r) * H * kD) = pk[k];
+        }
+        return;
+      }
+      // The previous TMA store has read the staging tile.
+      if (tid == 0) bulk_wait_read_all();
+      named_bar(1, kSStateThreads);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
         const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
-        const uint32_t pk = odd ? pack2(other, b) : pack2(a, other);
-        if (r < L) *reinterpret_cast<uint32_t*>(base + static_cast<long long>(r) * H * kD) = pk;
+        *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(r, j & ~1, 64)) = pk[k];
+      }
+      fence_async_smem();
+      named_bar(1, kSStateThreads);
+      if (tid == 0 && live && !s_abort) {
+        tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
+        tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
+        bulk_commit();
       }
     };
 
@@ -930,8 +976,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tmem_st_wait();
     tc_fence_before();
     named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+    if (tid == 0) s_ts[2] = clock64();
+#endif
     if (tid == 0) mbar_arrive(&s_bars[kSBarSB]);
     bool prev_ok = false;
+#ifdef KDA_PHASE_PROFILE
+    unsigned long long hand[4] = {};   // SB->MMA1 issue, MMA1 exec, UT->MMA2 issue, MMA2 exec
+#endif
 #ifdef KDA_PHASE_PROFILE
     unsigned long long prof_acc[10] = {}, prof_t = clock64();
 #endif
@@ -940,11 +992,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
       // (B) While MMA1 runs: the previous chunk's outputs.
-      if (__all_sync(0xFFFFFFFFu, c > 0 && prev_ok)) emit_out(c - 1);
+      if (c > 0) emit_out(c - 1, prev_ok);
       KDA_SMARK(0);
       // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
       const bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
       tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) {
+        const unsigned long long now = clock64();
+        hand[0] += s_ts[0] - s_ts[2];
+        hand[1] += now - s_ts[0];
+      }
+#endif
       KDA_SMARK(1);
       if (ok1) {
         float v[32], w[32];
@@ -960,6 +1019,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tc_fence_before();
       KDA_SMARK(2);
       named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) s_ts[3] = clock64();
+#endif
       if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
       KDA_SMARK(3);
       KDA_SMARK(4);
@@ -970,24 +1032,33 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const bool ok_next = !has_next || sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1);
       const bool ok2 = ok1 && sync.wait(kSBarMMA2, c & 1);
       tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) {
+        const unsigned long long now = clock64();
+        hand[2] += s_ts[1] - s_ts[3];
+        hand[3] += now - s_ts[1];
+      }
+#endif
       KDA_SMARK(5);
       if (ok2) {
         const bool decay = has_next && ok_next;
         const float* gam =
             reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot + kRecG);
-        tmem_ld32(tbase + lane_base + kSColO + 32 * hf, ov);
         const long long done = static_cast<long long>(win.cw0 + c + 1) * kC;
         float* ck = nullptr;
         if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
           const long long row = args.ckpt_offsets[n] + done / args.ckpt_interval - 1;
           ck = args.ckpt + (row * H + h) * kD * kD + j;
         }
-#pragma unroll 1
+        float sv[2][32];
+        tmem_ld32(tbase + lane_base + kSColO + 32 * hf, ov);
+        tmem_ld32(tbase + lane_base + kSColS + 64 * hf, sv[0]);
+        tmem_ld32(tbase + lane_base + kSColS + 64 * hf + 32, sv[1]);
+        tmem_ld_wait();
+#pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
           const int c0 = 64 * hf + 32 * cb;
-          float v[32];
-          tmem_ld32(tbase + lane_base + kSColS + c0, v);
-          tmem_ld_wait();
+          const float (&v)[32] = sv[cb];
           uint32_t b[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
@@ -1015,6 +1086,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tc_fence_before();
       KDA_SMARK(7);
       named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) s_ts[2] = clock64();
+#endif
       if (tid == 0 && ok2 && ok_next && has_next) mbar_arrive(&s_bars[kSBarSB]);
       KDA_SMARK(8);
       prev_ok = ok2;
@@ -1023,10 +1097,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #ifdef KDA_PHASE_PROFILE
     if (blockIdx.x == 0 && blockIdx.y == 0 && (tid == 0 || tid == 64)) {
       for (int i = 0; i < 10; ++i) kda_split_clocks[(tid ? 10 : 0) + i] = prof_acc[i];
-      if (tid == 0) kda_split_clocks[30] = nck;
+      if (tid == 0) {
+        kda_split_clocks[30] = nck;
+        for (int i = 0; i < 4; ++i) kda_split_clocks[20 + i] = hand[i];
+      }
     }
 #endif
-    if (__all_sync(0xFFFFFFFFu, prev_ok)) emit_out(nck - 1);
+    emit_out(nck - 1, prev_ok);
+    if (tid == 0) bulk_wait_all();
     if (!s_abort && dst) {
       // After the last chunk the fp32 state carries no further decay.
 #pragma unroll 1
@@ -1072,10 +1150,10 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  CUtensorMap maps[4] = {};
+  CUtensorMap maps[5] = {};
   if (a.total_tokens > 0) {
-    const void* bases[4] = {a.q, a.k, a.v, a.g};
-    for (int i = 0; i < 4; ++i)
+    const void* bases[5] = {a.q, a.k, a.v, a.g, a.out};
+    for (int i = 0; i < 5; ++i)
       if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
         return cudaErrorInvalidValue;
   }
@@ -1102,7 +1180,7 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     dim3 grid_s(a.n_seqs, a.heads);
-    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, stream>>>(a, w, maps[2]);
+    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, stream>>>(a, w, maps[2], maps[4]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (w.last) break;
   }
