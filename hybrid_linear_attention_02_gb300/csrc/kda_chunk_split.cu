@@ -37,6 +37,10 @@
 // state carried between them, which bounds the record buffer.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -59,6 +63,15 @@ constexpr uint32_t kRecT = 57344;    // T' = T diag(beta) 64 x 64  (K-major B)
 constexpr uint32_t kRecG = 65536;    // e^{G_C}, fp32 [128]
 constexpr uint32_t kRecBytes = 66048;
 constexpr uint32_t kRecSlot = 66560; // slot stride in shared memory (1024-aligned)
+constexpr long long kMinWindowChunks = 64;   // overlapped windows: at least this many chunks
+constexpr long long kPrepItemsPerCta = 4;    // overlapped windows: prep CTAs live this long
+
+// KDA_SPLIT_SERIAL=1 runs the windows of the split form one after another on
+// the caller's stream (no helper stream).
+bool split_serial_only() {
+  const char* v = getenv("KDA_SPLIT_SERIAL");
+  return v && strcmp(v, "1") == 0;
+}
 static_assert(kRecBytes == kSplitRecordBytes, "record size seen by the host");
 
 // ---------------------------------------------------------------- prep kernel
@@ -207,7 +220,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
   const int H = args.heads;
   window_prefix(args, win, s_cum);
   const int n_items = s_cum[args.n_seqs];
-  if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform over the block
+  // Items of this CTA: a contiguous run of win.per_cta (short-lived CTAs that
+  // free their SM often), or every gridDim.x-th item (a persistent grid).
+  const int it0 = win.per_cta ? static_cast<int>(blockIdx.x) * win.per_cta
+                              : static_cast<int>(blockIdx.x);
+  const int it_step = win.per_cta ? 1 : static_cast<int>(gridDim.x);
+  const int it_end = win.per_cta ? min(n_items, it0 + win.per_cta) : n_items;
+  if (it0 >= it_end) return;   // uniform over the block
 
   if (pw == 0) {
     tmem_alloc(&s_tmem, kPTmemCols);
@@ -263,7 +282,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
   };
 
-  Item cur = decode_item(args, win, s_cum, blockIdx.x);
+  Item cur = decode_item(args, win, s_cum, it0);
   if (loader) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -277,14 +296,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
   unsigned long long prof_acc[16] = {}, prof_t = clock64();
 #endif
 #pragma unroll 1
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k_iter) {
+  for (int it = it0; it < it_end; it += it_step, ++k_iter) {
     const uint32_t par = k_iter & 1;
     const long long c0 = cur.t0 + static_cast<long long>(cur.c) * kC;
     const int L = static_cast<int>(cur.t1 - c0 < kC ? cur.t1 - c0 : kC);
     uint8_t* rec = win.rec + static_cast<size_t>(it) * kRecBytes;
-    const int it_next = it + static_cast<int>(gridDim.x);
+    const int it_next = it + it_step;
     Item nxt = cur;
-    if (it_next < n_items) nxt = decode_item(args, win, s_cum, it_next);
+    if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
 
     // The previous item's T' store has read the TB tile before P1 rewrites
     // it (its -W store, the newest bulk group, may still be reading Khat's
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
-    if (it_next < n_items) load_beta(nxt);
+    if (it_next < it_end) load_beta(nxt);
     named_bar(2, kPThreads);
     KDA_SMARK(0);
     const bool ok_raw = sync.wait(kPBarRaw, par);
@@ -699,7 +718,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_after();
     KDA_SMARK(12);
     // [K';Q'] and Ktil are dead: the next item's raw tiles may land.
-    if (loader && ok_w && it_next < n_items) issue_raw(nxt);
+    if (loader && ok_w && it_next < it_end) issue_raw(nxt);
 
     // ---- P7: -W (row = token, column = key channel) staged where Khat was;
     // its two 64-channel panels are rows 64..127 of the record's WQ panels.
@@ -1136,6 +1155,43 @@ size_t split_record_bytes(int n_seqs, long long total_tokens, int heads) {
   return static_cast<size_t>(items) * kRecBytes;
 }
 
+namespace {
+
+// The helper stream (highest priority) that runs the state kernels beside the
+// caller's stream, and the events that order the two, one set per device.
+constexpr int kEvRing = 64;
+constexpr int kMaxDevices = 64;
+struct SplitStreams {
+  cudaStream_t state = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t prep_done[kEvRing] = {}, state_done[kEvRing] = {};
+  bool ready = false;
+};
+std::mutex g_split_mu;
+SplitStreams g_split[kMaxDevices];
+
+// Creates the device's helper stream and events on first use (call with
+// g_split_mu held); nullptr if that fails.
+SplitStreams* split_streams(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  SplitStreams& st = g_split[dev];
+  if (st.ready) return &st;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+  if (cudaStreamCreateWithPriority(&st.state, cudaStreamNonBlocking, greatest) != cudaSuccess)
+    return nullptr;
+  bool ok = cudaEventCreateWithFlags(&st.fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&st.join, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kEvRing; ++i)
+    ok = cudaEventCreateWithFlags(&st.prep_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&st.state_done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) return nullptr;
+  st.ready = true;
+  return &st;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
                                float* run_state, cudaStream_t stream) {
   if (a.n_seqs == 0 || a.heads == 0) return cudaSuccess;
@@ -1161,28 +1217,84 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   const long long cap_items = static_cast<long long>(record_bytes / kRecBytes);
   if (cap_items < pairs) return cudaErrorInvalidValue;
   const long long max_chunks = (a.total_tokens + kC - 1) / kC;   // of any one sequence
-  const long long wc = cap_items / pairs;                          // chunks per window
-  const long long item_bound_all = static_cast<long long>(a.heads) * (a.total_tokens / kC + a.n_seqs);
-  for (long long cw0 = 0;; cw0 += wc) {
-    SplitWindow w{};
-    w.rec = records;
-    w.cw0 = static_cast<int>(cw0);
-    w.cw1 = static_cast<int>(cw0 + wc < max_chunks ? cw0 + wc : max_chunks);
-    w.first = cw0 == 0;
-    w.last = cw0 + wc >= max_chunks;
-    w.s_run = run_state;
-    long long items = pairs * (w.cw1 - w.cw0);
+  const long long item_bound_all =
+      static_cast<long long>(a.heads) * (a.total_tokens / kC + a.n_seqs);
+
+  // Overlapped form, for pairs that leave at least half the SMs to spare:
+  // about eight windows of at least kMinWindowChunks chunks, two or more of
+  // which fit in the record buffer at once.  The preparation of window w + 1
+  // (caller's stream, short-lived CTAs) then runs beside the state pass of
+  // window w (helper stream, higher priority) on the SMs the state pass
+  // leaves idle, and a window's record region is rewritten only after the
+  // state pass that read it.
+  long long wc = (max_chunks + 7) / 8;
+  if (wc < kMinWindowChunks) wc = kMinWindowChunks;
+  if (pairs * wc * 2 > cap_items) wc = cap_items / (2 * pairs);
+  long long n_win = wc > 0 ? (max_chunks + wc - 1) / wc : 0;
+  long long n_regions = wc > 0 ? cap_items / (pairs * wc) : 0;
+  if (n_regions > kEvRing / 2) n_regions = kEvRing / 2;
+  const bool overlap = 2 * pairs <= sms && wc > 0 && n_win >= 2 && n_regions >= 2 &&
+                       !split_serial_only();
+  if (!overlap) {
+    wc = cap_items / pairs;
+    n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
+    n_regions = 1;
+  }
+
+  std::unique_lock<std::mutex> lock(g_split_mu, std::defer_lock);
+  SplitStreams* st = nullptr;
+  cudaStream_t s_state = stream;
+  if (overlap) {
+    lock.lock();
+    st = split_streams(dev);
+    if (!st) return cudaErrorUnknown;
+    s_state = st->state;
+    if ((e = cudaEventRecord(st->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s_state, st->fork, 0)) != cudaSuccess) return e;
+  }
+  const size_t region_bytes = static_cast<size_t>(pairs * wc) * kRecBytes;
+  for (long long w = 0; w < n_win || w == 0; ++w) {
+    const long long cw0 = w * wc;
+    SplitWindow win{};
+    win.rec = records + static_cast<size_t>(w % n_regions) * region_bytes;
+    win.cw0 = static_cast<int>(cw0);
+    win.cw1 = static_cast<int>(cw0 + wc < max_chunks ? cw0 + wc : max_chunks);
+    win.first = w == 0;
+    win.last = w + 1 >= n_win;
+    win.s_run = run_state;
+    long long items = pairs * (win.cw1 - win.cw0);
     if (items > item_bound_all) items = item_bound_all;
-    const long long grid_p = items < 2ll * sms ? items : 2ll * sms;
+    long long grid_p;
+    if (overlap) {
+      win.per_cta = kPrepItemsPerCta;
+      grid_p = (items + kPrepItemsPerCta - 1) / kPrepItemsPerCta;
+      if (w >= n_regions &&
+          (e = cudaStreamWaitEvent(stream, st->state_done[(w - n_regions) % kEvRing], 0)) !=
+              cudaSuccess)
+        return e;
+    } else {
+      win.per_cta = 0;
+      grid_p = items < 2ll * sms ? items : 2ll * sms;
+    }
     if (grid_p > 0) {
       chunk_prep_kernel<<<static_cast<unsigned>(grid_p), kPThreads, kPSmem, stream>>>(
-          a, w, maps[0], maps[1], maps[3]);
+          a, win, maps[0], maps[1], maps[3]);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    if (overlap) {
+      if ((e = cudaEventRecord(st->prep_done[w % kEvRing], stream)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(s_state, st->prep_done[w % kEvRing], 0)) != cudaSuccess)
+        return e;
+    }
     dim3 grid_s(a.n_seqs, a.heads);
-    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, stream>>>(a, w, maps[2], maps[4]);
+    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, s_state>>>(a, win, maps[2], maps[4]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (w.last) break;
+    if (overlap && (e = cudaEventRecord(st->state_done[w % kEvRing], s_state)) != cudaSuccess)
+      return e;
+  }
+  if (overlap) {
+    if ((e = cudaEventRecord(st->join, s_state)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(stream, st->join, 0)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }

@@ -53,6 +53,7 @@ struct SplitWindow {
   int cw0, cw1;
   bool first, last;
   float* s_run;        // state between windows (nullable with a single window)
+  int per_cta;         // prep items per CTA (contiguous), or 0: strided over the grid
 };
 
 // Record-buffer bytes the split path needs for these sizes.

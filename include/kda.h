@@ -25,7 +25,11 @@
  * the call and allocates no device memory; scratch comes from the caller's
  * workspace.
  * Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL is
- * the legacy default stream) and returns without synchronising.
+ * the legacy default stream) and returns without synchronising.  The split
+ * tensor-core prefill (see kda_chunk_fwd) also runs its state kernels on a
+ * helper stream of the library (one per device, highest priority), joined to
+ * `stream` by events before and after, so work on `stream` stays ordered;
+ * calls from several host threads serialise while they enqueue.
  * Errors: argument errors are detected on the host and returned before any
  * launch; launch failures return KDA_ERR_CUDA.  Errors found while kernels run
  * (a bounded wait that expired) are written to the optional device word

@@ -153,3 +153,19 @@ def test_split_windows_with_minimum_workspace(with_final):
     assert_close(out, ro, "bf16", "out")
     if with_final:
         assert_close(fin, rf, "bf16", "final_state")
+
+
+def test_split_overlapped_windows_match_serial(monkeypatch):
+    """The split form's overlapped windows (state passes on the library's
+    helper stream beside the preparation of the next window) give exactly the
+    results of the same kernels run one window after another."""
+    monkeypatch.setenv("KDA_CHUNK_PATH", "split")
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=7, device=DEV, lengths=[4000, 16384, 1500], heads=4)
+    o1, f1 = _run(d)
+    monkeypatch.setenv("KDA_SPLIT_SERIAL", "1")
+    o2, f2 = _run(d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    ro, rf = _oracle(d)
+    assert_close(o1, ro, "bf16", "out")
+    assert_close(f1, rf, "bf16", "final_state")
