@@ -534,26 +534,27 @@ __global__ void __launch_bounds__(kPThreads, 2)
     // T' = T diag(beta) in bf16 (same block scheme as the fused kernel).
     if (p < 64) {
       const int blk = p >> 4, jj = p & 15;
+      // Column jj of D_bb by forward substitution; the block's rows stream
+      // from shared memory (the 16 threads of a block read the same words).
       const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
-      float ar[16][16];
-#pragma unroll
-      for (int rr = 1; rr < 16; ++rr)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (4 * q < rr) {
-            const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
-            ar[rr][4 * q] = v.x; ar[rr][4 * q + 1] = v.y;
-            ar[rr][4 * q + 2] = v.z; ar[rr][4 * q + 3] = v.w;
-          }
-        }
       float x[16];
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < rr; ++i) {
-          if (i & 1) acc1 = fmaf(ar[rr][i], x[i], acc1);
-          else acc0 = fmaf(ar[rr][i], x[i], acc0);
+        for (int q = 0; q < 4; ++q) {
+          if (4 * q < rr) {
+            const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
+            const float a4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = 4 * q + u;
+              if (i < rr) {
+                if (i & 1) acc1 = fmaf(a4[u], x[i], acc1);
+                else acc0 = fmaf(a4[u], x[i], acc0);
+              }
+            }
+          }
         }
         x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -(acc0 + acc1));
       }
@@ -578,23 +579,24 @@ __global__ void __launch_bounds__(kPThreads, 2)
     //   acc[i][jj] += X[4 i4 + i][k] Y[k][2 j2 + jj],  k = 0..15.
     const int i4 = lane >> 3, j2 = lane & 7;
     auto prod16 = [&](const float* X, int xs, const float* Y, int ys, float (&acc)[4][2]) {
-      float2 yv[16];
-      float4 xv[4][4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float2*>(Y + k * ys + 2 * j2);
+      for (int q = 0; q < 4; ++q) {   // k = 4 q .. 4 q + 3
+        float4 xv[4];
+        float2 yv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
+          xv[i] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          xv[i][q] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
+        for (int kk = 0; kk < 4; ++kk)
+          yv[kk] = *reinterpret_cast<const float2*>(Y + (4 * q + kk) * ys + 2 * j2);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float4 xq = xv[i][k >> 2];
-          const float xk = (k & 3) == 0 ? xq.x : (k & 3) == 1 ? xq.y : (k & 3) == 2 ? xq.z : xq.w;
-          acc[i][0] = fmaf(xk, yv[k].x, acc[i][0]);
-          acc[i][1] = fmaf(xk, yv[k].y, acc[i][1]);
+          const float xk[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            acc[i][0] = fmaf(xk[kk], yv[kk].x, acc[i][0]);
+            acc[i][1] = fmaf(xk[kk], yv[kk].y, acc[i][1]);
+          }
         }
       }
     };
@@ -1233,8 +1235,20 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   long long n_win = wc > 0 ? (max_chunks + wc - 1) / wc : 0;
   long long n_regions = wc > 0 ? cap_items / (pairs * wc) : 0;
   if (n_regions > kEvRing / 2) n_regions = kEvRing / 2;
-  const bool overlap = 2 * pairs <= sms && wc > 0 && n_win >= 2 && n_regions >= 2 &&
-                       !split_serial_only();
+  bool overlap = 2 * pairs <= sms && wc > 0 && n_win >= 2 && n_regions >= 2;
+  // KDA_SPLIT_WINDOW=n: overlapped windows of n chunks whatever the pair count
+  // (a tuning knob); KDA_SPLIT_SERIAL=1: never overlap.
+  if (const char* fw = getenv("KDA_SPLIT_WINDOW")) {
+    const long long f = atoll(fw);
+    if (f > 0 && pairs * f * 2 <= cap_items) {
+      wc = f;
+      n_win = (max_chunks + wc - 1) / wc;
+      n_regions = cap_items / (pairs * wc);
+      if (n_regions > kEvRing / 2) n_regions = kEvRing / 2;
+      overlap = n_win >= 2;
+    }
+  }
+  if (split_serial_only()) overlap = false;
   if (!overlap) {
     wc = cap_items / pairs;
     n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
