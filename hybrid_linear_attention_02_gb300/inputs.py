@@ -162,3 +162,17 @@ def make_decode_tokens(w: Workload, step: int, seed: int = 0, device="cpu", n_se
     gen.manual_seed(seed * 1_000_003 + 1 + step)
     return draw_token_tensors(n_seqs or w.n_seqs, heads or w.heads, w.dk, w.dv, w.torch_dtype,
                               gen, device, w.a_dist)
+
+
+def make_output_gate(T: int, H: int, dv: int, dtype, seed: int = 0, device="cpu"):
+    """Synthetic inputs of the output epilogue: the gate pre-activation
+    z ~ N(0, 1) ([T, H, dv], the layer's dtype; stands in for the full-rank
+    projection of the hidden state), the RMSNorm scale w = 1 + 0.1 N(0, 1)
+    (fp32 [dv]) and eps = 1e-6.  Drawn after everything else, from their own
+    generator, so the other inputs of a workload do not change."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 1_000_003 + 999_983)
+    normal = _normal(gen, device)
+    z = normal((T, H, dv)).to(dtype)
+    w = 1.0 + 0.1 * normal((dv,))
+    return z, w.float(), 1e-6

@@ -115,8 +115,27 @@ def checkpoint_offsets(cu_seqlens, interval: int):
     return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
 
 
+def output_gate(o, z, weight, eps):
+    """KDA output epilogue, in fp64: head-wise RMSNorm of the output, then the
+    full-rank gate ("[Paper Review] Kimi K3: Open Frontier Intelligence",
+    section "Kimi Delta Attention (KDA)", paragraph "Full-rank gate"; its
+    formula was lost from the page, the reading is y = RMSNorm(o) * w * sigmoid(z)).
+
+    o, z: [..., dv] (z is the gate pre-activation of the same tokens and
+    heads); weight: [dv], the RMSNorm scale; eps: added to the mean square.
+    For every row: y = o / sqrt(mean(o^2) + eps) * weight * sigmoid(z).
+    """
+    o = np.asarray(o, dtype=np.float64)
+    z = _f64(z)
+    w = _f64(weight)
+    if z.shape != o.shape or w.shape != o.shape[-1:]:
+        raise ValueError("output_gate: shape mismatch")
+    ms = np.mean(o * o, axis=-1, keepdims=True)
+    return o / np.sqrt(ms + float(eps)) * w * (1.0 / (1.0 + np.exp(-z)))
+
+
 def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0,
-            ckpt_interval: int = 0):
+            ckpt_interval: int = 0, gate=None):
     """Token-by-token fp64 KDA over packed sequences.
 
     q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; init_state: [N, H, dk, dv]
@@ -124,6 +143,7 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0
     Returns (out [T, H, dv] fp64, final_state [N, H, dk, dv] fp64), plus the
     checkpoints [n_ckpt, H, dk, dv] (state after every ckpt_interval tokens of
     each sequence, rows laid out by checkpoint_offsets) when ckpt_interval > 0.
+    gate = (z [T, H, dv], weight [dv], eps): out is output_gate(o, z, weight, eps).
     """
     arrs = [_as_host(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"))]
     codes = {c for _, c in arrs}
@@ -162,6 +182,8 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0
     if rc < 0:
         raise RuntimeError(f"kda_oracle_prefill failed ({rc})")
     prefill.last_threads = rc
+    if gate is not None:
+        out = output_gate(out, *gate)
     if ckpt_interval:
         return out, fin, ck
     return out, fin
@@ -170,9 +192,10 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0
 prefill.last_threads = 0
 
 
-def decode(q, k, v, g, beta, state, threads: int = 0):
+def decode(q, k, v, g, beta, state, threads: int = 0, gate=None):
     """One fp64 decode step for N sequences; q, k, g: [N, H, dk], v: [N, H, dv],
-    beta: [N, H], state: [N, H, dk, dv].  Returns (out [N, H, dv], new_state)."""
+    beta: [N, H], state: [N, H, dk, dv].  Returns (out [N, H, dv], new_state);
+    gate = (z [N, H, dv], weight [dv], eps) applies output_gate to out."""
     arrs = [_as_host(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"))]
     (qa, dt), (ka, _), (va, _), (ga, _), (ba, _) = arrs
     N, H, dk = qa.shape
@@ -184,6 +207,8 @@ def decode(q, k, v, g, beta, state, threads: int = 0):
                                    out.ctypes.data, int(threads))
     if rc < 0:
         raise RuntimeError(f"kda_oracle_decode failed ({rc})")
+    if gate is not None:
+        out = output_gate(out, *gate)
     return out, st
 
 

@@ -288,3 +288,40 @@ def test_checkpoints_equal_prefix_final_states():
     # outputs are unchanged by asking for checkpoints
     o2, f2 = oracle.prefill(q, k, v, g, beta, init_state=S0, cu_seqlens=cu)
     assert np.array_equal(o2, out) and np.array_equal(f2, fin)
+
+
+# ---------------------------------------------------------------- output gate
+# Head-wise RMSNorm then the full-rank gate, y = o / sqrt(mean(o^2) + eps) * w
+# * sigmoid(z) (paper review, section "Kimi Delta Attention (KDA)", paragraph
+# "Full-rank gate"; the formula is read from the prose, the page lost it).
+
+def test_output_gate_hand_example():
+    gold = json.load(open(os.path.join(GOLDEN, "output_gate_hand.json")))
+    y = oracle.output_gate(np.array(gold["o"]), np.array(gold["z"]), np.array(gold["w"]),
+                           gold["eps"])
+    np.testing.assert_allclose(y, gold["y"], rtol=1e-14)
+    # exact values 0.3 sqrt(2) and 1.2 sqrt(2)
+    np.testing.assert_allclose(y, [0.3 * np.sqrt(2.0), 1.2 * np.sqrt(2.0)], rtol=1e-14)
+
+
+def test_output_gate_constant_rows_and_symmetries():
+    rng = np.random.default_rng(5)
+    dv = 16
+    a = rng.standard_normal((7, 1))
+    o = np.repeat(a, dv, axis=1)                       # constant rows: rms = |a|
+    z = rng.standard_normal((7, dv))
+    w = rng.standard_normal(dv)
+    y = oracle.output_gate(o, z, w, 0.0)
+    np.testing.assert_allclose(y, np.sign(a) * w / (1.0 + np.exp(-z)), rtol=1e-13)
+    o = rng.standard_normal((5, 3, dv))
+    z = rng.standard_normal((5, 3, dv))
+    y = oracle.output_gate(o, z, w, 0.0)
+    np.testing.assert_allclose(oracle.output_gate(3.7 * o, z, w, 0.0), y, rtol=1e-13)
+    np.testing.assert_allclose(oracle.output_gate(-o, z, w, 0.0), -y, rtol=1e-13)
+    # w = 1 and a saturated gate: every row has unit mean square.
+    y1 = oracle.output_gate(o, np.full_like(z, 60.0), np.ones(dv), 0.0)
+    np.testing.assert_allclose(np.mean(y1 * y1, axis=-1), 1.0, rtol=1e-13)
+    # eps far above the mean square: y -> o w sigmoid(z) / sqrt(eps).
+    big = 1e12
+    np.testing.assert_allclose(oracle.output_gate(o, z, w, big),
+                               o * w / (1.0 + np.exp(-z)) / np.sqrt(big), rtol=1e-9)
