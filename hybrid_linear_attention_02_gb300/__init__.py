@@ -71,6 +71,13 @@ def load():
             lib.kda_chunk_fwd_checkpoints.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp,
                                                       vp, sz, vp, vp, vp, vp, ip]
             lib.kda_chunk_fwd_checkpoints.restype = ip
+            fl = ctypes.c_float
+            lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, fl, vp, vp,
+                                                ip, dp, vp, sz, vp, vp]
+            lib.kda_chunk_fwd_gated.restype = ip
+            lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, fl, vp, vp, dp, vp,
+                                                  vp]
+            lib.kda_decode_step_gated.restype = ip
             lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
             lib.kda_chunk_fwd_algorithm.restype = ip
             _lib = lib
@@ -130,7 +137,7 @@ def checkpoint_offsets(lengths, interval: int) -> list:
 def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 64, *,
               n_seqs: int | None = None, out=None, final_state=None,
               output_final_state: bool = True, workspace=None, dev_status=None, stream=None,
-              ckpt_interval: int = 0, ckpt_offsets=None, checkpoints=None):
+              ckpt_interval: int = 0, ckpt_offsets=None, checkpoints=None, gate=None):
     """Chunkwise KDA prefill over packed sequences (``kda_chunk_fwd``).
 
     q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H] (fp32 or bf16, one dtype,
@@ -143,6 +150,10 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 6
     the state after every ckpt_interval tokens of each sequence, rows laid out
     by ckpt_offsets (int32 [N+1] on the device; computed from cu_seqlens when
     not given, which reads the lengths back to the host).
+
+    With gate = (z, norm_weight, eps) it calls ``kda_chunk_fwd_gated``: out is
+    RMSNorm(o) * norm_weight * sigmoid(z) per (token, head) row (z [T, H, dv]
+    in the inputs' dtype, norm_weight fp32 [dv]).
     """
     lib = load()
     if q.dim() != 3:
@@ -177,6 +188,21 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 6
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if gate is not None:
+        if ckpt_interval:
+            raise ValueError("checkpoints and the output gate are separate calls")
+        z, nw, eps = gate
+        _check_input("gate", z, (T, H, dv), dt, dev)
+        _check_input("norm_weight", nw, (dv,), torch.float32, dev)
+        with torch.cuda.device(dev):
+            rc = lib.kda_chunk_fwd_gated(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                _ptr(cu_seqlens), _ptr(z), _ptr(nw), float(eps), _ptr(out), _ptr(final_state),
+                int(chunk), ctypes.byref(d), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                _stream_handle(stream))
+        if rc != 0:
+            raise KDAError(rc, "kda_chunk_fwd_gated")
+        return out, final_state
     if ckpt_interval:
         if ckpt_offsets is None:
             lens = ([T // N] * N if cu_seqlens is None
@@ -206,9 +232,11 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, chunk: int = 6
     return out, final_state
 
 
-def decode_step(q, k, v, g, beta, state, *, out=None, dev_status=None, stream=None):
+def decode_step(q, k, v, g, beta, state, *, out=None, dev_status=None, stream=None, gate=None):
     """One KDA decode step (``kda_decode_step``): q, k, g [N, H, dk], v [N, H, dv],
-    beta [N, H]; state [N, H, dk, dv] fp32 is updated in place.  Returns out."""
+    beta [N, H]; state [N, H, dk, dv] fp32 is updated in place.  Returns out.
+    gate = (z [N, H, dv], norm_weight fp32 [dv], eps) applies the output
+    epilogue (``kda_decode_step_gated``)."""
     lib = load()
     N, H, dk = q.shape
     dv = v.shape[-1]
@@ -226,6 +254,18 @@ def decode_step(q, k, v, g, beta, state, *, out=None, dev_status=None, stream=No
     else:
         _check_input("out", out, (N, H, dv), dt, dev)
     d = _dims(N, N, H, dk, dv, dt)
+    if gate is not None:
+        z, nw, eps = gate
+        _check_input("gate", z, (N, H, dv), dt, dev)
+        _check_input("norm_weight", nw, (dv,), torch.float32, dev)
+        with torch.cuda.device(dev):
+            rc = lib.kda_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                           _ptr(z), _ptr(nw), float(eps), _ptr(state), _ptr(out),
+                                           ctypes.byref(d), _ptr(dev_status),
+                                           _stream_handle(stream))
+        if rc != 0:
+            raise KDAError(rc, "kda_decode_step_gated")
+        return out
     with torch.cuda.device(dev):
         rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                                  _ptr(out), ctypes.byref(d), _ptr(dev_status),

@@ -115,12 +115,31 @@ int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk) {
 
 namespace {
 
-// kda_chunk_fwd with optional prefix-cache checkpoints (ckpt == nullptr: none).
+// Optional parts of a prefill call: prefix-cache checkpoints (ckpt null: none)
+// and the output epilogue (gate null: none).
+struct Extras {
+  float* ckpt = nullptr;
+  const int* ckpt_offsets = nullptr;
+  int ckpt_interval = 0;
+  const void* gate = nullptr;
+  const float* gate_w = nullptr;
+  float gate_eps = 0.f;
+};
+
+int check_gate(const void* gate, const float* gate_w, float eps) {
+  if (!gate || !gate_w) return KDA_ERR_INVALID;
+  if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID;   // rejects NaN too
+  if (!aligned(gate, 16) || !aligned(gate_w, 16)) return KDA_ERR_ALIGNMENT;
+  return KDA_OK;
+}
+
 int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, const void* beta,
                    const float* init_state, const int* cu_seqlens, void* out, float* final_state,
                    int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
-                   int* dev_status, void* stream, float* ckpt, const int* ckpt_offsets,
-                   int ckpt_interval) {
+                   int* dev_status, void* stream, const Extras& x) {
+  float* ckpt = x.ckpt;
+  const int* ckpt_offsets = x.ckpt_offsets;
+  const int ckpt_interval = x.ckpt_interval;
   int rc = check_dims(dims);
   if (rc != KDA_OK) return rc;
   if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
@@ -130,6 +149,12 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
     if (!ckpt_offsets || ckpt_interval <= 0) return KDA_ERR_INVALID;
     if (ckpt_interval % 64 != 0) return KDA_ERR_UNSUPPORTED;
     if (!aligned(ckpt, 16)) return KDA_ERR_ALIGNMENT;
+  }
+  if (x.gate || x.gate_w) {
+    if (dims->total_tokens > 0 && dims->heads > 0) {
+      rc = check_gate(x.gate, x.gate_w, x.gate_eps);
+      if (rc != KDA_OK) return rc;
+    }
   }
   const int N = dims->n_seqs;
   if (N == 0 || dims->heads == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
@@ -159,6 +184,9 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   a.ckpt = ckpt;
   a.ckpt_offsets = ckpt ? ckpt_offsets : nullptr;
   a.ckpt_interval = ckpt ? ckpt_interval : 0;
+  a.gate = x.gate;
+  a.gate_w = x.gate_w;
+  a.gate_eps = x.gate_eps;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (need > 0 && cu_seqlens) {
@@ -184,10 +212,15 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   } else if (path != Path::kRecurrent) {
     e = kda::launch_chunk_tc(a, s);
   } else {
-    e = kda::launch_recurrent(a, s);
+    e = kda::launch_recurrent(a, s);   // applies the output epilogue itself
   }
+  if (e == cudaSuccess && a.gate && path != Path::kRecurrent) e = kda::launch_gate_epilogue(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
+
+int decode_impl(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                float* state, void* out, const kda_dims* dims, int* dev_status, void* stream,
+                const void* gate, const float* gate_w, float gate_eps);
 
 }  // namespace
 
@@ -198,7 +231,21 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, co
                   int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
                   int* dev_status, void* stream) {
   return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
-                        workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, 0);
+                        workspace, workspace_bytes, dev_status, stream, Extras{});
+}
+
+int kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, const float* init_state, const int* cu_seqlens,
+                        const void* gate, const float* norm_weight, float eps, void* out,
+                        float* final_state, int chunk, const kda_dims* dims, void* workspace,
+                        size_t workspace_bytes, int* dev_status, void* stream) {
+  if (!gate || !norm_weight) return KDA_ERR_INVALID;
+  Extras x;
+  x.gate = gate;
+  x.gate_w = norm_weight;
+  x.gate_eps = eps;
+  return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
+                        workspace, workspace_bytes, dev_status, stream, x);
 }
 
 int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const void* g,
@@ -208,13 +255,36 @@ int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const
                               void* stream, float* checkpoints, const int* ckpt_offsets,
                               int ckpt_interval) {
   if (!checkpoints) return KDA_ERR_INVALID;
+  Extras x;
+  x.ckpt = checkpoints;
+  x.ckpt_offsets = ckpt_offsets;
+  x.ckpt_interval = ckpt_interval;
   return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
-                        workspace, workspace_bytes, dev_status, stream, checkpoints, ckpt_offsets,
-                        ckpt_interval);
+                        workspace, workspace_bytes, dev_status, stream, x);
+}
+
+int kda_decode_step_gated(const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const void* gate, const float* norm_weight,
+                          float eps, float* state, void* out, const kda_dims* dims,
+                          int* dev_status, void* stream) {
+  if (!gate || !norm_weight) return KDA_ERR_INVALID;
+  return decode_impl(q, k, v, g, beta, state, out, dims, dev_status, stream, gate, norm_weight,
+                     eps);
 }
 
 int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
                     float* state, void* out, const kda_dims* dims, int* dev_status, void* stream) {
+  return decode_impl(q, k, v, g, beta, state, out, dims, dev_status, stream, nullptr, nullptr,
+                     0.f);
+}
+
+}  // extern "C"
+
+namespace {
+
+int decode_impl(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                float* state, void* out, const kda_dims* dims, int* dev_status, void* stream,
+                const void* gate, const float* gate_w, float gate_eps) {
   int rc = check_dims(dims);
   if (rc != KDA_OK) return rc;
   if (dims->total_tokens != dims->n_seqs) return KDA_ERR_INVALID;
@@ -223,7 +293,14 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* g, 
   if (rc != KDA_OK) return rc;
   if (!state) return KDA_ERR_INVALID;
   if (!aligned(state, 16)) return KDA_ERR_ALIGNMENT;
+  if (gate || gate_w) {
+    rc = check_gate(gate, gate_w, gate_eps);
+    if (rc != KDA_OK) return rc;
+  }
   LaunchArgs a{};
+  a.gate = gate;
+  a.gate_w = gate_w;
+  a.gate_eps = gate_eps;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.init_state = state;
   a.final_state = state;
@@ -239,4 +316,4 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* g, 
              : KDA_ERR_CUDA;
 }
 
-}  // extern "C"
+}  // namespace

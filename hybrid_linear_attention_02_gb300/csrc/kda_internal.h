@@ -24,12 +24,20 @@ struct LaunchArgs {
   float* ckpt;              // nullable: state after every ckpt_interval tokens
   const int* ckpt_offsets;  // [n_seqs + 1] first checkpoint row of each sequence
   int ckpt_interval;        // tokens between checkpoints (multiple of 64) or 0
+  // Output epilogue (nullable gate: none): out = RMSNorm(o) * gate_w * sigmoid(gate).
+  const void* gate;         // [T, H, dv] gate pre-activation, dtype of v
+  const float* gate_w;      // [dv] RMSNorm scale
+  float gate_eps;
 };
 
 // fp32 CUDA-core kernel that walks the recurrence token by token with the
 // state on chip.  Serves fp32 prefill, the shapes the tensor-core kernel does
 // not cover, and (with one token per sequence) the decode step.
 cudaError_t launch_recurrent(const LaunchArgs& a, cudaStream_t stream);
+
+// The output epilogue as its own pass over `out` (in place): for every
+// (token, head) row, out = out / sqrt(mean(out^2) + eps) * gate_w * sigmoid(gate).
+cudaError_t launch_gate_epilogue(const LaunchArgs& a, cudaStream_t stream);
 
 // Writes order[0..N) = sequence indices by decreasing length (ties by index).
 cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,

@@ -49,9 +49,11 @@ __device__ __forceinline__ void store_out4<__nv_bfloat16>(__nv_bfloat16* p, long
   *reinterpret_cast<uint2*>(p + i) = pk;
 }
 
-// kCkpt: also write the prefix-cache checkpoints (a separate instantiation,
-// so the prefill and decode code without them carries no extra test).
-template <int DK, int DV, typename T, bool kCkpt>
+// kCkpt: also write the prefix-cache checkpoints; kGate: apply the output
+// epilogue (head-wise RMSNorm, then the sigmoid gate) to every output row.
+// Each is its own instantiation, so the plain prefill and decode code carries
+// no extra test.
+template <int DK, int DV, typename T, bool kCkpt, bool kGate>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
   constexpr int CG = DV / 4;       // float4 column groups
   constexpr int RG = kThreads / CG;  // row groups
@@ -147,8 +149,22 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
         S[m].z = fmaf(kc, d.z, S[m].z); S[m].w = fmaf(kc, d.w, S[m].w);
       }
       if (rg == 0) {
-        const float4 o = make_float4(fmaf(qk, d.x, p.x), fmaf(qk, d.y, p.y), fmaf(qk, d.z, p.z),
-                                     fmaf(qk, d.w, p.w));
+        float4 o = make_float4(fmaf(qk, d.x, p.x), fmaf(qk, d.y, p.y), fmaf(qk, d.z, p.z),
+                               fmaf(qk, d.w, p.w));
+        if constexpr (kGate) {
+          // Threads rg == 0 are lanes 0 .. CG-1 of warp 0 and hold the whole row.
+          constexpr unsigned kMask = CG == 32 ? 0xFFFFFFFFu : ((1u << CG) - 1u);
+          float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+#pragma unroll
+          for (int m = CG / 2; m > 0; m >>= 1) ss += __shfl_xor_sync(kMask, ss, m);
+          const float rinv = rsqrtf(ss * (1.f / DV) + a.gate_eps);
+          const T* __restrict__ zg = static_cast<const T*>(a.gate);
+          const float4 wv = *reinterpret_cast<const float4*>(a.gate_w + 4 * cg);
+          o.x *= rinv * wv.x / (1.f + __expf(-load_in(zg, rv + 4 * cg)));
+          o.y *= rinv * wv.y / (1.f + __expf(-load_in(zg, rv + 4 * cg + 1)));
+          o.z *= rinv * wv.z / (1.f + __expf(-load_in(zg, rv + 4 * cg + 2)));
+          o.w *= rinv * wv.w / (1.f + __expf(-load_in(zg, rv + 4 * cg + 3)));
+        }
         store_out4(out, rv + 4 * cg, o);
       }
     }
@@ -181,17 +197,22 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(LaunchArgs a) {
 template <int DK, int DV>
 cudaError_t launch_dims(const LaunchArgs& a, cudaStream_t s) {
   dim3 grid(a.n_seqs, a.heads);
-  const bool ck = a.ckpt != nullptr;
+  // Checkpoints and the output gate are separate entry points, never both.
+  if (a.ckpt && a.gate) return cudaErrorInvalidValue;
   if (a.dtype == KDA_F32) {
-    if (ck)
-      recurrent_kernel<DK, DV, float, true><<<grid, kThreads, 0, s>>>(a);
+    if (a.ckpt)
+      recurrent_kernel<DK, DV, float, true, false><<<grid, kThreads, 0, s>>>(a);
+    else if (a.gate)
+      recurrent_kernel<DK, DV, float, false, true><<<grid, kThreads, 0, s>>>(a);
     else
-      recurrent_kernel<DK, DV, float, false><<<grid, kThreads, 0, s>>>(a);
+      recurrent_kernel<DK, DV, float, false, false><<<grid, kThreads, 0, s>>>(a);
   } else {
-    if (ck)
-      recurrent_kernel<DK, DV, __nv_bfloat16, true><<<grid, kThreads, 0, s>>>(a);
+    if (a.ckpt)
+      recurrent_kernel<DK, DV, __nv_bfloat16, true, false><<<grid, kThreads, 0, s>>>(a);
+    else if (a.gate)
+      recurrent_kernel<DK, DV, __nv_bfloat16, false, true><<<grid, kThreads, 0, s>>>(a);
     else
-      recurrent_kernel<DK, DV, __nv_bfloat16, false><<<grid, kThreads, 0, s>>>(a);
+      recurrent_kernel<DK, DV, __nv_bfloat16, false, false><<<grid, kThreads, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

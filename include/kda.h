@@ -145,6 +145,30 @@ KDA_API int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* 
                                       int ckpt_interval);
 
 /*
+ * kda_chunk_fwd followed by KDA's output epilogue: head-wise RMSNorm of every
+ * output row, then the input-dependent full-rank sigmoid gate ("[Paper
+ * Review] Kimi K3: Open Frontier Intelligence", section "Kimi Delta Attention
+ * (KDA)", paragraph "Full-rank gate"; the page lost the formula, read as
+ *   out[t, h, :] = o / sqrt(mean(o^2) + eps) * norm_weight * sigmoid(gate[t, h, :])
+ * with o the KDA output of token t, head h).
+ *   gate         [T_total, H, dv] gate pre-activation (the full-rank projection
+ *                of the hidden state, computed upstream), dtype of v, 16-byte
+ *                aligned.
+ *   norm_weight  fp32 [dv] RMSNorm scale (shared by the heads), device,
+ *                16-byte aligned.
+ *   eps          >= 0, added to the mean square.
+ * Everything else, including final_state, is as kda_chunk_fwd.  The
+ * CUDA-core path applies the epilogue in its own kernel; the tensor-core
+ * paths in a pass over `out` after the main kernels.
+ */
+KDA_API int kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* init_state, const int* cu_seqlens,
+                                const void* gate, const float* norm_weight, float eps, void* out,
+                                float* final_state, int chunk, const kda_dims* dims,
+                                void* workspace, size_t workspace_bytes, int* dev_status,
+                                void* stream);
+
+/*
  * One recurrent decode step (the "dedicated kernels for KDA decode" of the
  * section "Infrastructure: how to actually run trillion-scale"; the state is
  * the fixed-size d_k x d_v cache object per head).  Every one of the N
@@ -154,6 +178,15 @@ KDA_API int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* 
  */
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
                     float* state, void* out, const kda_dims* dims, int* dev_status, void* stream);
+
+/*
+ * kda_decode_step with the output epilogue of kda_chunk_fwd_gated applied to
+ * out inside the decode kernel (gate [N, H, dv], norm_weight fp32 [dv], eps).
+ */
+KDA_API int kda_decode_step_gated(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const void* gate, const float* norm_weight,
+                                  float eps, float* state, void* out, const kda_dims* dims,
+                                  int* dev_status, void* stream);
 
 /*
  * kda_chunk_fwd without a workspace, for callers that cannot allocate device

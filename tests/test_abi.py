@@ -87,6 +87,25 @@ def test_host_validation_checkpoints(lib):
     assert call(ck=MISALIGNED) == -5
 
 
+def test_host_validation_gated(lib):
+    d = _dims(n=1, t=64)
+
+    def call(gate=FAKE, w=FAKE, eps=1e-6):
+        return lib.kda_chunk_fwd_gated(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, gate, w,
+                                       ctypes.c_float(eps), FAKE, None, 64, ctypes.byref(d),
+                                       None, 0, None, None)
+
+    assert call(gate=None) == -1
+    assert call(w=None) == -1
+    assert call(eps=-1.0) == -1
+    assert call(eps=float("nan")) == -1
+    assert call(gate=MISALIGNED) == -5
+    dd = _dims(n=4, t=4)
+    assert lib.kda_decode_step_gated(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MISALIGNED,
+                                     ctypes.c_float(1e-6), FAKE, FAKE, ctypes.byref(dd), None,
+                                     None) == -5
+
+
 def test_host_validation_decode(lib):
     d = _dims(n=4, t=5)
     assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d),
