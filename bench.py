@@ -312,7 +312,32 @@ def run_gpu(args):
             "algorithmic_bytes_per_launch": ck_bytes,
             "achieved_gbs": ck_bytes / (ck_ms * 1e-3) / 1e9,
             "frac": ck_bytes / (ck_ms * 1e-3) / 1e9 / hbm_peak}
-    del d, args_pf, out, fin, ck_buf, ck_offs
+    del ck_buf, ck_offs
+
+    # ------- prefill with the output epilogue (head-wise RMSNorm + sigmoid gate) -------
+    gate = inputs.make_output_gate(T, H, w.dv, w.torch_dtype, seed=rank, device=dev)
+
+    def gated_step():
+        kda.chunk_fwd(*args_pf, d["init_state"], None, chunk=w.chunk, out=out, final_state=fin,
+                      gate=gate)
+
+    for _ in range(3):
+        gated_step()
+    barrier()
+    start.record(stream)
+    for _ in range(ck_steps):
+        gated_step()
+    end.record(stream)
+    barrier()
+    g_ms = max_over_ranks(start.elapsed_time(end)) / ck_steps
+    g_bytes = alg_bytes + T * H * w.dv * 2 + w.dv * 4
+    gated = {"value": job_throughput(world, T, g_ms) / 1e6, "unit": "Mtok/s",
+             "ms_per_step": g_ms, "steps": ck_steps, "overhead_vs_plain": g_ms / ms_step - 1.0,
+             "algorithmic_bytes_per_launch": g_bytes,
+             "achieved_gbs": g_bytes / (g_ms * 1e-3) / 1e9,
+             "frac": g_bytes / (g_ms * 1e-3) / 1e9 / hbm_peak,
+             "epilogue": "out = o / sqrt(mean(o^2) + 1e-6) * w * sigmoid(z), z [T, H, dv]"}
+    del d, args_pf, out, fin, gate
     torch.cuda.empty_cache()
     decode = None
     if args.only != "prefill":
@@ -355,6 +380,7 @@ def run_gpu(args):
             "gpu_launches": args.steps * launches,
             "clocks": clocks,
             "prefill_checkpoints": ckpt,
+            "prefill_gated": gated,
             "decode": decode,
         }
         print(json.dumps(line), flush=True)

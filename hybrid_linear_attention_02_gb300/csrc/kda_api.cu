@@ -201,7 +201,9 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   // means more (smaller) windows.
   const size_t split_min = need + split_state_bytes(dims) +
                            static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;
+  bool gate_done = path == Path::kRecurrent;   // the recurrence applies the epilogue itself
   if (path == Path::kSplit && workspace && workspace_bytes >= split_min) {
+    gate_done = true;                          // so does the split form's state kernel
     uint8_t* ws = static_cast<uint8_t*>(workspace) + need;
     float* run = reinterpret_cast<float*>(ws);
     uint8_t* rec = ws + split_state_bytes(dims);
@@ -212,9 +214,9 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   } else if (path != Path::kRecurrent) {
     e = kda::launch_chunk_tc(a, s);
   } else {
-    e = kda::launch_recurrent(a, s);   // applies the output epilogue itself
+    e = kda::launch_recurrent(a, s);
   }
-  if (e == cudaSuccess && a.gate && path != Path::kRecurrent) e = kda::launch_gate_epilogue(a, s);
+  if (e == cudaSuccess && a.gate && !gate_done) e = kda::launch_gate_epilogue(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -108,6 +108,8 @@ constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
 constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging 64 x 128 (TMA store image)
 constexpr uint32_t kSTiles = kSOffO + 16384;
 constexpr uint32_t kSSmem = kSTiles + 1024;
+constexpr uint32_t kSOffZ = kSTiles;           // gated variant: 2 gate tiles 64 x 128
+constexpr uint32_t kSSmemGated = kSTiles + 2 * 16384 + 1024;
 constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (lane = value column, column = key row)
 constexpr uint32_t kSColO = 128;   // 64 fp32: O^T  (MMA2 writes [S^T | O^T])
 constexpr uint32_t kSColU = 192;   // 64 fp32: U^T  (MMA1 writes [O^T | U^T])
@@ -116,7 +118,7 @@ constexpr uint32_t kSColUT = 320;  // 32: bf16 U^T, A operand
 constexpr uint32_t kSColU0 = 352;  // 2 x 64 fp32: U0^T = V^T T'^T, by chunk parity
 constexpr uint32_t kSTmemCols = 512;
 enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSBarSB,
-       kSBarUT, kSNumBars };
+       kSBarUT, kSBarZFull0, kSBarZFull1, kSBarZEmpty0, kSBarZEmpty1, kSNumBars };
 
 #ifdef KDA_PHASE_PROFILE
 // Per-phase SM-clock totals of two state-pass threads of CTA (0, 0)
@@ -132,6 +134,21 @@ __device__ unsigned long long kda_prep_clocks[32];
 #else
 #define KDA_SMARK(i) ((void)0)
 #endif
+
+// One step of a transposing butterfly sum across a warp: afterwards a[0..M)
+// hold, for the half of the rows this lane keeps (the upper half when lane
+// bit M is set), the sums over lane pairs M apart.  Steps 16 .. 1 over 32
+// rows leave lane l with row l summed over all 32 lanes.
+template <int M>
+__device__ __forceinline__ void butterfly_step(float (&a)[16], int lane) {
+  const bool up = lane & M;
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    const float send = up ? a[i] : a[i + M];
+    const float keep = up ? a[i + M] : a[i];
+    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, M);
+  }
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -766,9 +783,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
   if (pw == 0) tmem_dealloc(tbase, kPTmemCols);
 }
 
+// kGate: also apply the output epilogue (head-wise RMSNorm, then the sigmoid
+// gate) to every output row before it is stored; the gate tiles arrive by TMA
+// beside the records.
+template <bool kGate>
 __global__ void __launch_bounds__(kSThreads, 1)
     chunk_state_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_o) {
+                       const __grid_constant__ CUtensorMap tm_o,
+                       const __grid_constant__ CUtensorMap tm_z) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ int s_cum[kSplitMaxSeqs + 1];
@@ -778,6 +800,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #ifdef KDA_PHASE_PROFILE
   __shared__ volatile unsigned long long s_ts[4];   // MMA1 / MMA2 issue, SB / UT hand-off
 #endif
+  __shared__ __align__(16) float s_rsum[2][4][32];   // gated: row sums of squares, per warp
+  __shared__ __align__(16) float s_rinv[2][32];      // gated: 1 / rms of the chunk's rows
+  __shared__ __align__(16) float s_gw[kD];           // gated: RMSNorm scale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = args.heads;
@@ -837,6 +862,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(smem + kSOffV + s * 16384 + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
+        if constexpr (kGate) {
+          // The gate tile of chunk c is read when its outputs leave, during
+          // chunk c + 1; its slot is free once chunk c - 2's outputs have left.
+          if (c >= 2 && !sync.wait(kSBarZEmpty0 + s, ((c - 2) >> 1) & 1)) break;
+          uint64_t* zbar = &s_bars[kSBarZFull0 + s];
+          mbar_arrive_expect_tx(zbar, 16384);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem + kSOffZ + s * 16384 + hf * 8192, &tm_z, 64 * hf, h, c0, zbar);
+        }
       }
     }
   } else if (warp == kSMmaWarp) {
@@ -932,10 +967,51 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // state thread calls it (it holds barriers); `live` is false once a wait
     // has failed.
     float ov[32];
+    if constexpr (kGate) {
+      if (tid < kD) s_gw[tid] = args.gate_w[tid];   // the RMSNorm scale (a barrier follows)
+    }
     auto emit_out = [&](int cl, bool live) {
       const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool odd = lane & 1;
+      if constexpr (kGate) {
+        // Row sums of squares: a butterfly over the warp's 32 columns leaves
+        // lane l with row 32 hf + l; the four warps of a column half meet in
+        // shared memory.
+        float a[16];
+        {
+          const bool up = lane & 16;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo = ov[i] * ov[i], hi = ov[i + 16] * ov[i + 16];
+            a[i] = (up ? hi : lo) + __shfl_xor_sync(0xFFFFFFFFu, up ? lo : hi, 16);
+          }
+        }
+        butterfly_step<8>(a, lane);
+        butterfly_step<4>(a, lane);
+        butterfly_step<2>(a, lane);
+        butterfly_step<1>(a, lane);
+        s_rsum[hf][q][lane] = a[0];
+        named_bar(1, kSStateThreads);
+        if (q == 0) {
+          const float ss = s_rsum[hf][0][lane] + s_rsum[hf][1][lane] + s_rsum[hf][2][lane] +
+                           s_rsum[hf][3][lane];
+          s_rinv[hf][lane] = rsqrtf(ss * (1.f / kD) + args.gate_eps);
+        }
+        named_bar(1, kSStateThreads);
+        // The gate tile already holds w * sigmoid(z) (made while MMA2 ran;
+        // the barriers since then make it visible).
+        const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
+#pragma unroll
+        for (int r = 0; r < 32; r += 4) {
+          const float4 ri = *reinterpret_cast<const float4*>(&s_rinv[hf][r]);
+          const float rr[4] = {ri.x, ri.y, ri.z, ri.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            ov[r + u] *= rr[u] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                     zt + sw128_off(32 * hf + r + u, j, 64)));
+        }
+      }
       uint32_t pk[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
@@ -951,6 +1027,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (live && r < L)
             *reinterpret_cast<uint32_t*>(base + static_cast<long long>(r) * H * kD) = pk[k];
         }
+        if constexpr (kGate) {
+          named_bar(1, kSStateThreads);   // every gate-tile read is done
+          if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);
+        }
         return;
       }
       // The previous TMA store has read the staging tile.
@@ -963,6 +1043,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       fence_async_smem();
       named_bar(1, kSStateThreads);
+      if constexpr (kGate) {
+        if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);   // gate tile read
+      }
       if (tid == 0 && live && !s_abort) {
         tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
         tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
@@ -1016,7 +1099,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (c > 0) emit_out(c - 1, prev_ok);
       KDA_SMARK(0);
       // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
-      const bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
+      bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
       tc_fence_after();
 #ifdef KDA_PHASE_PROFILE
       if (tid == 0) {
@@ -1045,6 +1128,45 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #endif
       if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
       KDA_SMARK(3);
+      if constexpr (kGate) {
+        // While MMA2 runs: this chunk's gate tile becomes w * sigmoid(z) in
+        // place (each thread its own column and 32 rows; read back by the
+        // same thread when the outputs leave).
+        const int zs = c & 1;
+        const bool zok = sync.wait(kSBarZFull0 + zs, (c >> 1) & 1);
+        uint8_t* zt = smem + kSOffZ + zs * 16384;
+        // Thread t takes the 8-column group t & 15 of rows t >> 4, + 16, + 32, + 48:
+        // four 16-byte vectors, all loaded before any is stored.
+        uint4 zv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          zv[i] = *reinterpret_cast<const uint4*>(zt + sw128_off((tid >> 4) + 16 * i, 8 * (tid & 15), 64));
+        float gw8[8];
+        {
+          const float4 wa = *reinterpret_cast<const float4*>(&s_gw[8 * (tid & 15)]);
+          const float4 wb = *reinterpret_cast<const float4*>(&s_gw[8 * (tid & 15) + 4]);
+          gw8[0] = wa.x; gw8[1] = wa.y; gw8[2] = wa.z; gw8[3] = wa.w;
+          gw8[4] = wb.x; gw8[5] = wb.y; gw8[6] = wb.z; gw8[7] = wb.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t wv[4] = {zv[i].x, zv[i].y, zv[i].z, zv[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float lo, hi;
+            f2_unpack(bf16x2_to_f2(wv[u]), lo, hi);
+            if (!zok) lo = hi = 0.f;
+            lo = gw8[2 * u] * fmaf(0.5f, tanh_fast(0.5f * lo), 0.5f);
+            hi = gw8[2 * u + 1] * fmaf(0.5f, tanh_fast(0.5f * hi), 0.5f);
+            wv[u] = pack2(lo, hi);
+          }
+          zv[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(zt + sw128_off((tid >> 4) + 16 * i, 8 * (tid & 15), 64)) = zv[i];
+        ok1 = ok1 && zok;
+      }
       KDA_SMARK(4);
       // (E) Outputs to registers; new state -> bf16 operand copy (the serial
       // step) and, for the next chunk, the decayed fp32 state; checkpoints;
@@ -1201,17 +1323,21 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPSmem));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(chunk_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSSmemGated));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  CUtensorMap maps[5] = {};
+  CUtensorMap maps[6] = {};
+  const int n_maps = a.gate ? 6 : 5;
   if (a.total_tokens > 0) {
-    const void* bases[5] = {a.q, a.k, a.v, a.g, a.out};
-    for (int i = 0; i < 5; ++i)
+    const void* bases[6] = {a.q, a.k, a.v, a.g, a.out, a.gate};
+    for (int i = 0; i < n_maps; ++i)
       if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
         return cudaErrorInvalidValue;
   }
@@ -1301,7 +1427,12 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
         return e;
     }
     dim3 grid_s(a.n_seqs, a.heads);
-    chunk_state_kernel<<<grid_s, kSThreads, kSSmem, s_state>>>(a, win, maps[2], maps[4]);
+    if (a.gate)
+      chunk_state_kernel<true><<<grid_s, kSThreads, kSSmemGated, s_state>>>(a, win, maps[2],
+                                                                            maps[4], maps[5]);
+    else
+      chunk_state_kernel<false><<<grid_s, kSThreads, kSSmem, s_state>>>(a, win, maps[2], maps[4],
+                                                                        maps[5]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (overlap && (e = cudaEventRecord(st->state_done[w % kEvRing], s_state)) != cudaSuccess)
       return e;

@@ -353,6 +353,13 @@ __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// tanh to about 11 bits (the PTX approximate instruction, one MUFU op).
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- layout
 // Byte offset of element (row, col) in a 128B-swizzled tile of bf16 whose
 // 64-column halves each hold `rows` rows of 128 bytes (the layout TMA writes

@@ -158,8 +158,9 @@ KDA_API int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* 
  *                16-byte aligned.
  *   eps          >= 0, added to the mean square.
  * Everything else, including final_state, is as kda_chunk_fwd.  The
- * CUDA-core path applies the epilogue in its own kernel; the tensor-core
- * paths in a pass over `out` after the main kernels.
+ * CUDA-core recurrence and the split tensor-core form apply the epilogue
+ * inside their kernels (from the fp32 outputs); after the fused tensor-core
+ * kernel it runs as a pass over `out`.
  */
 KDA_API int kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
                                 const void* beta, const float* init_state, const int* cu_seqlens,
