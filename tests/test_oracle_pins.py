@@ -325,3 +325,76 @@ def test_output_gate_constant_rows_and_symmetries():
     big = 1e12
     np.testing.assert_allclose(oracle.output_gate(o, z, w, big),
                                o * w / (1.0 + np.exp(-z)) / np.sqrt(big), rtol=1e-9)
+
+
+# ---------------------------------------------------------------- KCP composition
+# The paper review's infrastructure section: KDA context parallelism computes
+# each segment's state transition locally and composes the segments
+# associatively.  A segment maps its entry state to S_end = M S_0 + H with
+# M = product of the per-token (I - beta k k^T) Diag(alpha) (dk x dk) and H the
+# end state from S_0 = 0; M is the end state of the same tokens run from S_0 = I
+# with v = 0.  Two segments compose as (M2, H2) o (M1, H1) = (M2 M1, M2 H1 + H2).
+
+def _transition(x, cu):
+    """(M [N, H, dk, dk], H [N, H, dk, dv]) of each sequence, from the oracle."""
+    q, k, v, g, b = x
+    N = len(cu) - 1
+    Hh, dk = q.shape[1], q.shape[2]
+    eye = np.broadcast_to(np.eye(dk), (N, Hh, dk, dk)).copy()
+    _, M = oracle.prefill(q, k, torch.zeros(v.shape[0], Hh, dk, dtype=v.dtype), g, b, eye, cu)
+    _, Hs = oracle.prefill(q, k, v, g, b, None, cu)
+    return M, Hs
+
+
+def test_kcp_transition_is_the_segment_map():
+    w = inputs.Workload("kcp", heads=2, dk=8, dv=8, dtype="f32", init_state=True)
+    d = inputs.make_prefill(w, seed=41, device="cpu", lengths=[37])
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    M, Hs = _transition(x, d["cu_seqlens"])
+    _, fin = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
+    s0 = d["init_state"].double().numpy()
+    np.testing.assert_allclose(M @ s0 + Hs, fin, rtol=1e-12, atol=1e-12)
+    # M is the product of the explicit per-token transition matrices.
+    q, k, v, g, b = (t.double().numpy() for t in x)
+    for h in range(2):
+        P = np.eye(8)
+        for t in range(37):
+            A = (np.eye(8) - b[t, h] * np.outer(k[t, h], k[t, h])) @ np.diag(np.exp(g[t, h]))
+            P = A @ P
+        np.testing.assert_allclose(M[0, h], P, rtol=1e-12, atol=1e-13)
+
+
+def test_kcp_composition_is_associative_and_matches_the_whole_sequence():
+    w = inputs.Workload("kcp", heads=2, dk=8, dv=6, dtype="f32", init_state=True)
+    T = 90
+    d = inputs.make_prefill(w, seed=42, device="cpu", lengths=[T])
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    cuts = [0, 20, 51, 77, T]
+    seg = torch.tensor(cuts, dtype=torch.int32)
+    M, Hs = _transition(x, seg)                       # one transition per segment
+    Mall, Hall = _transition(x, d["cu_seqlens"])      # the whole sequence at once
+
+    def compose(a, b):                                # b after a
+        return b[0] @ a[0], b[0] @ a[1] + b[1]
+
+    parts = [(M[i], Hs[i]) for i in range(len(cuts) - 1)]
+    left = parts[0]
+    for p in parts[1:]:
+        left = compose(left, p)                       # ((1 2) 3) 4
+    right = parts[-1]
+    for p in reversed(parts[:-1]):
+        right = compose(p, right)                     # 1 (2 (3 4))
+    for a, b_ in ((left, right), (left, (Mall[0], Hall[0]))):
+        np.testing.assert_allclose(a[0], b_[0], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(a[1], b_[1], rtol=1e-11, atol=1e-12)
+    # Segment entry states from the composed prefixes reproduce the outputs of
+    # the whole sequence when each segment is run from its own entry state.
+    s = d["init_state"].double().numpy()[0]
+    starts = []
+    for Mi, Hi in parts:
+        starts.append(s)
+        s = Mi @ s + Hi
+    out_seg, fin_seg = oracle.prefill(*x, np.stack(starts), seg)
+    out, fin = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
+    np.testing.assert_allclose(out_seg, out, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(fin_seg[-1], fin[0], rtol=1e-11, atol=1e-12)
