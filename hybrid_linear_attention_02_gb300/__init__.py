@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
+__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "chunk_transition", "transition_apply", "chunk_fwd_kcp", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libkda.so"
@@ -78,6 +78,19 @@ def load():
             lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, fl, vp, vp, dp, vp,
                                                   vp]
             lib.kda_decode_step_gated.restype = ip
+            ll = ctypes.c_longlong
+            lib.kda_chunk_transition_workspace_size.argtypes = [dp]
+            lib.kda_chunk_transition_workspace_size.restype = sz
+            lib.kda_chunk_transition.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz,
+                                                 vp, vp]
+            lib.kda_chunk_transition.restype = ip
+            lib.kda_transition_apply.argtypes = [vp, vp, vp, vp, ll, ip, ip, vp]
+            lib.kda_transition_apply.restype = ip
+            lib.kda_chunk_fwd_kcp_workspace_size.argtypes = [dp, ip]
+            lib.kda_chunk_fwd_kcp_workspace_size.restype = sz
+            lib.kda_chunk_fwd_kcp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
+                                              vp]
+            lib.kda_chunk_fwd_kcp.restype = ip
             lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
             lib.kda_chunk_fwd_algorithm.restype = ip
             _lib = lib
@@ -273,3 +286,73 @@ def decode_step(q, k, v, g, beta, state, *, out=None, dev_status=None, stream=No
     if rc != 0:
         raise KDAError(rc, "kda_decode_step")
     return out
+
+
+def chunk_transition(q, k, v, g, beta, cu_seqlens=None, *, n_seqs: int | None = None,
+                     workspace=None, dev_status=None, stream=None):
+    """Segment transitions (``kda_chunk_transition``): for each (sequence, head)
+    of the packed input, (M [N, H, dk, dk], H [N, H, dk, dv]) with
+    S_end = M S_0 + H."""
+    lib = load()
+    T, Hh, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (n_seqs or 1)
+    for name, t, shp in (("q", q, (T, Hh, dk)), ("k", k, (T, Hh, dk)), ("g", g, (T, Hh, dk)),
+                         ("v", v, (T, Hh, dv)), ("beta", beta, (T, Hh))):
+        _check_input(name, t, shp, dt, dev)
+    d = _dims(N, T, Hh, dk, dv, dt)
+    M = torch.empty((N, Hh, dk, dk), dtype=torch.float32, device=dev)
+    Hs = torch.empty((N, Hh, dk, dv), dtype=torch.float32, device=dev)
+    need = int(lib.kda_chunk_transition_workspace_size(ctypes.byref(d)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.kda_chunk_transition(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                      _ptr(cu_seqlens), _ptr(M), _ptr(Hs), 64, ctypes.byref(d),
+                                      _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                      _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_chunk_transition")
+    return M, Hs
+
+
+def transition_apply(M, H, S, *, out=None, stream=None):
+    """``kda_transition_apply``: out = M S + H per (…, dk, dv) pair (H may be None)."""
+    lib = load()
+    dk, dv = S.shape[-2], S.shape[-1]
+    pairs = S.numel() // (dk * dv)
+    if out is None:
+        out = torch.empty_like(S)
+    with torch.cuda.device(S.device):
+        rc = lib.kda_transition_apply(_ptr(M), _ptr(H), _ptr(S), _ptr(out), pairs, dk, dv,
+                                      _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_transition_apply")
+    return out
+
+
+def chunk_fwd_kcp(q, k, v, g, beta, init_state=None, *, n_seqs: int = 1, segments: int = 4,
+                  out=None, final_state=None, workspace=None, dev_status=None, stream=None):
+    """Single-GPU KCP prefill (``kda_chunk_fwd_kcp``) of n_seqs equal-length
+    sequences, each cut into `segments` segments.  Returns (out, final_state)."""
+    lib = load()
+    T, Hh, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if out is None:
+        out = torch.empty((T, Hh, dv), dtype=dt, device=dev)
+    if final_state is None:
+        final_state = torch.empty((n_seqs, Hh, dk, dv), dtype=torch.float32, device=dev)
+    d = _dims(n_seqs, T, Hh, dk, dv, dt)
+    need = int(lib.kda_chunk_fwd_kcp_workspace_size(ctypes.byref(d), int(segments)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.kda_chunk_fwd_kcp(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(init_state), _ptr(out), _ptr(final_state), int(segments),
+                                   ctypes.byref(d), _ptr(workspace), workspace.numel(),
+                                   _ptr(dev_status), _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_chunk_fwd_kcp")
+    return out, final_state

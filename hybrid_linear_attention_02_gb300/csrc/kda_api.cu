@@ -5,6 +5,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "kda_internal.h"
 
 namespace {
@@ -263,6 +265,164 @@ int kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const
   x.ckpt_interval = ckpt_interval;
   return chunk_fwd_impl(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, chunk, dims,
                         workspace, workspace_bytes, dev_status, stream, x);
+}
+
+size_t kda_chunk_transition_workspace_size(const kda_dims* dims) {
+  if (check_dims(dims) != KDA_OK || dims->n_seqs <= 0 || dims->heads <= 0) return 0;
+  return order_bytes(dims->n_seqs) + split_workspace_bytes(dims);
+}
+
+int kda_chunk_transition(const void* q, const void* k, const void* v, const void* g,
+                         const void* beta, const int* cu_seqlens, float* trans_M, float* trans_H,
+                         int chunk, const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                         int* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  LaunchArgs a{};
+  a.n_seqs = dims->n_seqs; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
+  a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
+  if (!kda::chunk_tc_supported(a) || dims->n_seqs > kda::kSplitMaxSeqs) return KDA_ERR_UNSUPPORTED;
+  const int N = dims->n_seqs;
+  if (N == 0 || dims->heads == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
+  if (!trans_M || !trans_H) return KDA_ERR_INVALID;
+  if (!aligned(trans_M, 16) || !aligned(trans_H, 16)) return KDA_ERR_ALIGNMENT;
+  rc = check_io_pointers(q, k, v, g, beta, trans_H, dims);   // trans_H stands in for out
+  if (rc != KDA_OK) return rc;
+  long long seq_len = 0;
+  if (!cu_seqlens) {
+    if (dims->total_tokens % N != 0) return KDA_ERR_INVALID;
+    seq_len = dims->total_tokens / N;
+  }
+  const size_t need = order_bytes(N);
+  const size_t split_min = need + split_state_bytes(dims) +
+                           static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;
+  if (!workspace || workspace_bytes < split_min) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, kWorkspaceAlign)) return KDA_ERR_ALIGNMENT;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.cu_seqlens = cu_seqlens;
+  a.seq_len = seq_len;
+  a.out = trans_H;   // never written: transitions produce no outputs
+  a.dev_status = dev_status;
+  a.trans_M = trans_M;
+  a.trans_H = trans_H;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (need > 0 && cu_seqlens) {
+    if (kda::launch_length_order(cu_seqlens, N, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    a.order = reinterpret_cast<int*>(ws);
+  }
+  size_t rec_bytes = workspace_bytes - need - split_state_bytes(dims);
+  const size_t full = kda::split_record_bytes(N, dims->total_tokens, dims->heads);
+  if (rec_bytes > full) rec_bytes = full;
+  const cudaError_t e = kda::launch_chunk_split(a, ws + need + split_state_bytes(dims), rec_bytes,
+                                                nullptr, s);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_transition_apply(const float* M, const float* H, const float* S_in, float* S_out,
+                         long long pairs, int dk, int dv, void* stream) {
+  if (pairs < 0 || !((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) {
+    return pairs < 0 ? KDA_ERR_INVALID : KDA_ERR_UNSUPPORTED;
+  }
+  if (pairs == 0) return KDA_OK;
+  if (!M || !S_in || !S_out) return KDA_ERR_INVALID;
+  if (S_out == S_in || S_out == M) return KDA_ERR_INVALID;
+  if (pairs > (1ll << 30)) return KDA_ERR_UNSUPPORTED;
+  return kda::launch_transition_apply(M, H, S_in, S_out, pairs, dk, dv,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
+size_t kda_chunk_fwd_kcp_workspace_size(const kda_dims* dims, int n_segments) {
+  if (check_dims(dims) != KDA_OK || n_segments < 1 || dims->n_seqs <= 0 || dims->heads <= 0)
+    return 0;
+  kda_dims sd = *dims;
+  sd.n_seqs = dims->n_seqs * n_segments;
+  const size_t pair = static_cast<size_t>(dims->dk) * dims->dv * sizeof(float);
+  const size_t mats = align_up(static_cast<size_t>(sd.n_seqs) * dims->heads * pair);
+  const size_t inner = std::max(kda_chunk_transition_workspace_size(&sd),
+                                kda_chunk_fwd_workspace_size(&sd, 64));
+  return align_up(sizeof(int) * (static_cast<size_t>(sd.n_seqs) + 1)) + 4 * mats + inner;
+}
+
+int kda_chunk_fwd_kcp(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const float* init_state, void* out, float* final_state,
+                      int n_segments, const kda_dims* dims, void* workspace,
+                      size_t workspace_bytes, int* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (n_segments < 1) return KDA_ERR_INVALID;
+  const int N = dims->n_seqs, H = dims->heads;
+  if (N == 0 || H == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
+  if (dims->total_tokens % N != 0) return KDA_ERR_INVALID;
+  if (dims->dk != dims->dv) return KDA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * n_segments > kda::kSplitMaxSeqs) return KDA_ERR_UNSUPPORTED;
+  kda_dims sd = *dims;
+  sd.n_seqs = N * n_segments;
+  LaunchArgs probe{};
+  probe.n_seqs = sd.n_seqs; probe.heads = H; probe.dk = dims->dk; probe.dv = dims->dv;
+  probe.dtype = dims->dtype; probe.chunk = 64; probe.total_tokens = dims->total_tokens;
+  if (!kda::chunk_tc_supported(probe)) return KDA_ERR_UNSUPPORTED;
+  rc = check_io_pointers(q, k, v, g, beta, out, dims);
+  if (rc != KDA_OK) return rc;
+  if ((init_state && !aligned(init_state, 16)) || (final_state && !aligned(final_state, 16)))
+    return KDA_ERR_ALIGNMENT;
+  const size_t need = kda_chunk_fwd_kcp_workspace_size(dims, n_segments);
+  if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, kWorkspaceAlign)) return KDA_ERR_ALIGNMENT;
+
+  // Workspace: segment offsets, then M, H, entry states and end states of
+  // every segment, then the inner calls' workspace.
+  const long long L = dims->total_tokens / N;
+  const long long seg_len = ((L + n_segments - 1) / n_segments + 63) / 64 * 64;
+  const size_t pair = static_cast<size_t>(dims->dk) * dims->dv;
+  const size_t mats = align_up(static_cast<size_t>(sd.n_seqs) * H * pair * sizeof(float));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* cu_seg = reinterpret_cast<int*>(ws);
+  ws += align_up(sizeof(int) * (static_cast<size_t>(sd.n_seqs) + 1));
+  float* Ms = reinterpret_cast<float*>(ws);
+  float* Hs = reinterpret_cast<float*>(ws + mats);
+  float* starts = reinterpret_cast<float*>(ws + 2 * mats);
+  float* ends = reinterpret_cast<float*>(ws + 3 * mats);
+  uint8_t* inner = ws + 4 * mats;
+  const size_t inner_bytes = workspace_bytes - static_cast<size_t>(inner - static_cast<uint8_t*>(workspace));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t seq_bytes = static_cast<size_t>(H) * pair * sizeof(float);   // one sequence's states
+
+  if (kda::launch_segment_offsets(cu_seg, N, L, n_segments, seg_len, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  // 1. Every segment's transition (M, H), all segments at once.
+  rc = kda_chunk_transition(q, k, v, g, beta, cu_seg, Ms, Hs, 64, &sd, inner, inner_bytes,
+                            dev_status, stream);
+  if (rc != KDA_OK) return rc;
+  // 2. Entry states: segment 0 starts from init_state, segment s + 1 from
+  //    M_s S_s + H_s (the composed prefix), for every sequence at once.
+  cudaError_t e =
+      init_state ? cudaMemcpy2DAsync(starts, n_segments * seq_bytes, init_state, seq_bytes,
+                                     seq_bytes, N, cudaMemcpyDeviceToDevice, s)
+                 : cudaMemset2DAsync(starts, n_segments * seq_bytes, 0, seq_bytes, N, s);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  const long long stride = static_cast<long long>(n_segments) * H;   // pairs between sequences
+  for (int sg = 0; sg + 1 < n_segments; ++sg) {
+    const size_t off = static_cast<size_t>(sg) * H * pair;
+    e = kda::launch_transition_apply_strided(Ms + off, Hs + off, starts + off,
+                                             starts + off + H * pair, N, H, stride, stride,
+                                             stride, dims->dk, dims->dv, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  // 3. Every segment from its entry state: outputs, and end states.
+  rc = kda_chunk_fwd(q, k, v, g, beta, starts, cu_seg, out, ends, 64, &sd, inner, inner_bytes,
+                     dev_status, stream);
+  if (rc != KDA_OK) return rc;
+  if (final_state) {
+    e = cudaMemcpy2DAsync(final_state, seq_bytes,
+                          reinterpret_cast<uint8_t*>(ends) + (n_segments - 1) * seq_bytes,
+                          n_segments * seq_bytes, seq_bytes, N, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
 }
 
 int kda_decode_step_gated(const void* q, const void* k, const void* v, const void* g,

@@ -783,10 +783,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
   if (pw == 0) tmem_dealloc(tbase, kPTmemCols);
 }
 
-// kGate: also apply the output epilogue (head-wise RMSNorm, then the sigmoid
-// gate) to every output row before it is stored; the gate tiles arrive by TMA
-// beside the records.
-template <bool kGate>
+// Variants: kGate also applies the output epilogue (head-wise RMSNorm, then
+// the sigmoid gate) to every output row before it is stored, the gate tiles
+// arriving by TMA beside the records; kTrans computes segment transitions
+// (below) instead of outputs.  Each is its own instantiation.
+template <bool kGate, bool kTrans>
 __global__ void __launch_bounds__(kSThreads, 1)
     chunk_state_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o,
@@ -814,16 +815,29 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int nck = (s_cum[n + 1] - s_cum[n]) / H;     // chunks of this pair in the window
   const int rbase = s_cum[n] + h * nck;
   const long long soff = (static_cast<long long>(n) * H + h) * kD * kD;
-  const float* src = win.first ? args.init_state : win.s_run;
-  float* dst = win.last ? args.final_state : win.s_run;
+  // Transition mode (args.trans_M set, grid depth 2): z = 0 runs the chunks
+  // from S_0 = 0 and leaves H in trans_H, z = 1 runs them from S_0 = I with
+  // v = 0 and leaves M in trans_M (dk = dv); no outputs.  Between windows the
+  // two buffers carry the partial maps.
+  const int tmode = kTrans ? 1 + static_cast<int>(blockIdx.z) : 0;   // 0 off, 1 H, 2 M
+  const bool vzero = tmode == 2;
+  float* tbuf = tmode == 1 ? args.trans_H : args.trans_M;
+  const float* src = tmode ? (win.first ? nullptr : tbuf)
+                           : (win.first ? args.init_state : win.s_run);
+  const bool src_identity = tmode == 2 && win.first;
+  float* dst = tmode ? tbuf : (win.last ? args.final_state : win.s_run);
 
   if (nck == 0) {
-    // No chunk of this pair in the window: carry its state through.
+    // No chunk of this pair in the window: carry its state (or map) through.
     if (dst && dst != src) {
       float4* d4 = reinterpret_cast<float4*>(dst + soff);
       const float4* s4 = reinterpret_cast<const float4*>(src + soff);
-      for (int e = tid; e < kD * kD / 4; e += kSThreads)
-        d4[e] = src ? s4[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = tid; e < kD * kD / 4; e += kSThreads) {
+        const int r = (4 * e) / kD, c = (4 * e) % kD;
+        d4[e] = src ? s4[e]
+                    : src_identity ? make_float4(r == c, r == c + 1, r == c + 2, r == c + 3)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     return;
   }
@@ -852,16 +866,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int s = c & 1;
         if (c >= 2 && !sync.wait(kSBarEmpty0 + s, ((c - 2) >> 1) & 1)) break;
         uint64_t* bar = &s_bars[kSBarFull0 + s];
-        mbar_arrive_expect_tx(bar, kRecBytes + 16384);
+        mbar_arrive_expect_tx(bar, kRecBytes + (vzero ? 0 : 16384));
         const uint8_t* rec = win.rec + static_cast<size_t>(rbase + c) * kRecBytes;
         uint8_t* slot = smem + kSOffRec + s * kRecSlot;
 #pragma unroll
         for (int i = 0; i < 4; ++i) bulk_load(slot + 16384 * i, rec + 16384 * i, 16384, bar);
         bulk_load(slot + kRecG, rec + kRecG, kRecBytes - kRecG, bar);
         const int c0 = static_cast<int>(t0 + static_cast<long long>(win.cw0 + c) * kC);
+        if (!vzero) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem + kSOffV + s * 16384 + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem + kSOffV + s * 16384 + hf * 8192, &tm_v, 64 * hf, h, c0, bar);
+        }
         if constexpr (kGate) {
           // The gate tile of chunk c is read when its outputs leave, during
           // chunk c + 1; its slot is free once chunk c - 2's outputs have left.
@@ -888,7 +904,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
       };
       bool ok = sync.wait(kSBarFull0, 0);
-      if (ok) {
+      if (ok && !vzero) {
         tc_fence_after();
         issue_mma0(0);
       }
@@ -929,7 +945,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           umma_commit(&s_bars[kSBarMMA2]);
         }
         // The next chunk's U0^T runs while the state warps convert S^T.
-        if (c + 1 < nck) {
+        if (c + 1 < nck && !vzero) {
           if (!sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1)) break;
           tc_fence_after();
           issue_mma0(s ^ 1);
@@ -952,7 +968,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       uint32_t f[32], b[16];
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        f[u] = __float_as_uint(src ? __ldcs(src + soff + (c0 + u) * kD + j) : 0.f);
+        f[u] = __float_as_uint(src ? __ldcs(src + soff + (c0 + u) * kD + j)
+                                   : (src_identity && c0 + u == j ? 1.f : 0.f));
 #pragma unroll
       for (int u = 0; u < 16; ++u)
         b[u] = pack2(__uint_as_float(f[2 * u]), __uint_as_float(f[2 * u + 1]));
@@ -1096,7 +1113,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
       // (B) While MMA1 runs: the previous chunk's outputs.
-      if (c > 0) emit_out(c - 1, prev_ok);
+      if (c > 0 && tmode == 0) emit_out(c - 1, prev_ok);
       KDA_SMARK(0);
       // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
       bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
@@ -1112,8 +1129,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (ok1) {
         float v[32], w[32];
         tmem_ld32(tbase + lane_base + kSColU + 32 * hf, v);
-        tmem_ld32(tbase + lane_base + kSColU0 + 64 * s + 32 * hf, w);
+        if (!vzero) tmem_ld32(tbase + lane_base + kSColU0 + 64 * s + 32 * hf, w);
         tmem_ld_wait();
+        if (vzero) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) w[u] = 0.f;
+        }
         uint32_t b[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u] + w[2 * u], v[2 * u + 1] + w[2 * u + 1]);
@@ -1246,7 +1267,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
 #endif
-    emit_out(nck - 1, prev_ok);
+    if (tmode == 0) emit_out(nck - 1, prev_ok);
     if (tid == 0) bulk_wait_all();
     if (!s_abort && dst) {
       // After the last chunk the fp32 state carries no further decay.
@@ -1323,11 +1344,15 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPSmem));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSSmem));
+  e = cudaFuncSetAttribute(chunk_state_kernel<false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(chunk_state_kernel<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSSmemGated));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1361,7 +1386,7 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   long long n_win = wc > 0 ? (max_chunks + wc - 1) / wc : 0;
   long long n_regions = wc > 0 ? cap_items / (pairs * wc) : 0;
   if (n_regions > kEvRing / 2) n_regions = kEvRing / 2;
-  bool overlap = 2 * pairs <= sms && wc > 0 && n_win >= 2 && n_regions >= 2;
+  bool overlap = 2 * pairs <= sms && wc > 0 && n_win >= 2 && n_regions >= 2 && !a.trans_M;
   // KDA_SPLIT_WINDOW=n: overlapped windows of n chunks whatever the pair count
   // (a tuning knob); KDA_SPLIT_SERIAL=1: never overlap.
   if (const char* fw = getenv("KDA_SPLIT_WINDOW")) {
@@ -1374,7 +1399,7 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       overlap = n_win >= 2;
     }
   }
-  if (split_serial_only()) overlap = false;
+  if (split_serial_only() || a.trans_M) overlap = false;
   if (!overlap) {
     wc = cap_items / pairs;
     n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
@@ -1426,13 +1451,16 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       if ((e = cudaStreamWaitEvent(s_state, st->prep_done[w % kEvRing], 0)) != cudaSuccess)
         return e;
     }
-    dim3 grid_s(a.n_seqs, a.heads);
-    if (a.gate)
-      chunk_state_kernel<true><<<grid_s, kSThreads, kSSmemGated, s_state>>>(a, win, maps[2],
-                                                                            maps[4], maps[5]);
+    dim3 grid_s(a.n_seqs, a.heads, a.trans_M ? 2 : 1);
+    if (a.trans_M)
+      chunk_state_kernel<false, true><<<grid_s, kSThreads, kSSmem, s_state>>>(
+          a, win, maps[2], maps[4], maps[5]);
+    else if (a.gate)
+      chunk_state_kernel<true, false><<<grid_s, kSThreads, kSSmemGated, s_state>>>(
+          a, win, maps[2], maps[4], maps[5]);
     else
-      chunk_state_kernel<false><<<grid_s, kSThreads, kSSmem, s_state>>>(a, win, maps[2], maps[4],
-                                                                        maps[5]);
+      chunk_state_kernel<false, false><<<grid_s, kSThreads, kSSmem, s_state>>>(
+          a, win, maps[2], maps[4], maps[5]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (overlap && (e = cudaEventRecord(st->state_done[w % kEvRing], s_state)) != cudaSuccess)
       return e;

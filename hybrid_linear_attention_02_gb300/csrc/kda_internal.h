@@ -28,6 +28,10 @@ struct LaunchArgs {
   const void* gate;         // [T, H, dv] gate pre-activation, dtype of v
   const float* gate_w;      // [dv] RMSNorm scale
   float gate_eps;
+  // Segment transitions (split form only; trans_M null: off): per (sequence,
+  // head) M [dk, dk] and H [dk, dv] with S_end = M S_0 + H; no outputs.
+  float* trans_M;
+  float* trans_H;
 };
 
 // fp32 CUDA-core kernel that walks the recurrence token by token with the
@@ -38,6 +42,26 @@ cudaError_t launch_recurrent(const LaunchArgs& a, cudaStream_t stream);
 // The output epilogue as its own pass over `out` (in place): for every
 // (token, head) row, out = out / sqrt(mean(out^2) + eps) * gate_w * sigmoid(gate).
 cudaError_t launch_gate_epilogue(const LaunchArgs& a, cudaStream_t stream);
+
+// S_out[p] = M[p] S_in[p] (+ H[p] when H is not null), fp32, for `pairs`
+// independent (dk x dk) (dk x dv) products; S_out must not alias M or S_in.
+cudaError_t launch_transition_apply(const float* M, const float* H, const float* S_in,
+                                    float* S_out, long long pairs, int dk, int dv,
+                                    cudaStream_t stream);
+
+// The same over a grid of pairs: pair (o, i), o < n_outer, i < n_inner, of
+// each array at base + (o * stride + i) * (its matrix size).
+cudaError_t launch_transition_apply_strided(const float* M, const float* H, const float* S,
+                                            float* out, long long n_outer, int n_inner,
+                                            long long m_stride, long long s_stride,
+                                            long long o_stride, int dk, int dv,
+                                            cudaStream_t stream);
+
+// cu_seg[n * P + s] = start of segment s of sequence n (equal-length sequences
+// of L tokens cut into P segments of seg_len tokens, the last ones shorter or
+// empty); cu_seg[N * P] = N * L.
+cudaError_t launch_segment_offsets(int* cu_seg, int n_seqs, long long seq_len, int n_segments,
+                                   long long seg_len, cudaStream_t stream);
 
 // Writes order[0..N) = sequence indices by decreasing length (ties by index).
 cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,

@@ -170,6 +170,54 @@ KDA_API int kda_chunk_fwd_gated(const void* q, const void* k, const void* v, con
                                 void* stream);
 
 /*
+ * Segment transitions, the building block of KDA context parallelism (the
+ * paper review's infrastructure section: each segment's state transition is
+ * computed locally and the segments are composed associatively).  For every
+ * (sequence, head), with the sequences of cu_seqlens taken as segments:
+ *   S_end = M S_0 + H  for every entry state S_0, where
+ *   M [dk, dk] = the product over the segment's tokens of
+ *                (I - beta_t k_t k_t^T) Diag(alpha_t)  (later tokens on the left)
+ *   H [dk, dv] = the end state from S_0 = 0.
+ * trans_M, trans_H: fp32 [N, H, dk, dk] and [N, H, dk, dv] (16-byte aligned).
+ * Runs the split tensor-core form (bf16, dk = dv = 128, chunk 64, N <= 1024;
+ * KDA_ERR_UNSUPPORTED otherwise) with a workspace of at least
+ * kda_chunk_transition_workspace_size(dims) bytes.  No outputs are written.
+ */
+KDA_API size_t kda_chunk_transition_workspace_size(const kda_dims* dims);
+KDA_API int kda_chunk_transition(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, const int* cu_seqlens, float* trans_M,
+                                 float* trans_H, int chunk, const kda_dims* dims,
+                                 void* workspace, size_t workspace_bytes, int* dev_status,
+                                 void* stream);
+
+/*
+ * S_out[p] = M[p] S_in[p] + H[p] for p < pairs (fp32 on the device; H may be
+ * NULL for no addend; dk, dv each 64 or 128).  With S_in = a later segment's
+ * entry state this moves a state across a segment; with (M, H) = (M2, H2) and
+ * S_in = H1 (then M1 with H = NULL) it composes (M2, H2) after (M1, H1).
+ * S_out must not alias S_in or M.
+ */
+KDA_API int kda_transition_apply(const float* M, const float* H, const float* S_in,
+                                 float* S_out, long long pairs, int dk, int dv, void* stream);
+
+/*
+ * Single-GPU KCP prefill: each of the N equal-length sequences (no
+ * cu_seqlens: T_total / N tokens each) is cut into n_segments segments
+ * (multiples of 64 tokens, the last ones shorter); every segment's transition
+ * is computed at once, the segments' entry states follow from the composed
+ * prefixes, and every segment then runs from its own entry state.  Results are
+ * those of kda_chunk_fwd on the same inputs (up to rounding).  bf16,
+ * dk = dv = 128, N * n_segments <= 1024; workspace of
+ * kda_chunk_fwd_kcp_workspace_size(dims, n_segments) bytes.
+ */
+KDA_API size_t kda_chunk_fwd_kcp_workspace_size(const kda_dims* dims, int n_segments);
+KDA_API int kda_chunk_fwd_kcp(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int n_segments, const kda_dims* dims,
+                              void* workspace, size_t workspace_bytes, int* dev_status,
+                              void* stream);
+
+/*
  * One recurrent decode step (the "dedicated kernels for KDA decode" of the
  * section "Infrastructure: how to actually run trillion-scale"; the state is
  * the fixed-size d_k x d_v cache object per head).  Every one of the N
