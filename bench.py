@@ -14,6 +14,7 @@ reports it under "decode".  Under torchrun every rank runs its own replica
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -337,7 +338,41 @@ def run_gpu(args):
              "achieved_gbs": g_bytes / (g_ms * 1e-3) / 1e9,
              "frac": g_bytes / (g_ms * 1e-3) / 1e9 / hbm_peak,
              "epilogue": "out = o / sqrt(mean(o^2) + 1e-6) * w * sigmoid(z), z [T, H, dv]"}
-    del d, args_pf, out, fin, gate
+    del gate
+
+    # ------- single-GPU KCP: 4 segments per sequence, and the transitions alone -------
+    kcp_seg = 4
+    dk_ = kda._dims(1, T, H, w.dk, w.dv, w.torch_dtype)
+    kws = torch.empty(int(kda.load().kda_chunk_fwd_kcp_workspace_size(ctypes.byref(dk_), kcp_seg)),
+                      dtype=torch.uint8, device=dev)
+
+    def kcp_step():
+        kda.chunk_fwd_kcp(*args_pf, d["init_state"], segments=kcp_seg, out=out,
+                          final_state=fin, workspace=kws)
+
+    tws = torch.empty(int(kda.load().kda_chunk_transition_workspace_size(ctypes.byref(dk_))),
+                      dtype=torch.uint8, device=dev)
+
+    def trans_step():
+        kda.chunk_transition(*args_pf, None, workspace=tws)
+
+    legs = {}
+    for name, fn in (("kcp_prefill", kcp_step), ("transition", trans_step)):
+        for _ in range(3):
+            fn()
+        barrier()
+        start.record(stream)
+        for _ in range(ck_steps):
+            fn()
+        end.record(stream)
+        barrier()
+        legs[name] = max_over_ranks(start.elapsed_time(end)) / ck_steps
+    kcp = {"segments": kcp_seg, "value": job_throughput(world, T, legs["kcp_prefill"]) / 1e6,
+           "unit": "Mtok/s", "ms_per_step": legs["kcp_prefill"], "steps": ck_steps,
+           "overhead_vs_plain": legs["kcp_prefill"] / ms_step - 1.0,
+           "transition_ms": legs["transition"],
+           "transition_mtok_s": job_throughput(world, T, legs["transition"]) / 1e6}
+    del d, args_pf, out, fin, kws, tws
     torch.cuda.empty_cache()
     decode = None
     if args.only != "prefill":
@@ -381,6 +416,7 @@ def run_gpu(args):
             "clocks": clocks,
             "prefill_checkpoints": ckpt,
             "prefill_gated": gated,
+            "kcp": kcp,
             "decode": decode,
         }
         print(json.dumps(line), flush=True)
