@@ -134,6 +134,44 @@ def output_gate(o, z, weight, eps):
     return o / np.sqrt(ms + float(eps)) * w * (1.0 / (1.0 + np.exp(-z)))
 
 
+G_MIN = -5.0
+CONV_LEN = 4
+
+
+def prologue(q_pre, k_pre, z, conv_q, conv_k, a_log, cu_seqlens=None, eps: float = 1e-6):
+    """KDA's input prologue, in fp64 ("[Paper Review] Kimi K3: Open Frontier
+    Intelligence", section "Kimi Delta Attention (KDA)": query and key pass
+    through a short convolution, then Swish, and are L2-normalised; the
+    log-decay is the scaled sigmoid g = g_min sigmoid(exp(A_h) z), g_min = -5;
+    the page lost both formulas, these are their plain readings).
+
+    q_pre, k_pre, z: [T, H, dk] pre-activations (z is the decay logit);
+    conv_q, conv_k: [H, dk, 4] depthwise causal kernels, tap 3 on the current
+    token (out_t = sum_i w[i] x_{t-3+i}, zero before each sequence's start);
+    a_log: [H] the per-head log-scale A_h.  Returns q, k, g ([T, H, dk] fp64).
+    """
+    xq, xk, zz = _f64(q_pre), _f64(k_pre), _f64(z)
+    wq, wk, al = _f64(conv_q), _f64(conv_k), _f64(a_log)
+    T, H, dk = xq.shape
+    cu = (np.array([0, T]) if cu_seqlens is None
+          else np.asarray(_f64(cu_seqlens), dtype=np.int64))
+
+    def branch(x, w):
+        y = np.zeros_like(x)
+        for n in range(len(cu) - 1):
+            t0, t1 = int(cu[n]), int(cu[n + 1])
+            for t in range(t0, t1):
+                for i in range(CONV_LEN):
+                    src = t - (CONV_LEN - 1) + i
+                    if src >= t0:
+                        y[t] += w[:, :, i] * x[src]
+        y = y / (1.0 + np.exp(-y))                    # Swish: y sigmoid(y)
+        return y / np.sqrt(np.sum(y * y, axis=-1, keepdims=True) + eps)
+
+    g = G_MIN / (1.0 + np.exp(-(np.exp(al)[None, :, None] * zz)))
+    return branch(xq, wq), branch(xk, wk), g
+
+
 def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, threads: int = 0,
             ckpt_interval: int = 0, gate=None):
     """Token-by-token fp64 KDA over packed sequences.

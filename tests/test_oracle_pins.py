@@ -398,3 +398,56 @@ def test_kcp_composition_is_associative_and_matches_the_whole_sequence():
     out, fin = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
     np.testing.assert_allclose(out_seg, out, rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(fin_seg[-1], fin[0], rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- prologue
+# ShortConv (4 causal depthwise taps, tap 3 on the current token) -> Swish ->
+# L2 norm for q and k; g = -5 sigmoid(exp(A_h) z) (paper review, section
+# "Kimi Delta Attention (KDA)"; the formulas are read from the prose).
+
+def test_prologue_hand_example():
+    gold = json.load(open(os.path.join(GOLDEN, "prologue_hand.json")))
+    x = np.array(gold["q_pre"])
+    w = np.array(gold["conv"])
+    q, k, g = oracle.prologue(x, x, np.array(gold["z"]), w, w, np.array(gold["a_log"]),
+                              None, eps=0.0)
+    np.testing.assert_allclose(q, gold["q"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(k, q, rtol=0, atol=0)
+    np.testing.assert_allclose(g, gold["g"], rtol=1e-14)
+
+
+def test_prologue_kernels_shifts_norms_and_decay():
+    rng = np.random.default_rng(61)
+    T, H, dk = 23, 2, 8
+    x = rng.standard_normal((T, H, dk))
+    z = rng.standard_normal((T, H, dk))
+    cu = np.array([0, 9, 9, 23])
+    imp = np.zeros((H, dk, 4))
+    imp[:, :, 3] = 1.0                         # the current token only
+    q, _, _ = oracle.prologue(x, x, z, imp, imp, np.zeros(H), cu, eps=0.0)
+    sw = x / (1.0 + np.exp(-x))
+    np.testing.assert_allclose(q, sw / np.linalg.norm(sw, axis=-1, keepdims=True), rtol=1e-13)
+    shift = np.zeros((H, dk, 4))
+    shift[:, :, 2] = 1.0                       # the previous token only
+    q, _, _ = oracle.prologue(x, x, z, shift, shift, np.zeros(H), cu, eps=1e-6)
+    for t0 in (0, 9):                          # nothing before a sequence start
+        assert np.all(q[t0] == 0.0)
+    swp = np.roll(sw, 1, axis=0)
+    for t in list(range(1, 9)) + list(range(10, 23)):
+        np.testing.assert_allclose(q[t], swp[t] / np.sqrt(np.sum(swp[t] ** 2, -1, keepdims=True)
+                                                           + 1e-6), rtol=1e-13)
+    w = rng.standard_normal((H, dk, 4))
+    a = rng.standard_normal(H)
+    q, k, g = oracle.prologue(x, x, z, w, w, a, cu, eps=0.0)
+    np.testing.assert_allclose(np.linalg.norm(q, axis=-1), 1.0, rtol=1e-13)
+    np.testing.assert_array_equal(k, q)               # same input, same kernel, same branch
+    assert np.all(g < 0) and np.all(g > -5)
+    _, _, g0 = oracle.prologue(x, x, np.exp(a)[None, :, None] * z, w, w, np.zeros(H), cu)
+    np.testing.assert_allclose(g, g0, rtol=1e-14)
+    _, _, gz = oracle.prologue(x, x, np.zeros_like(z), w, w, a, cu)
+    np.testing.assert_allclose(gz, -2.5, rtol=1e-15)
+    # Packing is separate calls: no tap reaches across a sequence boundary.
+    qa, _, _ = oracle.prologue(x[:9], x[:9], z[:9], w, w, a, None)
+    qb, _, _ = oracle.prologue(x[9:], x[9:], z[9:], w, w, a, None)
+    q, _, _ = oracle.prologue(x, x, z, w, w, a, cu)
+    np.testing.assert_allclose(q, np.concatenate([qa, qb]), rtol=1e-14)
