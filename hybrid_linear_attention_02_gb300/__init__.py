@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "chunk_transition", "transition_apply", "chunk_fwd_kcp", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
+__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "prologue", "chunk_transition", "transition_apply", "chunk_fwd_kcp", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libkda.so"
@@ -91,6 +91,8 @@ def load():
             lib.kda_chunk_fwd_kcp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
                                               vp]
             lib.kda_chunk_fwd_kcp.restype = ip
+            lib.kda_prologue.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
+            lib.kda_prologue.restype = ip
             lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
             lib.kda_chunk_fwd_algorithm.restype = ip
             _lib = lib
@@ -356,3 +358,30 @@ def chunk_fwd_kcp(q, k, v, g, beta, init_state=None, *, n_seqs: int = 1, segment
     if rc != 0:
         raise KDAError(rc, "kda_chunk_fwd_kcp")
     return out, final_state
+
+
+def prologue(q_pre, k_pre, z, conv_q, conv_k, a_log, cu_seqlens=None, *, n_seqs: int = 1,
+             q=None, k=None, g=None, stream=None):
+    """``kda_prologue``: (q, k, g) from the pre-activations ([T, H, dk], one
+    dtype), the 4-tap convolution kernels conv_q, conv_k (fp32 [H, dk, 4]) and
+    a_log (fp32 [H])."""
+    lib = load()
+    T, Hh, dk = q_pre.shape
+    dev, dt = q_pre.device, q_pre.dtype
+    for name, t in (("q_pre", q_pre), ("k_pre", k_pre), ("z", z)):
+        _check_input(name, t, (T, Hh, dk), dt, dev)
+    _check_input("conv_q", conv_q, (Hh, dk, 4), torch.float32, dev)
+    _check_input("conv_k", conv_k, (Hh, dk, 4), torch.float32, dev)
+    _check_input("a_log", a_log, (Hh,), torch.float32, dev)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else n_seqs
+    q = torch.empty_like(q_pre) if q is None else q
+    k = torch.empty_like(q_pre) if k is None else k
+    g = torch.empty_like(q_pre) if g is None else g
+    d = _dims(N, T, Hh, dk, dk, dt)
+    with torch.cuda.device(dev):
+        rc = lib.kda_prologue(_ptr(q_pre), _ptr(k_pre), _ptr(z), _ptr(conv_q), _ptr(conv_k),
+                              _ptr(a_log), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(g),
+                              ctypes.byref(d), _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_prologue")
+    return q, k, g

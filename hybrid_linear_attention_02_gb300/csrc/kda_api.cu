@@ -425,6 +425,36 @@ int kda_chunk_fwd_kcp(const void* q, const void* k, const void* v, const void* g
   return KDA_OK;
 }
 
+int kda_prologue(const void* q_pre, const void* k_pre, const void* z, const float* conv_q,
+                 const float* conv_k, const float* a_log, const int* cu_seqlens, void* q, void* k,
+                 void* g, const kda_dims* dims, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  const int N = dims->n_seqs;
+  if (dims->total_tokens == 0 || dims->heads == 0) return KDA_OK;
+  if (N <= 0) return KDA_ERR_INVALID;
+  if (!q_pre || !k_pre || !z || !conv_q || !conv_k || !a_log || !q || !k || !g)
+    return KDA_ERR_INVALID;
+  const void* vec[] = {q_pre, k_pre, z, conv_q, conv_k, q, k, g};
+  for (const void* p : vec)
+    if (!aligned(p, 16)) return KDA_ERR_ALIGNMENT;
+  long long seq_len = 0;
+  if (!cu_seqlens) {
+    if (dims->total_tokens % N != 0) return KDA_ERR_INVALID;
+    seq_len = dims->total_tokens / N;
+  }
+  kda::PrologueArgs a{};
+  a.q_pre = q_pre; a.k_pre = k_pre; a.z = z;
+  a.conv_q = conv_q; a.conv_k = conv_k; a.a_log = a_log;
+  a.cu_seqlens = cu_seqlens; a.seq_len = seq_len;
+  a.q = q; a.k = k; a.g = g;
+  a.n_seqs = N; a.heads = dims->heads; a.dk = dims->dk; a.dtype = dims->dtype;
+  a.total_tokens = dims->total_tokens;
+  return kda::launch_prologue(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
 int kda_decode_step_gated(const void* q, const void* k, const void* v, const void* g,
                           const void* beta, const void* gate, const float* norm_weight,
                           float eps, float* state, void* out, const kda_dims* dims,

@@ -63,6 +63,20 @@ cudaError_t launch_transition_apply_strided(const float* M, const float* H, cons
 cudaError_t launch_segment_offsets(int* cu_seg, int n_seqs, long long seq_len, int n_segments,
                                    long long seg_len, cudaStream_t stream);
 
+// The input prologue: q, k from their pre-activations (4-tap causal depthwise
+// convolution, Swish, L2 norm) and g = -5 sigmoid(exp(A_h) z).
+struct PrologueArgs {
+  const void *q_pre, *k_pre, *z;
+  const float *conv_q, *conv_k;   // [H, dk, 4]
+  const float* a_log;             // [H]
+  const int* cu_seqlens;          // nullable: sequences of seq_len tokens
+  long long seq_len;
+  void *q, *k, *g;
+  int n_seqs, heads, dk, dtype;
+  long long total_tokens;
+};
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream);
+
 // Writes order[0..N) = sequence indices by decreasing length (ties by index).
 cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,
                                 cudaStream_t stream);

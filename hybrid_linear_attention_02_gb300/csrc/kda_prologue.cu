@@ -1,0 +1,152 @@
+// KDA's input prologue in one pass ("[Paper Review] Kimi K3: Open Frontier
+// Intelligence", section "Kimi Delta Attention (KDA)"):
+//   q = L2norm(Swish(ShortConv_q(q_pre))),  k = L2norm(Swish(ShortConv_k(k_pre)))
+//   g = g_min sigmoid(exp(A_h) z),  g_min = -5
+// ShortConv is a depthwise causal convolution of 4 taps along each sequence
+// (tap 3 on the current token, zero before the sequence's first token);
+// L2norm(y) = y / sqrt(sum(y^2) + 1e-6) over the dk channels of a head.
+// One warp per (token, head) row, each lane dk / 32 consecutive channels; the
+// three earlier rows a tap reads come from L1/L2, so HBM sees each input and
+// output row about once.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kTaps = 4;
+constexpr float kGMin = -5.f;
+constexpr float kNormEps = 1e-6f;
+
+// PER consecutive elements as one vector access (8 or 16 bytes for PER = 4,
+// 4 or 8 bytes for PER = 2); the row offsets keep them aligned.
+template <int PER>
+__device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&y)[PER]) {
+  if constexpr (PER == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    y[0] = __uint_as_float(u.x << 16); y[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    y[2] = __uint_as_float(u.y << 16); y[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    y[0] = __uint_as_float(u << 16); y[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+}
+template <int PER>
+__device__ __forceinline__ void ldv(const float* p, float (&y)[PER]) {
+  if constexpr (PER == 4) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    y[0] = u.x; y[1] = u.y; y[2] = u.z; y[3] = u.w;
+  } else {
+    const float2 u = *reinterpret_cast<const float2*>(p);
+    y[0] = u.x; y[1] = u.y;
+  }
+}
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <int PER>
+__device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&y)[PER]) {
+  if constexpr (PER == 4)
+    *reinterpret_cast<uint2*>(p) = make_uint2(bf2(y[0], y[1]), bf2(y[2], y[3]));
+  else
+    *reinterpret_cast<uint32_t*>(p) = bf2(y[0], y[1]);
+}
+template <int PER>
+__device__ __forceinline__ void stv(float* p, const float (&y)[PER]) {
+  if constexpr (PER == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
+  constexpr int PER = DK / 32;
+  const int lane = threadIdx.x & 31;
+  const long long rows = a.total_tokens * a.heads;
+  const long long row = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const long long t = row / a.heads;
+  const int h = static_cast<int>(row % a.heads);
+  // First token of t's sequence: the last cu_seqlens entry <= t.
+  long long t0 = 0;
+  if (a.cu_seqlens) {
+    int lo = 0, hi = a.n_seqs;   // cu[lo] <= t < cu[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.cu_seqlens[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    t0 = a.cu_seqlens[lo];
+  } else if (a.seq_len > 0) {
+    t0 = t - t % a.seq_len;
+  }
+  const int c0 = PER * lane;
+  const long long rs = static_cast<long long>(a.heads) * DK;   // row stride
+
+#pragma unroll
+  for (int br = 0; br < 2; ++br) {
+    const T* x = static_cast<const T*>(br ? a.k_pre : a.q_pre);
+    const float* w = (br ? a.conv_k : a.conv_q) + (static_cast<long long>(h) * DK + c0) * kTaps;
+    T* y_out = static_cast<T*>(br ? a.k : a.q) + t * rs + static_cast<long long>(h) * DK + c0;
+    float4 wt[PER];   // the 4 taps of each channel
+#pragma unroll
+    for (int u = 0; u < PER; ++u) wt[u] = __ldg(reinterpret_cast<const float4*>(w) + u);
+    float y[PER] = {};
+#pragma unroll
+    for (int i = 0; i < kTaps; ++i) {
+      const long long src = t - (kTaps - 1) + i;
+      if (src < t0) continue;
+      float xv[PER];
+      ldv<PER>(x + src * rs + static_cast<long long>(h) * DK + c0, xv);
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const float wi = i == 0 ? wt[u].x : i == 1 ? wt[u].y : i == 2 ? wt[u].z : wt[u].w;
+        y[u] = fmaf(wi, xv[u], y[u]);
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      y[u] = __fdividef(y[u], 1.f + __expf(-y[u]));   // Swish
+      ss = fmaf(y[u], y[u], ss);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
+    const float rinv = rsqrtf(ss + kNormEps);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) y[u] *= rinv;
+    stv<PER>(y_out, y);
+  }
+  const float scale = __expf(__ldg(a.a_log + h));
+  const long long off = t * rs + static_cast<long long>(h) * DK + c0;
+  float zv[PER];
+  ldv<PER>(static_cast<const T*>(a.z) + off, zv);
+#pragma unroll
+  for (int u = 0; u < PER; ++u) zv[u] = __fdividef(kGMin, 1.f + __expf(-scale * zv[u]));
+  stv<PER>(static_cast<T*>(a.g) + off, zv);
+}
+
+template <typename T, int DK>
+cudaError_t launch_typed(const PrologueArgs& a, cudaStream_t s) {
+  const long long rows = a.total_tokens * a.heads;
+  const long long blocks = (rows + kWarps - 1) / kWarps;
+  if (blocks >= (1ll << 31)) return cudaErrorInvalidValue;
+  prologue_kernel<T, DK><<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
+  if (a.total_tokens == 0 || a.heads == 0) return cudaSuccess;
+  const bool f32 = a.dtype == KDA_F32;
+  if (a.dk == 128) return f32 ? launch_typed<float, 128>(a, s) : launch_typed<__nv_bfloat16, 128>(a, s);
+  if (a.dk == 64) return f32 ? launch_typed<float, 64>(a, s) : launch_typed<__nv_bfloat16, 64>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

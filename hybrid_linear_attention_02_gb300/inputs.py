@@ -176,3 +176,20 @@ def make_output_gate(T: int, H: int, dv: int, dtype, seed: int = 0, device="cpu"
     z = normal((T, H, dv)).to(dtype)
     w = 1.0 + 0.1 * normal((dv,))
     return z, w.float(), 1e-6
+
+
+def make_prologue_inputs(T: int, H: int, dk: int, dtype, seed: int = 0, device="cpu"):
+    """Synthetic prologue inputs: q_pre, k_pre ~ N(0, 1) and the decay logit
+    z ~ N(0, 1) ([T, H, dk], dtype), 4-tap kernels ~ N(0, 1/4) (fp32
+    [H, dk, 4]) and A_h ~ N(0, 0.25) (fp32 [H]; the page initialises A_h at 0,
+    a spread exercises its scaling)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 1_000_003 + 777_767)
+    normal = _normal(gen, device)
+    q_pre = normal((T, H, dk)).to(dtype)
+    k_pre = normal((T, H, dk)).to(dtype)
+    z = normal((T, H, dk)).to(dtype)
+    conv_q = 0.5 * normal((H, dk, 4))
+    conv_k = 0.5 * normal((H, dk, 4))
+    a_log = 0.5 * normal((H,))
+    return q_pre, k_pre, z, conv_q, conv_k, a_log

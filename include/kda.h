@@ -218,6 +218,29 @@ KDA_API int kda_chunk_fwd_kcp(const void* q, const void* k, const void* v, const
                               void* stream);
 
 /*
+ * KDA's input prologue, in one pass ("[Paper Review] Kimi K3: Open Frontier
+ * Intelligence", section "Kimi Delta Attention (KDA)": queries and keys pass
+ * through a short convolution and Swish and are L2-normalised; the log-decay
+ * is the lower-bounded scaled sigmoid; the page lost both formulas, read as):
+ *   q = L2norm(Swish(conv(q_pre, conv_q))),  k = L2norm(Swish(conv(k_pre, conv_k)))
+ *   g = -5 sigmoid(exp(a_log[h]) z)
+ * conv is depthwise and causal with 4 taps along each sequence, tap 3 on the
+ * current token (out_t = sum_i w[i] x_{t-3+i}, nothing before the sequence's
+ * first token); Swish(y) = y sigmoid(y); L2norm(y) = y / sqrt(sum(y^2) + 1e-6)
+ * over a head's dk channels.
+ *   q_pre, k_pre, z   [T_total, H, dk] pre-activations (dtype of dims), z the
+ *                     decay logit
+ *   conv_q, conv_k    fp32 [H, dk, 4];  a_log fp32 [H] (A_h)
+ *   cu_seqlens        as kda_chunk_fwd (NULL: N equal-length sequences)
+ *   q, k, g           [T_total, H, dk] outputs, ready for kda_chunk_fwd
+ * dims->dv is not used.  All vectors 16-byte aligned.
+ */
+KDA_API int kda_prologue(const void* q_pre, const void* k_pre, const void* z,
+                         const float* conv_q, const float* conv_k, const float* a_log,
+                         const int* cu_seqlens, void* q, void* k, void* g, const kda_dims* dims,
+                         void* stream);
+
+/*
  * One recurrent decode step (the "dedicated kernels for KDA decode" of the
  * section "Infrastructure: how to actually run trillion-scale"; the state is
  * the fixed-size d_k x d_v cache object per head).  Every one of the N
