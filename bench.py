@@ -372,7 +372,30 @@ def run_gpu(args):
            "overhead_vs_plain": legs["kcp_prefill"] / ms_step - 1.0,
            "transition_ms": legs["transition"],
            "transition_mtok_s": job_throughput(world, T, legs["transition"]) / 1e6}
-    del d, args_pf, out, fin, kws, tws
+    del kws, tws
+
+    # ------- input prologue (ShortConv, Swish, L2 norm; scaled-sigmoid decay) -------
+    px = inputs.make_prologue_inputs(T, H, w.dk, w.torch_dtype, seed=rank, device=dev)
+    pq, pk, pg = (torch.empty_like(px[0]) for _ in range(3))
+
+    def prologue_step():
+        kda.prologue(*px, None, q=pq, k=pk, g=pg)
+
+    for _ in range(3):
+        prologue_step()
+    barrier()
+    start.record(stream)
+    for _ in range(ck_steps):
+        prologue_step()
+    end.record(stream)
+    barrier()
+    p_ms = max_over_ranks(start.elapsed_time(end)) / ck_steps
+    p_bytes = 6 * T * H * w.dk * 2 + 2 * H * w.dk * 4 * 4 + H * 4
+    prologue = {"value": job_throughput(world, T, p_ms) / 1e6, "unit": "Mtok/s",
+                "ms_per_step": p_ms, "steps": ck_steps, "algorithmic_bytes_per_launch": p_bytes,
+                "achieved_gbs": p_bytes / (p_ms * 1e-3) / 1e9,
+                "frac": p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, "bound": "hbm"}
+    del d, args_pf, out, fin, px, pq, pk, pg
     torch.cuda.empty_cache()
     decode = None
     if args.only != "prefill":
@@ -417,6 +440,7 @@ def run_gpu(args):
             "prefill_checkpoints": ckpt,
             "prefill_gated": gated,
             "kcp": kcp,
+            "prologue": prologue,
             "decode": decode,
         }
         print(json.dumps(line), flush=True)

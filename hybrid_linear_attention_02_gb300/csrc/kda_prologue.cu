@@ -5,17 +5,20 @@
 // ShortConv is a depthwise causal convolution of 4 taps along each sequence
 // (tap 3 on the current token, zero before the sequence's first token);
 // L2norm(y) = y / sqrt(sum(y^2) + 1e-6) over the dk channels of a head.
-// One warp per (token, head) row, each lane dk / 32 consecutive channels; the
-// three earlier rows a tap reads come from L1/L2, so HBM sees each input and
-// output row about once.
+// One warp per head and 8 consecutive tokens, each lane dk / 32 consecutive
+// channels; the warp loads the 11 rows its taps read once per branch, so HBM
+// sees each input and output row about once.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;         // heads per block
+constexpr int kRowsPerWarp = 8;   // consecutive tokens per warp
 constexpr int kTaps = 4;
 constexpr float kGMin = -5.f;
 constexpr float kNormEps = 1e-6f;
@@ -62,17 +65,8 @@ __device__ __forceinline__ void stv(float* p, const float (&y)[PER]) {
     *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
 }
 
-template <typename T, int DK>
-__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
-  constexpr int PER = DK / 32;
-  const int lane = threadIdx.x & 31;
-  const long long rows = a.total_tokens * a.heads;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const long long t = row / a.heads;
-  const int h = static_cast<int>(row % a.heads);
-  // First token of t's sequence: the last cu_seqlens entry <= t.
-  long long t0 = 0;
+// First token of the sequence that holds token t.
+__device__ __forceinline__ long long seq_start(const PrologueArgs& a, long long t) {
   if (a.cu_seqlens) {
     int lo = 0, hi = a.n_seqs;   // cu[lo] <= t < cu[hi]
     while (hi - lo > 1) {
@@ -80,62 +74,121 @@ __global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
       if (a.cu_seqlens[mid] <= t) lo = mid;
       else hi = mid;
     }
-    t0 = a.cu_seqlens[lo];
-  } else if (a.seq_len > 0) {
-    t0 = t - t % a.seq_len;
+    return a.cu_seqlens[lo];
   }
-  const int c0 = PER * lane;
-  const long long rs = static_cast<long long>(a.heads) * DK;   // row stride
+  if (a.seq_len <= 0) return 0;
+  const unsigned sl = static_cast<unsigned>(a.seq_len);
+  return static_cast<long long>(static_cast<unsigned>(t) / sl) * sl;
+}
 
+// Warp w of block (b, hb) handles head 8 hb + w and tokens 8 b .. 8 b + 7: the
+// 11 rows its taps read are loaded once per branch.
+// Raw PER-element vectors (kept packed until used).
+template <typename T, int PER>
+struct Raw;
+template <>
+struct Raw<__nv_bfloat16, 4> { using type = uint2; };
+template <>
+struct Raw<__nv_bfloat16, 2> { using type = uint32_t; };
+template <>
+struct Raw<float, 4> { using type = float4; };
+template <>
+struct Raw<float, 2> { using type = float2; };
+
+template <int PER, typename R>
+__device__ __forceinline__ void unpack(const R& v, float (&y)[PER]) {
+  ldv<PER>(reinterpret_cast<const typename std::conditional<
+               sizeof(R) == 2 * PER, __nv_bfloat16, float>::type*>(&v), y);
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
+  constexpr int PER = DK / 32;
+  constexpr int R = kRowsPerWarp;
+  constexpr int WIN = R + kTaps - 1;
+  using RawT = typename Raw<T, PER>::type;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kWarps + (threadIdx.x >> 5);
+  if (h >= a.heads) return;
+  const long long tb = static_cast<long long>(blockIdx.x) * R;   // first token
+  const long long n_tok = a.total_tokens;
+  const int c0 = PER * lane;
+  const long long rs = static_cast<long long>(a.heads) * DK;      // row stride
+  const long long col = static_cast<long long>(h) * DK + c0;
+  // Every load first: the tap windows of q and k (rows tb - 3 .. tb + R - 1,
+  // clamped into the tensor) and the z rows.
+  RawT xw[2][WIN], zr[R];
 #pragma unroll
   for (int br = 0; br < 2; ++br) {
     const T* x = static_cast<const T*>(br ? a.k_pre : a.q_pre);
-    const float* w = (br ? a.conv_k : a.conv_q) + (static_cast<long long>(h) * DK + c0) * kTaps;
-    T* y_out = static_cast<T*>(br ? a.k : a.q) + t * rs + static_cast<long long>(h) * DK + c0;
+#pragma unroll
+    for (int i = 0; i < WIN; ++i) {
+      long long src = tb - (kTaps - 1) + i;
+      src = src < 0 ? 0 : src >= n_tok ? n_tok - 1 : src;
+      xw[br][i] = *reinterpret_cast<const RawT*>(x + src * rs + col);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    zr[r] = *reinterpret_cast<const RawT*>(static_cast<const T*>(a.z) +
+                                           (tb + r < n_tok ? tb + r : n_tok - 1) * rs + col);
+  long long t0[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) t0[r] = tb + r < n_tok ? seq_start(a, tb + r) : tb + r;
+
+#pragma unroll
+  for (int br = 0; br < 2; ++br) {
+    const float* w = (br ? a.conv_k : a.conv_q) + col * kTaps;
+    T* y_out = static_cast<T*>(br ? a.k : a.q) + col;
     float4 wt[PER];   // the 4 taps of each channel
 #pragma unroll
     for (int u = 0; u < PER; ++u) wt[u] = __ldg(reinterpret_cast<const float4*>(w) + u);
-    float y[PER] = {};
 #pragma unroll
-    for (int i = 0; i < kTaps; ++i) {
-      const long long src = t - (kTaps - 1) + i;
-      if (src < t0) continue;
-      float xv[PER];
-      ldv<PER>(x + src * rs + static_cast<long long>(h) * DK + c0, xv);
+    for (int r = 0; r < R; ++r) {
+      const long long t = tb + r;
+      float y[PER] = {};
+#pragma unroll
+      for (int i = 0; i < kTaps; ++i) {
+        const bool on = t - (kTaps - 1) + i >= t0[r];
+        float xv[PER];
+        unpack<PER>(xw[br][r + i], xv);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const float wi = i == 0 ? wt[u].x : i == 1 ? wt[u].y : i == 2 ? wt[u].z : wt[u].w;
+          y[u] = fmaf(on ? wi : 0.f, xv[u], y[u]);
+        }
+      }
+      float ss = 0.f;
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
-        const float wi = i == 0 ? wt[u].x : i == 1 ? wt[u].y : i == 2 ? wt[u].z : wt[u].w;
-        y[u] = fmaf(wi, xv[u], y[u]);
+        y[u] = __fdividef(y[u], 1.f + __expf(-y[u]));   // Swish
+        ss = fmaf(y[u], y[u], ss);
       }
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
+      const float rinv = rsqrtf(ss + kNormEps);
+#pragma unroll
+      for (int u = 0; u < PER; ++u) y[u] *= rinv;
+      if (t < n_tok) stv<PER>(y_out + t * rs, y);
     }
-    float ss = 0.f;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      y[u] = __fdividef(y[u], 1.f + __expf(-y[u]));   // Swish
-      ss = fmaf(y[u], y[u], ss);
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
-    const float rinv = rsqrtf(ss + kNormEps);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) y[u] *= rinv;
-    stv<PER>(y_out, y);
   }
   const float scale = __expf(__ldg(a.a_log + h));
-  const long long off = t * rs + static_cast<long long>(h) * DK + c0;
-  float zv[PER];
-  ldv<PER>(static_cast<const T*>(a.z) + off, zv);
 #pragma unroll
-  for (int u = 0; u < PER; ++u) zv[u] = __fdividef(kGMin, 1.f + __expf(-scale * zv[u]));
-  stv<PER>(static_cast<T*>(a.g) + off, zv);
+  for (int r = 0; r < R; ++r) {
+    float zv[PER];
+    unpack<PER>(zr[r], zv);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) zv[u] = __fdividef(kGMin, 1.f + __expf(-scale * zv[u]));
+    if (tb + r < n_tok) stv<PER>(static_cast<T*>(a.g) + (tb + r) * rs + col, zv);
+  }
 }
 
 template <typename T, int DK>
 cudaError_t launch_typed(const PrologueArgs& a, cudaStream_t s) {
-  const long long rows = a.total_tokens * a.heads;
-  const long long blocks = (rows + kWarps - 1) / kWarps;
-  if (blocks >= (1ll << 31)) return cudaErrorInvalidValue;
-  prologue_kernel<T, DK><<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(a);
+  const long long tblocks = (a.total_tokens + kRowsPerWarp - 1) / kRowsPerWarp;
+  if (tblocks >= (1ll << 31)) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(tblocks), (a.heads + kWarps - 1) / kWarps);
+  prologue_kernel<T, DK><<<grid, 32 * kWarps, 0, s>>>(a);
   return cudaGetLastError();
 }
 
