@@ -93,7 +93,8 @@ constexpr uint32_t kPOffD = kPOffA + 64 * kLdA * 4;        // D   4 x 16 x 20
 constexpr uint32_t kPOffN = kPOffD + 4 * 16 * kLdB * 4;    // N   6 x 16 x 20
 constexpr uint32_t kPOffN2 = kPOffN + 6 * 16 * kLdB * 4;   // N^2 3 x 16 x 20
 constexpr uint32_t kPOffN3 = kPOffN2 + 3 * 16 * kLdB * 4;  // N^3 16 x 20
-static_assert(kPOffN3 + 16 * kLdB * 4 <= kPOffKH + 40960, "inverse scratch fits");
+constexpr uint32_t kPOffAt = kPOffN3 + 16 * kLdB * 4;     // A_bb^T 4 x 16 x 20
+static_assert(kPOffAt + 4 * 16 * kLdB * 4 <= kPOffKH + 40960, "inverse scratch fits");
 constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W (lanes 0..63) reuses 0..127
 enum { kPBarAP = 0, kPBarW, kPBarRaw, kPNumBars };
 
@@ -272,11 +273,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
   float* Nm = reinterpret_cast<float*>(smem + kPOffN);
   float* N2m = reinterpret_cast<float*>(smem + kPOffN2);
   float* N3m = reinterpret_cast<float*>(smem + kPOffN3);
+  float* Atm = reinterpret_cast<float*>(smem + kPOffAt);
   float* tile_tot = reinterpret_cast<float*>(smem + kPOffTileTot);
   float* tabR = reinterpret_cast<float*>(smem + kPOffTabR);
 
-  // Raw k, q (into the [K';Q'] tile) and g (into the Ktil tile), two boxes each.
-  auto issue_raw = [&](const Item& x) {
+  // Raw k, q (into the [K';Q'] tile, free once the masked products are done)
+  // and g (into the Ktil tile, free once W is done), two boxes each, all on
+  // one barrier phase: the first call expects the bytes of both.
+  auto issue_raw_kq = [&](const Item& x) {
     const int c0 = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
     uint64_t* bar = &s_bars[kPBarRaw];
     mbar_arrive_expect_tx(bar, 3 * 16384);
@@ -284,8 +288,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
     for (int hf = 0; hf < 2; ++hf) {
       tma_load_3d(smem + kPOffKQ + hf * 8192, &tm_k, 64 * hf, x.h, c0, bar);
       tma_load_3d(smem + kPOffKQ + 16384 + hf * 8192, &tm_q, 64 * hf, x.h, c0, bar);
-      tma_load_3d(smem + kPOffKT + hf * 8192, &tm_g, 64 * hf, x.h, c0, bar);
     }
+  };
+  auto issue_raw_g = [&](const Item& x) {
+    const int c0 = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+      tma_load_3d(smem + kPOffKT + hf * 8192, &tm_g, 64 * hf, x.h, c0, &s_bars[kPBarRaw]);
   };
   float rb[4];
   auto load_beta = [&](const Item& x) {
@@ -304,7 +313,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_g);
-    issue_raw(cur);
+    issue_raw_kq(cur);
+    issue_raw_g(cur);
   }
   load_beta(cur);
 
@@ -319,8 +329,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const int L = static_cast<int>(cur.t1 - c0 < kC ? cur.t1 - c0 : kC);
     uint8_t* rec = win.rec + static_cast<size_t>(it) * kRecBytes;
     const int it_next = it + it_step;
-    Item nxt = cur;
-    if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
+    Item nxt = cur;   // decoded while the masked products run
 
     // The previous item's T' store has read the TB tile before P1 rewrites
     // it (its -W store, the newest bulk group, may still be reading Khat's
@@ -329,7 +338,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
-    if (it_next < it_end) load_beta(nxt);
     named_bar(2, kPThreads);
     KDA_SMARK(0);
     const bool ok_raw = sync.wait(kPBarRaw, par);
@@ -470,16 +478,34 @@ __global__ void __launch_bounds__(kPThreads, 2)
       }
       // Kbar^T (row = key channel, 4 tokens row0 .. row0 + 3 per 8-byte
       // piece) replaces the factor tables once every thread has read them.
+      // Step s of lane x = lane & 7 writes channel row 8 cg + (s ^ x): the
+      // eight lanes of a token group then hit eight different swizzled
+      // 16-byte chunks instead of one.  okb[m][w] is first permuted to
+      // okb[m][w ^ (x >> 1)], so step s reads register pair s >> 1.
+      const int x = lane & 7;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (x & 2) {
+          uint32_t t = okb[m][0]; okb[m][0] = okb[m][1]; okb[m][1] = t;
+          t = okb[m][2]; okb[m][2] = okb[m][3]; okb[m][3] = t;
+        }
+        if (x & 4) {
+          uint32_t t = okb[m][0]; okb[m][0] = okb[m][2]; okb[m][2] = t;
+          t = okb[m][1]; okb[m][1] = okb[m][3]; okb[m][3] = t;
+        }
+      }
+      const uint32_t sel_even = (x & 1) ? 0x7632u : 0x5410u;   // halves of channel pair
+      const uint32_t sel_odd = (x & 1) ? 0x5410u : 0x7632u;
+      uint8_t* kbt = smem + kPOffTB + static_cast<uint32_t>(8 * cg) * 128u + (row0 & 7) * 2;
       named_bar(2, kPThreads);
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t sel = e ? 0x7632u : 0x5410u;
-          *reinterpret_cast<uint2*>(smem + kPOffTB + sw128_off(8 * cg + 2 * w + e, row0, 128)) =
-              make_uint2(__byte_perm(okb[0][w], okb[1][w], sel),
-                         __byte_perm(okb[2][w], okb[3][w], sel));
-        }
+      for (int st = 0; st < 8; ++st) {
+        const int w = st >> 1, j = st ^ x;
+        const uint32_t sel = (st & 1) ? sel_odd : sel_even;
+        *reinterpret_cast<uint2*>(kbt + j * 128 + (((row0 >> 3) ^ j) << 4)) =
+            make_uint2(__byte_perm(okb[0][w], okb[1][w], sel),
+                       __byte_perm(okb[2][w], okb[3][w], sel));
+      }
     }
     fence_async_smem();
     named_bar(2, kPThreads);
@@ -500,21 +526,32 @@ __global__ void __launch_bounds__(kPThreads, 2)
                   umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarAP]);
     }
+    if (it_next < it_end) {
+      nxt = decode_item(args, win, s_cum, it_next);
+      load_beta(nxt);
+    }
     const bool ok_ap = sync.wait(kPBarAP, par);
     tc_fence_after();
+    // [K';Q'] is dead: the next item's raw k and q may land.
+    if (loader && ok_ap && it_next < it_end) issue_raw_kq(nxt);
     KDA_SMARK(5);
 
     // ---- P4: A (x beta, strictly lower; fp32, shared) and P (lower inclusive;
-    // bf16, straight to the record).
-    if (pw < 4 && ok_ap) {
-      const int a = pw, rl = lane & 15, r = 16 * a + rl;
+    // bf16, straight to the record).  Warps pw and pw + 4 share row tile
+    // pw & 3 (the same TMEM lanes): the first takes column blocks 0 and 2, the
+    // second 1 and 3.  A's blocks above the diagonal are never read, so only
+    // P's are written (as zeros); A's diagonal blocks go out transposed (the
+    // substitution below reads them by column).
+    if (ok_ap) {
+      const int a = pw & 3, b0 = pw >> 2, rl = lane & 15, r = 16 * a + rl;
       const bool isP = lane >= 16;
       const float br = s_beta[r];
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int j = 0; j < 2; ++j) {
+        const int blk = b0 + 2 * j;
         float v[16];
         if (blk <= a) {
-          tmem_ld16(tbase + (static_cast<uint32_t>(32 * pw) << 16) + khat_row0(a) + 16 * blk, v);
+          tmem_ld16(tbase + (static_cast<uint32_t>(32 * a) << 16) + khat_row0(a) + 16 * blk, v);
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
@@ -533,7 +570,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
             for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
             st_tile8(rec + kRecKP, 128 + r, 16 * blk + 8 * h8, 192, f8);
           }
-        } else {
+        } else if (blk == a) {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) Atm[(16 * a + u) * kLdB + rl] = v[u];
+        } else if (blk < a) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             *reinterpret_cast<float4*>(&Am[r * kLdA + 16 * blk + 4 * q4]) =
@@ -551,32 +591,30 @@ __global__ void __launch_bounds__(kPThreads, 2)
     // T' = T diag(beta) in bf16 (same block scheme as the fused kernel).
     if (p < 64) {
       const int blk = p >> 4, jj = p & 15;
-      // Column jj of D_bb by forward substitution; the block's rows stream
-      // from shared memory (the 16 threads of a block read the same words).
-      const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
-      float x[16];
+      // Column jj of D_bb by right-looking substitution: once x_i is final it
+      // is taken off every later row, so the dependent chain is one FMA per
+      // row.  Column i of A_bb is row i of its transposed copy (the 16
+      // threads of a block read the same words).
+      const float* At = Atm + 16 * blk * kLdB;
+      float y[16];
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        float acc0 = 0.f, acc1 = 0.f;
+      for (int r = 0; r < 16; ++r) y[r] = r == jj ? 1.f : 0.f;
+#pragma unroll
+      for (int i = 0; i < 15; ++i) {
+        const float xi = y[i];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (4 * q < rr) {
-            const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
+          if (4 * q + 3 > i) {
+            const float4 v = *reinterpret_cast<const float4*>(At + i * kLdB + 4 * q);
             const float a4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i = 4 * q + u;
-              if (i < rr) {
-                if (i & 1) acc1 = fmaf(a4[u], x[i], acc1);
-                else acc0 = fmaf(a4[u], x[i], acc0);
-              }
-            }
+            for (int u = 0; u < 4; ++u)
+              if (4 * q + u > i) y[4 * q + u] = fmaf(-a4[u], xi, y[4 * q + u]);
           }
         }
-        x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -(acc0 + acc1));
       }
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = x[rr];
+      for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = y[rr];
     } else {
       for (int e = p - 64; e < 192; e += kPThreads - 64) {
         const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
@@ -736,28 +774,29 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const bool ok_w = sync.wait(kPBarW, par);
     tc_fence_after();
     KDA_SMARK(12);
-    // [K';Q'] and Ktil are dead: the next item's raw tiles may land.
-    if (loader && ok_w && it_next < it_end) issue_raw(nxt);
+    // Ktil is dead: the next item's raw g may land.
+    if (loader && ok_w && it_next < it_end) issue_raw_g(nxt);
 
     // ---- P7: -W (row = token, column = key channel) staged where Khat was;
     // its two 64-channel panels are rows 64..127 of the record's WQ panels.
     // Warps 0, 1 take channels 0..63 and warps 4, 5 channels 64..127 of
     // TMEM lanes 0..63.
     if ((pw & 3) < 2 && ok_w) {
-      const int t = 32 * (pw & 3) + lane;
-#pragma unroll 1
-      for (int q32 = 2 * (pw >> 2); q32 < 2 * (pw >> 2) + 2; ++q32) {
-        float w[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + 32 * q32, w);
-        tmem_ld_wait();
+      const int t = 32 * (pw & 3) + lane, q0 = 2 * (pw >> 2);
+      float w[2][32];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        tmem_ld32(tbase + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + 32 * (q0 + j), w[j]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           float f8[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) f8[u] = -w[8 * q8 + u];
-          st_tile8(smem + kPOffKH, t, 32 * q32 + 8 * q8, 64, f8);
+          for (int u = 0; u < 8; ++u) f8[u] = -w[j][8 * q8 + u];
+          st_tile8(smem + kPOffKH, t, 32 * (q0 + j) + 8 * q8, 64, f8);
         }
-      }
     }
     fence_async_smem();
     tc_fence_before();
