@@ -17,8 +17,8 @@
 //    state-independent chain (cumulative decay, scaled operand tiles, the
 //    masked products A and P in one MMA, T by block-Neumann inversion,
 //    W = T' Ktil by MMA) and writes one 66,048-byte record per chunk: the
-//    byte images of the operand tiles the state pass reads (Qtil, -W,
-//    Kbar^T, P, T' = T diag(beta)) and e^{G_C}.
+//    byte images of the operand tiles the state pass reads (Qtil, -W, Kbar,
+//    P, T' = T diag(beta)) and e^{G_C}.
 //  chunk_state_kernel: one CTA per pair walks its chunks in order; a producer
 //    warp streams records (1-D bulk copies) and v tiles (TMA) into a two-slot
 //    ring, one warp issues every MMA, and eight warps (two per TMEM lane
@@ -26,7 +26,7 @@
 //    resident in TMEM and the bf16 operands:
 //      U0^T = V^T T'^T                                     (MMA0, off the chain)
 //      [O^T | U^T] = S^T [Qtil; -W]^T,  U^T += U0^T         (MMA1, N = 128)
-//      [S^T | O^T] += U^T [Kbar^T; P]^T                     (MMA2, N = 192)
+//      S^T += U^T Kbar,  O^T += U^T P^T                      (MMA2, N = 128 + 64)
 //    The serial chain per chunk is MMA1 -> U^T to bf16 -> MMA2 -> S^T to
 //    bf16 (with the next chunk's decay Diag(e^{G_C}) applied to the fp32
 //    copy in the same pass); the previous chunk's output stores run while
@@ -55,10 +55,12 @@ using namespace chunk;
 // ---- one chunk record: shared-memory operand images, 1024-aligned tiles.
 // WQ: K-major B operand, N = 128 rows (rows 0..63 Qtil, rows 64..127 -W, one
 //     per token) by K = 128 key channels; two 16 KB channel panels.
-// KP: K-major B operand, N = 192 rows by K = 64 tokens: Kbar^T (rows 0..127,
-//     one per key channel), then P (rows 128..191, one per output token).
+// KB: Kbar, one row per token: an MN-major B operand (N = 128 key channels
+//     in two 64-channel panels, K = 64 tokens).
+// P:  K-major B operand, 64 rows (one per output token) by K = 64 tokens.
 constexpr uint32_t kRecWQ = 0;       // [Qtil; -W]        128 x 128
-constexpr uint32_t kRecKP = 32768;   // [Kbar^T; P]       192 x 64
+constexpr uint32_t kRecKB = 32768;   // Kbar              64 x 128
+constexpr uint32_t kRecP = 49152;    // P                 64 x 64
 constexpr uint32_t kRecT = 57344;    // T' = T diag(beta) 64 x 64  (K-major B)
 constexpr uint32_t kRecG = 65536;    // e^{G_C}, fp32 [128]
 constexpr uint32_t kRecBytes = 66048;
@@ -79,8 +81,8 @@ constexpr int kPThreads = 256;
 constexpr uint32_t kPOffKQ = 0;        // [K';Q'] 128 x 128; raw k at 0, raw q at 16384
 constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W
 constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128; raw g before P2
-// TB: tile sums and e^{R_a} tables (P1/P2), then Kbar^T (P2..P4), then
-// [T'; 0] 128 x 64, the A operand of W = T' Ktil (rows 64..127 zero).
+// TB: tile sums and e^{R_a} tables (P1/P2), then [T'; 0] 128 x 64, the A
+// operand of W = T' Ktil (rows 64..127 zero).
 constexpr uint32_t kPOffTB = 90112;
 constexpr uint32_t kPTiles = 106496;
 constexpr uint32_t kPSmem = kPTiles + 1024;
@@ -329,7 +331,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const int L = static_cast<int>(cur.t1 - c0 < kC ? cur.t1 - c0 : kC);
     uint8_t* rec = win.rec + static_cast<size_t>(it) * kRecBytes;
     const int it_next = it + it_step;
-    Item nxt = cur;   // decoded while the masked products run
+    // The next item, decoded now so that its loads are done by the masked
+    // products' MMA, where its beta is fetched and its raw tiles are issued.
+    Item nxt = cur;
+    if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
 
     // The previous item's T' store has read the TB tile before P1 rewrites
     // it (its -W store, the newest bulk group, may still be reading Khat's
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     named_bar(2, kPThreads);
     KDA_SMARK(3);
 
-    // ---- P2: scaled operand tiles; Qtil goes straight to the record.
+    // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
     {
       const int sc0 = 4 * cg;
       auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
@@ -432,13 +437,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
             make_uint4(v[0], v[1], v[2], v[3]);
       };
       uint64_t kh[4][4];
-      uint32_t okb[4][4];   // Kbar rows of this thread (bf16 pairs)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int r = row0 + m, rl = 4 * r4 + m;
         const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
         const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
-        uint32_t okp[4], oqp[4], okt[4], okh[4], oqt[4];
+        uint32_t okp[4], oqp[4], okt[4], okh[4], oqt[4], okb[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
@@ -452,13 +456,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
           oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
           kh[m][w] = f2_mul(kp, ei);
           okh[w] = f2_to_bf16x2(kh[m][w]);
-          okb[m][w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
+          okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
         }
         st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
         st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
         st4(smem + kPOffKT, r, 64, okt);
         st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
         st4(rec + kRecWQ, r, 128, oqt);
+        st4(rec + kRecKB, r, 64, okb);
       }
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
@@ -476,43 +481,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
           }
         }
       }
-      // Kbar^T (row = key channel, 4 tokens row0 .. row0 + 3 per 8-byte
-      // piece) replaces the factor tables once every thread has read them.
-      // Step s of lane x = lane & 7 writes channel row 8 cg + (s ^ x): the
-      // eight lanes of a token group then hit eight different swizzled
-      // 16-byte chunks instead of one.  okb[m][w] is first permuted to
-      // okb[m][w ^ (x >> 1)], so step s reads register pair s >> 1.
-      const int x = lane & 7;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        if (x & 2) {
-          uint32_t t = okb[m][0]; okb[m][0] = okb[m][1]; okb[m][1] = t;
-          t = okb[m][2]; okb[m][2] = okb[m][3]; okb[m][3] = t;
-        }
-        if (x & 4) {
-          uint32_t t = okb[m][0]; okb[m][0] = okb[m][2]; okb[m][2] = t;
-          t = okb[m][1]; okb[m][1] = okb[m][3]; okb[m][3] = t;
-        }
-      }
-      const uint32_t sel_even = (x & 1) ? 0x7632u : 0x5410u;   // halves of channel pair
-      const uint32_t sel_odd = (x & 1) ? 0x5410u : 0x7632u;
-      uint8_t* kbt = smem + kPOffTB + static_cast<uint32_t>(8 * cg) * 128u + (row0 & 7) * 2;
-      named_bar(2, kPThreads);
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const int w = st >> 1, j = st ^ x;
-        const uint32_t sel = (st & 1) ? sel_odd : sel_even;
-        *reinterpret_cast<uint2*>(kbt + j * 128 + (((row0 >> 3) ^ j) << 4)) =
-            make_uint2(__byte_perm(okb[0][w], okb[1][w], sel),
-                       __byte_perm(okb[2][w], okb[3][w], sel));
-      }
     }
     fence_async_smem();
     named_bar(2, kPThreads);
-    if (leader && !s_abort) {
-      bulk_store(rec + kRecKP, smem + kPOffTB, 16384);
-      bulk_commit();
-    }
     KDA_SMARK(4);
 
     // ---- P3: every masked intra-chunk product in one MMA (M=128, N=160, K=128).
@@ -526,10 +497,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
                   umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarAP]);
     }
-    if (it_next < it_end) {
-      nxt = decode_item(args, win, s_cum, it_next);
-      load_beta(nxt);
-    }
+    if (it_next < it_end) load_beta(nxt);
     const bool ok_ap = sync.wait(kPBarAP, par);
     tc_fence_after();
     // [K';Q'] is dead: the next item's raw k and q may land.
@@ -568,7 +536,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
             float f8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
-            st_tile8(rec + kRecKP, 128 + r, 16 * blk + 8 * h8, 192, f8);
+            st_tile8(rec + kRecP, r, 16 * blk + 8 * h8, 64, f8);
           }
         } else if (blk == a) {
 #pragma unroll
@@ -581,8 +549,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
       }
     }
-    // Kbar^T has left the TB tile before P5 writes T' there.
-    if (leader) bulk_wait_read_all();
     tc_fence_before();
     named_bar(2, kPThreads);
     KDA_SMARK(6);
@@ -967,19 +933,23 @@ __global__ void __launch_bounds__(kSThreads, 1)
                              t > 0);
           umma_commit(&s_bars[kSBarMMA1]);
         }
-        // [S^T | O^T] += U^T [Kbar^T; P]^T        (M = 128, N = 192, K = 64 tokens)
+        // S^T += U^T Kbar,  O^T += U^T P^T        (M = 128, N = 128 + 64, K = 64 tokens)
         if (!sync.wait(kSBarUT, c & 1)) break;
         tc_fence_after();
 #ifdef KDA_PHASE_PROFILE
         s_ts[1] = clock64();
 #endif
         {
-          const uint32_t idesc = umma_idesc_bf16(128, 192, 0, 0);
-          const uint32_t bKP = smem_u32(slot + kRecKP);
+          const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 1);
+          const uint32_t idesc_o = umma_idesc_bf16(128, 64, 0, 0);
+          const uint32_t bKB = smem_u32(slot + kRecKB), bP = smem_u32(slot + kRecP);
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
+          for (int t = 0; t < 4; ++t) {
             umma_bf16_tmem_a(tbase + kSColS, tbase + kSColUT + 8 * t,
-                             umma_desc(bKP + t * 32, 16, 1024), idesc, 1);
+                             umma_desc(bKB + t * 2048, 64 * 128, 1024), idesc_s, 1);
+            umma_bf16_tmem_a(tbase + kSColO, tbase + kSColUT + 8 * t,
+                             umma_desc(bP + t * 32, 16, 1024), idesc_o, 1);
+          }
           umma_commit(&s_bars[kSBarEmpty0 + s]);
           umma_commit(&s_bars[kSBarMMA2]);
         }
