@@ -508,8 +508,19 @@ __global__ void __launch_bounds__(kPThreads, 2)
     // bf16, straight to the record).  Warps pw and pw + 4 share row tile
     // pw & 3 (the same TMEM lanes): the first takes column blocks 0 and 2, the
     // second 1 and 3.  A's blocks above the diagonal are never read, so only
-    // P's are written (as zeros); A's diagonal blocks go out transposed (the
-    // substitution below reads them by column).
+    // P's are written (as zeros); A's diagonal blocks go out transposed, and
+    // the warp that holds one also inverts it (P5 below).
+    // The [T'; 0] tile's zeros (blocks above the diagonal, rows 64..127) go
+    // in first: the factor tables that shared the tile are dead.
+    for (int e = p; e < 192; e += kPThreads) {
+      const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+      const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
+      const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      st_tile8(smem + kPOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
+    }
+    for (int e = p; e < 512; e += kPThreads)
+      *reinterpret_cast<uint4*>(smem + kPOffTB + 8192 + 16 * e) = make_uint4(0, 0, 0, 0);
     if (ok_ap) {
       const int a = pw & 3, b0 = pw >> 2, rl = lane & 15, r = 16 * a + rl;
       const bool isP = lane >= 16;
@@ -548,52 +559,42 @@ __global__ void __launch_bounds__(kPThreads, 2)
                 make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
         }
       }
+      // ---- P5 (diagonal blocks): D_aa = (I + A_aa)^-1, column jj = lane by
+      // right-looking substitution: once x_i is final it is taken off every
+      // later row, so the dependent chain is one FMA per row.  Column i of
+      // A_aa is row i of its transposed copy (the 16 lanes read the same words).
+      if (b0 == (a & 1)) {
+        __syncwarp();
+        if (lane < 16) {
+          const int jj = lane;
+          const float* At = Atm + 16 * a * kLdB;
+          float y[16];
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) y[rr] = rr == jj ? 1.f : 0.f;
+#pragma unroll
+          for (int i = 0; i < 15; ++i) {
+            const float xi = y[i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (4 * q + 3 > i) {
+                const float4 w4 = *reinterpret_cast<const float4*>(At + i * kLdB + 4 * q);
+                const float a4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (4 * q + u > i) y[4 * q + u] = fmaf(-a4[u], xi, y[4 * q + u]);
+              }
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) Dm[(a * 16 + rr) * kLdB + jj] = y[rr];
+        }
+      }
     }
     tc_fence_before();
     named_bar(2, kPThreads);
     KDA_SMARK(6);
-
-    // ---- P5: T = (I + A)^-1 = (I - N + N^2 - N^3) D in fp32, written as
-    // T' = T diag(beta) in bf16 (same block scheme as the fused kernel).
-    if (p < 64) {
-      const int blk = p >> 4, jj = p & 15;
-      // Column jj of D_bb by right-looking substitution: once x_i is final it
-      // is taken off every later row, so the dependent chain is one FMA per
-      // row.  Column i of A_bb is row i of its transposed copy (the 16
-      // threads of a block read the same words).
-      const float* At = Atm + 16 * blk * kLdB;
-      float y[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) y[r] = r == jj ? 1.f : 0.f;
-#pragma unroll
-      for (int i = 0; i < 15; ++i) {
-        const float xi = y[i];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (4 * q + 3 > i) {
-            const float4 v = *reinterpret_cast<const float4*>(At + i * kLdB + 4 * q);
-            const float a4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (4 * q + u > i) y[4 * q + u] = fmaf(-a4[u], xi, y[4 * q + u]);
-          }
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = y[rr];
-    } else {
-      for (int e = p - 64; e < 192; e += kPThreads - 64) {
-        const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
-        const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
-        const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
-        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        st_tile8(smem + kPOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
-      }
-      // Rows 64..127 of the [T'; 0] operand.
-      for (int e = p - 64; e < 512; e += kPThreads - 64)
-        *reinterpret_cast<uint4*>(smem + kPOffTB + 8192 + 16 * e) = make_uint4(0, 0, 0, 0);
-    }
-    named_bar(2, kPThreads);
+    // ---- P5: T = (I + A)^-1 = (I - N + N^2 - N^3) D in fp32 with N = D A
+    // (strictly block-lower, N^4 = 0), written as T' = T diag(beta) in bf16.
     KDA_SMARK(7);
     // Block products, one warp per 16 x 16 x 16 product: lane (i4, j2) owns
     // rows 4 i4 .. + 3 and columns 2 j2, 2 j2 + 1 of the output block.
@@ -653,13 +654,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     named_bar(2, kPThreads);
     KDA_SMARK(8);
-    // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
-    if (pw < 3) {
+    // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, and (3,0) = N31 N10
+    // + N32 N20 as two halves (warps 2, 3; the second where A_bb^T was).
+    if (pw < 4) {
       float acc[4][2] = {};
-      const int xa = pw == 0 ? 2 : pw == 1 ? 5 : 4, ya = pw == 0 ? 0 : pw == 1 ? 2 : 0;
+      const int xa = pw == 0 ? 2 : pw == 1 ? 5 : pw == 2 ? 4 : 5;
+      const int ya = pw == 0 ? 0 : pw == 1 ? 2 : pw == 2 ? 0 : 1;
       prod16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, acc);
-      if (pw == 2) prod16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, acc);
-      store_blk(N2m + pw * 16 * kLdB, acc);
+      store_blk(pw < 3 ? N2m + pw * 16 * kLdB : Atm, acc);
     }
     named_bar(2, kPThreads);
     KDA_SMARK(9);
@@ -698,10 +700,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const int row = 4 * i4 + i;
           float2* nv = reinterpret_cast<float2*>(Nm + (3 * 16 + row) * kLdB + 2 * j2);
           const float2 n2 = *reinterpret_cast<const float2*>(N2m + (2 * 16 + row) * kLdB + 2 * j2);
+          const float2 n2b = *reinterpret_cast<const float2*>(Atm + row * kLdB + 2 * j2);
           const float2 n3 = *reinterpret_cast<const float2*>(N3m + row * kLdB + 2 * j2);
           float2 m = *nv;
-          m.x = n2.x - m.x - n3.x;
-          m.y = n2.y - m.y - n3.y;
+          m.x = n2.x + n2b.x - m.x - n3.x;
+          m.y = n2.y + n2b.y - m.y - n3.y;
           *nv = m;
         }
         __syncwarp();
