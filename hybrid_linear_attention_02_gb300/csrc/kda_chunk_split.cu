@@ -79,15 +79,17 @@ static_assert(kRecBytes == kSplitRecordBytes, "record size seen by the host");
 // ---------------------------------------------------------------- prep kernel
 constexpr int kPThreads = 256;
 constexpr uint32_t kPOffKQ = 0;        // [K';Q'] 128 x 128; raw k at 0, raw q at 16384
-constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W
-constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128; raw g before P2
-// TB: tile sums and e^{R_a} tables (P1/P2), then [T'; 0] 128 x 64, the A
-// operand of W = T' Ktil (rows 64..127 zero).
+constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W, raw g
+constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128
+// TB: [T'; 0] 128 x 64, the A operand of W = T' Ktil (rows 64..127 zero;
+// before P4 they hold the tile sums and e^{R_a} tables).
 constexpr uint32_t kPOffTB = 90112;
 constexpr uint32_t kPTiles = 106496;
 constexpr uint32_t kPSmem = kPTiles + 1024;
-constexpr uint32_t kPOffTileTot = kPOffTB;          // fp32 [4][128]
-constexpr uint32_t kPOffTabR = kPOffTB + 2048;      // fp32 [2][4][128]
+// The tables sit in the zero rows of [T'; 0], which the T' store never reads.
+constexpr uint32_t kPOffTileTot = kPOffTB + 8192;   // fp32 [4][128]
+constexpr uint32_t kPOffTabR = kPOffTB + 10240;     // fp32 [2][4][128]
+constexpr uint32_t kPOffG = kPOffKH + 24576;        // raw g of the next item (after step 4)
 constexpr int kLdA = 68;
 constexpr uint32_t kPOffA = kPOffKH;                       // A   64 x 68 fp32
 constexpr int kLdB = 20;
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const int c0 = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
-      tma_load_3d(smem + kPOffKT + hf * 8192, &tm_g, 64 * hf, x.h, c0, &s_bars[kPBarRaw]);
+      tma_load_3d(smem + kPOffG + hf * 8192, &tm_g, 64 * hf, x.h, c0, &s_bars[kPBarRaw]);
   };
   float rb[4];
   auto load_beta = [&](const Item& x) {
@@ -336,10 +338,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
     Item nxt = cur;
     if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
 
-    // The previous item's T' store has read the TB tile before P1 rewrites
-    // it (its -W store, the newest bulk group, may still be reading Khat's
-    // tile until P2).
-    if (leader) bulk_wait_read_allbut1();
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
@@ -357,7 +355,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const int r = row0 + m;
         const uint32_t off = sw128_off(r, 8 * cg, 64);
         if (r < L && ok_raw) {
-          rgt[m] = *reinterpret_cast<const uint4*>(smem + kPOffKT + off);
+          rgt[m] = *reinterpret_cast<const uint4*>(smem + kPOffG + off);
           rq[m] = *reinterpret_cast<const uint4*>(smem + kPOffKQ + 16384 + off);
           rk[m] = *reinterpret_cast<const uint4*>(smem + kPOffKQ + off);
         } else {
@@ -413,7 +411,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
       facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
       reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
     }
-    // The previous item's -W store has read Khat's tile before P2 rewrites it.
+    // The previous item's T' and -W stores have read their tiles before P2
+    // (Khat's tile) and P4 (the T' rows) rewrite them.
     if (leader) bulk_wait_read_all();
     named_bar(2, kPThreads);
     KDA_SMARK(3);
@@ -722,6 +721,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
     fence_async_smem();
     named_bar(2, kPThreads);
     KDA_SMARK(11);
+    // The inverse scratch is dead: the next item's raw g may land behind it.
+    if (loader && ok_ap && it_next < it_end) issue_raw_g(nxt);
     // T' is final: it leaves for the record now (it stays the A operand of W).
     if (leader && !s_abort) {
       bulk_store(rec + kRecT, smem + kPOffTB, 8192);
@@ -743,8 +744,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const bool ok_w = sync.wait(kPBarW, par);
     tc_fence_after();
     KDA_SMARK(12);
-    // Ktil is dead: the next item's raw g may land.
-    if (loader && ok_w && it_next < it_end) issue_raw_g(nxt);
 
     // ---- P7: -W (row = token, column = key channel) staged where Khat was;
     // its two 64-channel panels are rows 64..127 of the record's WQ panels.
