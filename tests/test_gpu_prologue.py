@@ -56,3 +56,20 @@ def test_projections_to_outputs():
                             d["beta"].cpu().double(), d["init_state"], d["cu_seqlens"])
     assert_close(out, ro, "bf16", "out")
     assert_close(fin, rf, "bf16", "final_state")
+
+
+@pytest.mark.parametrize("dk", [64, 128])
+def test_prologue_long_varlen_partial_head_block(dk):
+    """A long varlen input (sequence starts inside and between token blocks,
+    an empty sequence) with a head count that is not a multiple of the
+    heads per block."""
+    lengths = [4099, 1, 4000, 0, 97]
+    T, H = sum(lengths), 10
+    cu = inputs.cu_from_lengths(lengths).to(DEV)
+    x = inputs.make_prologue_inputs(T, H, dk, torch.bfloat16, seed=74, device=DEV)
+    q, k, g = kda.prologue(*x, cu)
+    torch.cuda.synchronize()
+    rq, rk, rg = oracle.prologue(*x, cu)
+    assert_close(q, rq, "bf16", "q")
+    assert_close(k, rk, "bf16", "k")
+    assert_close(g, rg, "bf16", "g")
