@@ -108,6 +108,9 @@ constexpr int kSStateThreads = 32 * kSStateWarps;
 constexpr int kSProducerWarp = 8;          // records and v tiles into the ring
 constexpr int kSMmaWarp = 9;               // issues every MMA
 constexpr int kSThreads = 32 * 10;
+constexpr int kSGateWarp = 10;             // gated variant: warps 10, 11 make the gate
+constexpr int kSGateWarps = 2;             // tiles w * sigmoid(z), 32 rows each
+constexpr int kSThreadsGated = 32 * (10 + kSGateWarps);
 constexpr uint32_t kSOffRec = 0;           // 2 record slots
 constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
 constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging 64 x 128 (TMA store image)
@@ -123,7 +126,8 @@ constexpr uint32_t kSColUT = 320;  // 32: bf16 U^T, A operand
 constexpr uint32_t kSColU0 = 352;  // 2 x 64 fp32: U0^T = V^T T'^T, by chunk parity
 constexpr uint32_t kSTmemCols = 512;
 enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSBarSB,
-       kSBarUT, kSBarZFull0, kSBarZFull1, kSBarZEmpty0, kSBarZEmpty1, kSNumBars };
+       kSBarUT, kSBarZFull0, kSBarZFull1, kSBarZEmpty0, kSBarZEmpty1, kSBarZReady0,
+       kSBarZReady1, kSNumBars };
 
 #ifdef KDA_PHASE_PROFILE
 // Per-phase SM-clock totals of two state-pass threads of CTA (0, 0)
@@ -795,7 +799,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 // arriving by TMA beside the records; kTrans computes segment transitions
 // (below) instead of outputs.  Each is its own instantiation.
 template <bool kGate, bool kTrans>
-__global__ void __launch_bounds__(kSThreads, 1)
+__global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     chunk_state_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o,
                        const __grid_constant__ CUtensorMap tm_z) {
@@ -839,7 +843,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (dst && dst != src) {
       float4* d4 = reinterpret_cast<float4*>(dst + soff);
       const float4* s4 = reinterpret_cast<const float4*>(src + soff);
-      for (int e = tid; e < kD * kD / 4; e += kSThreads) {
+      for (int e = tid; e < kD * kD / 4; e += static_cast<int>(blockDim.x)) {
         const int r = (4 * e) / kD, c = (4 * e) % kD;
         d4[e] = src ? s4[e]
                     : src_identity ? make_float4(r == c, r == c + 1, r == c + 2, r == c + 3)
@@ -854,9 +858,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < kSNumBars; ++b) mbar_init(&s_bars[b], 1);
+    for (int b = 0; b < kSNumBars; ++b)
+      mbar_init(&s_bars[b], b == kSBarZReady0 || b == kSBarZReady1 ? kSGateWarps : 1);
     s_abort = 0;
     fence_mbar_init();
+  }
+  if constexpr (kGate) {
+    if (tid < kD) s_gw[tid] = args.gate_w[tid];   // the RMSNorm scale
   }
   tc_fence_before();
   __syncthreads();
@@ -864,7 +872,43 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t tbase = s_tmem;
   Sync sync{s_bars, &s_abort};
 
-  if (warp == kSProducerWarp) {
+  if (warp >= kSGateWarp) {
+    // ================================ gate tiles ===============================
+    // Off the serial chain: each chunk's gate tile becomes w * sigmoid(z) in
+    // place as soon as it lands (sigmoid(x) = (1 + tanh(x / 2)) / 2; the tile
+    // is bf16, far coarser than the approximation), ready before the chunk's
+    // outputs leave.  Lane l of gate warp g takes the 8-column group l & 15
+    // of rows 32 g + (l >> 4) + 2 i.
+    if constexpr (kGate) {
+      const int cgp = lane & 15, rg = 32 * (warp - kSGateWarp) + (lane >> 4);
+      float gw8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) gw8[u] = s_gw[8 * cgp + u];
+#pragma unroll 1
+      for (int c = 0; c < nck; ++c) {
+        const int zs = c & 1;
+        if (!sync.wait(kSBarZFull0 + zs, (c >> 1) & 1)) break;
+        uint8_t* zt = smem + kSOffZ + zs * 16384;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          uint4* pz = reinterpret_cast<uint4*>(zt + sw128_off(rg + 2 * i, 8 * cgp, 64));
+          const uint4 zv = *pz;
+          uint32_t wv[4] = {zv.x, zv.y, zv.z, zv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float lo, hi;
+            f2_unpack(bf16x2_to_f2(wv[u]), lo, hi);
+            lo = gw8[2 * u] * fmaf(0.5f, tanh_fast(0.5f * lo), 0.5f);
+            hi = gw8[2 * u + 1] * fmaf(0.5f, tanh_fast(0.5f * hi), 0.5f);
+            wv[u] = pack2(lo, hi);
+          }
+          *pz = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_bars[kSBarZReady0 + zs]);
+      }
+    }
+  } else if (warp == kSProducerWarp) {
     // ================================ producer ================================
     if (lane == 0) {
       prefetch_tmap(&tm_v);
@@ -995,15 +1039,86 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // state thread calls it (it holds barriers); `live` is false once a wait
     // has failed.
     float ov[32];
-    if constexpr (kGate) {
-      if (tid < kD) s_gw[tid] = args.gate_w[tid];   // the RMSNorm scale (a barrier follows)
-    }
+    // A full chunk with the output epilogue: raw outputs to the staging tile,
+    // then 8 threads per row (16 columns each, 16-byte vectors) take the
+    // row's sum of squares with 3 shuffles and scale it in place by
+    // 1 / rms times the gate tile's w * sigmoid(z), then the TMA stores.
+    auto emit_gated_full = [&](int cl, long long c0, bool live, bool odd) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float a = ov[2 * k], b = ov[2 * k + 1];
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
+        pk[k] = odd ? pack2(other, b) : pack2(a, other);
+      }
+      // The previous TMA store has read the staging tile.
+      if (tid == 0) bulk_wait_read_all();
+      named_bar(1, kSStateThreads);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(r, j & ~1, 64)) = pk[k];
+      }
+      // The gate tile holds w * sigmoid(z) once the gate warps are done with it.
+      if (!sync.wait(kSBarZReady0 + (cl & 1), (cl >> 1) & 1)) live = false;
+      named_bar(1, kSStateThreads);
+      const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
+      const int sg = tid & 7;
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const int r = (tid >> 3) + 32 * rh;
+        uint4* po[2];
+        uint4 ov4[2], gv4[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t off = sw128_off(r, 16 * sg + 8 * e, 64);
+          po[e] = reinterpret_cast<uint4*>(smem + kSOffO + off);
+          ov4[e] = *po[e];
+          gv4[e] = *reinterpret_cast<const uint4*>(zt + off);
+        }
+        float x[16];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          unpack8(ov4[e], *reinterpret_cast<float(*)[8]>(&x[8 * e]));
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) ss = fmaf(x[u], x[u], ss);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+        const float rinv = rsqrtf(ss * (1.f / kD) + args.gate_eps);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float gz[8];
+          unpack8(gv4[e], gz);
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w4[u] = pack2(x[8 * e + 2 * u] * rinv * gz[2 * u],
+                          x[8 * e + 2 * u + 1] * rinv * gz[2 * u + 1]);
+          *po[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      fence_async_smem();
+      named_bar(1, kSStateThreads);
+      if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);   // gate tile read
+      if (tid == 0 && live && !s_abort) {
+        tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
+        tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
+        bulk_commit();
+      }
+    };
     auto emit_out = [&](int cl, bool live) {
       const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool odd = lane & 1;
       if constexpr (kGate) {
-        // Row sums of squares: a butterfly over the warp's 32 columns leaves
+        if (L == kC) {
+          emit_gated_full(cl, c0, live, odd);
+          return;
+        }
+        // (A sequence's ragged last chunk.)  Row sums of squares: a butterfly over the warp's 32 columns leaves
         // lane l with row 32 hf + l; the four warps of a column half meet in
         // shared memory.
         float a[16];
@@ -1027,8 +1142,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
           s_rinv[hf][lane] = rsqrtf(ss * (1.f / kD) + args.gate_eps);
         }
         named_bar(1, kSStateThreads);
-        // The gate tile already holds w * sigmoid(z) (made while MMA2 ran;
-        // the barriers since then make it visible).
+        // The gate tile holds w * sigmoid(z) once the gate warp is done with it.
+        if (!sync.wait(kSBarZReady0 + (cl & 1), (cl >> 1) & 1)) live = false;
         const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
 #pragma unroll
         for (int r = 0; r < 32; r += 4) {
@@ -1160,45 +1275,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #endif
       if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
       KDA_SMARK(3);
-      if constexpr (kGate) {
-        // While MMA2 runs: this chunk's gate tile becomes w * sigmoid(z) in
-        // place (each thread its own column and 32 rows; read back by the
-        // same thread when the outputs leave).
-        const int zs = c & 1;
-        const bool zok = sync.wait(kSBarZFull0 + zs, (c >> 1) & 1);
-        uint8_t* zt = smem + kSOffZ + zs * 16384;
-        // Thread t takes the 8-column group t & 15 of rows t >> 4, + 16, + 32, + 48:
-        // four 16-byte vectors, all loaded before any is stored.
-        uint4 zv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          zv[i] = *reinterpret_cast<const uint4*>(zt + sw128_off((tid >> 4) + 16 * i, 8 * (tid & 15), 64));
-        float gw8[8];
-        {
-          const float4 wa = *reinterpret_cast<const float4*>(&s_gw[8 * (tid & 15)]);
-          const float4 wb = *reinterpret_cast<const float4*>(&s_gw[8 * (tid & 15) + 4]);
-          gw8[0] = wa.x; gw8[1] = wa.y; gw8[2] = wa.z; gw8[3] = wa.w;
-          gw8[4] = wb.x; gw8[5] = wb.y; gw8[6] = wb.z; gw8[7] = wb.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t wv[4] = {zv[i].x, zv[i].y, zv[i].z, zv[i].w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float lo, hi;
-            f2_unpack(bf16x2_to_f2(wv[u]), lo, hi);
-            if (!zok) lo = hi = 0.f;
-            lo = gw8[2 * u] * fmaf(0.5f, tanh_fast(0.5f * lo), 0.5f);
-            hi = gw8[2 * u + 1] * fmaf(0.5f, tanh_fast(0.5f * hi), 0.5f);
-            wv[u] = pack2(lo, hi);
-          }
-          zv[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(zt + sw128_off((tid >> 4) + 16 * i, 8 * (tid & 15), 64)) = zv[i];
-        ok1 = ok1 && zok;
-      }
       KDA_SMARK(4);
       // (E) Outputs to registers; new state -> bf16 operand copy (the serial
       // step) and, for the next chunk, the decayed fp32 state; checkpoints;
@@ -1467,7 +1543,7 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       chunk_state_kernel<false, true><<<grid_s, kSThreads, kSSmem, s_state>>>(
           a, win, maps[2], maps[4], maps[5]);
     else if (a.gate)
-      chunk_state_kernel<true, false><<<grid_s, kSThreads, kSSmemGated, s_state>>>(
+      chunk_state_kernel<true, false><<<grid_s, kSThreadsGated, kSSmemGated, s_state>>>(
           a, win, maps[2], maps[4], maps[5]);
     else
       chunk_state_kernel<false, false><<<grid_s, kSThreads, kSSmem, s_state>>>(
