@@ -62,8 +62,10 @@ Path choose_path(const kda_dims* d, int chunk) {
   const char* env = getenv("KDA_CHUNK_PATH");
   if (env && strcmp(env, "fused") == 0) return Path::kFused;
   if (env && strcmp(env, "split") == 0) return Path::kSplit;
-  return static_cast<long long>(d->n_seqs) * d->heads <= kda::kSplitMaxPairs ? Path::kSplit
-                                                                              : Path::kFused;
+  return static_cast<long long>(d->n_seqs) * d->heads <= kda::kSplitMaxPairs ||
+                 d->n_seqs <= kda::kSplitAnyPairsSeqs
+             ? Path::kSplit
+             : Path::kFused;
 }
 
 // Split-path workspace after the order array: the carried state, then records.

@@ -1381,7 +1381,12 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
 size_t split_record_bytes(int n_seqs, long long total_tokens, int heads) {
   const long long pairs = static_cast<long long>(n_seqs) * heads;
   const long long bound = static_cast<long long>(heads) * (total_tokens / kC + n_seqs);
-  const long long budget = static_cast<long long>(kSplitRecordBudget / kRecBytes);
+  size_t cap = pairs <= kSplitOverlapPairs ? kSplitRecordBudgetOverlap : kSplitRecordBudget;
+  if (const char* v = getenv("KDA_SPLIT_RECORD_GIB")) {   // tuning knob: the cap in GiB
+    const long long g = atoll(v);
+    if (g > 0) cap = static_cast<size_t>(g) << 30;
+  }
+  const long long budget = static_cast<long long>(cap / kRecBytes);
   long long items = bound < budget ? bound : budget;
   if (items < pairs) items = pairs;
   return static_cast<size_t>(items) * kRecBytes;

@@ -87,12 +87,18 @@ cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream);
 
 // The same computation split into a parallel preparation kernel, which writes
 // one record per chunk, and a serial state kernel (for few sequence-head
-// pairs).  Records of a window of chunk indices [cw0, cw1) of every sequence;
-// the state is carried between windows in s_run.
+// pairs, or few sequences).  Records of a window of chunk indices [cw0, cw1)
+// of every sequence; the state is carried between windows in s_run.
 constexpr int kSplitMaxSeqs = 1024;              // sequences per call on this path
-constexpr long long kSplitMaxPairs = 304;        // default: sequence-head pairs up to this
+constexpr long long kSplitMaxPairs = 304;        // default: sequence-head pairs up to this,
+constexpr int kSplitAnyPairsSeqs = 32;           // or any pair count with this many sequences
 constexpr size_t kSplitRecordBytes = 66048;      // one chunk record
-constexpr size_t kSplitRecordBudget = 2ull << 30;  // record buffer cap (bytes)
+// Record buffer cap (bytes): pairs that leave half of a GB300's 152 SMs free
+// run overlapped windows, for which a small buffer is best; otherwise windows
+// run one after another and fewer of them is better.
+constexpr long long kSplitOverlapPairs = 76;
+constexpr size_t kSplitRecordBudgetOverlap = 2ull << 30;
+constexpr size_t kSplitRecordBudget = 16ull << 30;
 
 struct SplitWindow {
   uint8_t* rec;

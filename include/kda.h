@@ -102,11 +102,14 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  * Paths: bf16 with dk = dv = 128 and chunk = 64 runs on tcgen05 tensor cores
  * (requires q, k, v, g, out 16-byte aligned); every other supported case runs
  * the fp32 CUDA-core kernel that walks the recurrence.  On tensor cores, few
- * (sequence, head) pairs (N x H <= 304, N <= 1024) run the split form, given
- * a workspace of kda_chunk_fwd_workspace_size() bytes: a preparation kernel
- * over every chunk at once, which writes a 66,048-byte record per chunk into
- * the workspace (at most 2 GiB of records; longer inputs run in windows of
- * chunks with the state carried between them), then a state kernel per pair.
+ * (sequence, head) pairs (N x H <= 304) or few sequences (N <= 32) run the
+ * split form, given a workspace of kda_chunk_fwd_workspace_size() bytes: a
+ * preparation kernel over every chunk at once, which writes a 66,048-byte
+ * record per chunk into the workspace, then a state kernel per pair.  The
+ * records fill at most 2 GiB when N x H <= 76 (windows of chunks then overlap
+ * the state pass of one with the preparation of the next) and at most 16 GiB
+ * otherwise; longer inputs run in windows with the state carried between
+ * them.
  * A smaller workspace that still holds the order array, N x H fp32 states and
  * one record per pair runs the split form in more, smaller windows; below
  * that, and otherwise, one fused kernel per pair runs.  The

@@ -131,11 +131,16 @@ def test_workspace_size(lib):
     d = _dims(n=1, t=8192, h=96)
     assert algo(d) == 2
     assert size(d) == 96 * 128 * 128 * 4 + 96 * (8192 // 64 + 1) * REC
-    # Long inputs: the record buffer is capped (2 GiB), the rest runs in windows.
+    # Long inputs: the record buffer is capped (2 GiB for pairs that run
+    # overlapped windows), the rest runs in windows.
     d = _dims(n=1, t=1 << 20, h=32)
     assert size(d) == 32 * 128 * 128 * 4 + ((2 << 30) // REC) * REC
-    # Many pairs: one fused kernel per pair, order array only.
+    # Many pairs from few sequences: still split, records capped at 16 GiB.
     d = _dims(n=32, t=270000, h=96)
+    assert algo(d) == 2
+    assert size(d) == 256 + 32 * 96 * 128 * 128 * 4 + ((16 << 30) // REC) * REC
+    # Many pairs from many sequences: one fused kernel per pair, order array only.
+    d = _dims(n=64, t=270000, h=96)
     assert algo(d) == 1 and size(d) == 256
     # chunk 16 or 32 runs the CUDA-core path.
     assert algo(_dims(n=1, t=8192, h=96), 32) == 0
@@ -148,7 +153,7 @@ def test_path_override(lib, monkeypatch):
     assert lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64) == 1
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), 64) == 0
     monkeypatch.setenv("KDA_CHUNK_PATH", "split")
-    d = _dims(n=32, t=270000, h=96)
+    d = _dims(n=64, t=270000, h=96)
     assert lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64) == 2
 
 
