@@ -79,7 +79,7 @@ static_assert(kRecBytes == kSplitRecordBytes, "record size seen by the host");
 // ---------------------------------------------------------------- prep kernel
 constexpr int kPThreads = 256;
 constexpr uint32_t kPOffKQ = 0;        // [K';Q'] 128 x 128; raw k at 0, raw q at 16384
-constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then -W, raw g
+constexpr uint32_t kPOffKH = 32768;    // Khat 160 x 128; then A + inverse scratch; then raw g
 constexpr uint32_t kPOffKT = 73728;    // Ktil 64 x 128
 // TB: [T'; 0] 128 x 64, the A operand of W = T' Ktil (rows 64..127 zero;
 // before P4 they hold the tile sums and e^{R_a} tables).
@@ -415,8 +415,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
       reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
     }
-    // The previous item's T' and -W stores have read their tiles before P2
-    // (Khat's tile) and P4 (the T' rows) rewrite them.
+    // The previous item's T' store has read the T' rows before P4 rewrites them.
     if (leader) bulk_wait_read_all();
     named_bar(2, kPThreads);
     KDA_SMARK(3);
@@ -749,10 +748,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_after();
     KDA_SMARK(12);
 
-    // ---- P7: -W (row = token, column = key channel) staged where Khat was;
-    // its two 64-channel panels are rows 64..127 of the record's WQ panels.
-    // Warps 0, 1 take channels 0..63 and warps 4, 5 channels 64..127 of
-    // TMEM lanes 0..63.
+    // ---- P7: -W (row = token, column = key channel) straight to the record,
+    // where its two 64-channel panels are rows 64..127 of the WQ panels (the
+    // same swizzled image a staged copy would have).  Warps 0, 1 take
+    // channels 0..63 and warps 4, 5 channels 64..127 of TMEM lanes 0..63.
     if ((pw & 3) < 2 && ok_w) {
       const int t = 32 * (pw & 3) + lane, q0 = 2 * (pw >> 2);
       float w[2][32];
@@ -767,17 +766,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
           float f8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) f8[u] = -w[j][8 * q8 + u];
-          st_tile8(smem + kPOffKH, t, 32 * (q0 + j) + 8 * q8, 64, f8);
+          st_tile8(rec + kRecWQ, 64 + t, 32 * (q0 + j) + 8 * q8, 128, f8);
         }
     }
-    fence_async_smem();
     tc_fence_before();
-    named_bar(2, kPThreads);
-    if (leader && !s_abort) {
-      bulk_store(rec + kRecWQ + 8192, smem + kPOffKH, 8192);
-      bulk_store(rec + kRecWQ + 16384 + 8192, smem + kPOffKH + 8192, 8192);
-      bulk_commit();
-    }
     KDA_SMARK(13);
     cur = nxt;
   }

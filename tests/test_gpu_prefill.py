@@ -169,3 +169,26 @@ def test_split_overlapped_windows_match_serial(monkeypatch):
     ro, rf = _oracle(d)
     assert_close(o1, ro, "bf16", "out")
     assert_close(f1, rf, "bf16", "final_state")
+
+
+def test_split_many_pairs_few_sequences_windows():
+    """More than 304 sequence-head pairs from few sequences take the split form
+    by default; with a workspace a few records per pair larger than the
+    minimum the input runs in several windows, the state carried between
+    them."""
+    w = W["prefill_T8192_H96_d128_bf16"]
+    lengths = [700, 64, 1, 450, 0, 513, 129, 300]
+    N, H = len(lengths), 40
+    assert kda.algorithm(N, sum(lengths), H, 128, 128) == "tcgen05_split"
+    d = inputs.make_prefill(w, seed=8, device=DEV, lengths=lengths, heads=H)
+    order = (N * 4 + 255) // 256 * 256
+    ws = torch.empty(order + N * H * 128 * 128 * 4 + 3 * N * H * 66048, dtype=torch.uint8,
+                     device=DEV)
+    out, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                             d["cu_seqlens"], chunk=64, workspace=ws)
+    torch.cuda.synchronize()
+    heads = [0, 17, 39]
+    ro, rf = _oracle(d, heads)
+    hs = torch.tensor(heads, device=DEV)
+    assert_close(fin[:, hs], rf, "bf16", "final_state")
+    assert_close(out[:, hs], ro, "bf16", "out")
