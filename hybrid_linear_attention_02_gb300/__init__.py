@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "prologue", "chunk_transition", "transition_apply", "chunk_fwd_kcp", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
+__all__ = ["chunk_fwd", "decode_step", "checkpoint_offsets", "prologue", "chunk_transition", "transition_apply", "chunk_fwd_kcp", "debug_wait_timeout", "workspace_size", "algorithm", "KDAError", "lib_path", "load"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libkda.so"
@@ -86,6 +86,8 @@ def load():
             lib.kda_chunk_transition.restype = ip
             lib.kda_transition_apply.argtypes = [vp, vp, vp, vp, ll, ip, ip, vp]
             lib.kda_transition_apply.restype = ip
+            lib.kda_debug_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
+            lib.kda_debug_wait_timeout.restype = ip
             lib.kda_chunk_fwd_kcp_workspace_size.argtypes = [dp, ip]
             lib.kda_chunk_fwd_kcp_workspace_size.restype = sz
             lib.kda_chunk_fwd_kcp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
@@ -317,6 +319,17 @@ def chunk_transition(q, k, v, g, beta, cu_seqlens=None, *, n_seqs: int | None = 
     if rc != 0:
         raise KDAError(rc, "kda_chunk_transition")
     return M, Hs
+
+
+def debug_wait_timeout(dev_status, timeout_us: int, *, stream=None):
+    """``kda_debug_wait_timeout``: a kernel whose bounded wait cannot succeed
+    stores KDA_ERR_TIMEOUT (-4) into the device int ``dev_status`` after
+    ``timeout_us`` microseconds and returns (failure-detection self-test)."""
+    lib = load()
+    with torch.cuda.device(dev_status.device):
+        rc = lib.kda_debug_wait_timeout(_ptr(dev_status), int(timeout_us), _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_debug_wait_timeout")
 
 
 def transition_apply(M, H, S, *, out=None, stream=None):

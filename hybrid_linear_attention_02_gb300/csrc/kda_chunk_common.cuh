@@ -53,6 +53,11 @@ struct Sync {
   uint64_t* bars;
   volatile int* abort;
   __device__ __forceinline__ bool wait(int b, uint32_t parity) {
+    return wait_for(b, parity, 2000000000ull);
+  }
+  // As wait, giving up after limit_ns of wall time (a compile-time constant
+  // in the kernels, so it costs them no register).
+  __device__ __forceinline__ bool wait_for(int b, uint32_t parity, uint64_t limit_ns) {
     if (*abort) return false;
     if (mbar_try_wait(&bars[b], parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -60,7 +65,7 @@ struct Sync {
       // Suspended until the phase completes (or 20 us pass), not spinning.
       if (mbar_try_wait_sleep(&bars[b], parity, 20000u)) return true;
       if (*abort) return false;
-      if (global_timer_ns() - t0 > 2000000000ull) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

@@ -311,6 +311,18 @@ KDA_API int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk);
 /* Static description of a status code (never NULL). */
 KDA_API const char* kda_status_string(int status);
 
+/*
+ * Failure-detection self-test (diagnostic).  Launches one small kernel that
+ * runs the library's bounded mbarrier wait on a barrier nothing ever arrives
+ * at, with a limit of `timeout_us` microseconds (1 .. 10,000,000) instead of
+ * the kernels' 2 s; when the limit passes, the kernel stores KDA_ERR_TIMEOUT
+ * into *dev_status (device int, caller-owned, required) and returns, leaving
+ * the context usable.  Asynchronous on `stream`; returns KDA_ERR_INVALID for
+ * a NULL dev_status or an out-of-range limit, KDA_ERR_CUDA if the launch
+ * fails, KDA_OK otherwise.
+ */
+KDA_API int kda_debug_wait_timeout(int* dev_status, unsigned timeout_us, void* stream);
+
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 KDA_API int kda_version(void);
 

@@ -36,6 +36,12 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, s), f"{s} declared in include/ but not exported"
 
 
+def test_wait_timeout_self_test_rejects_bad_arguments(lib):
+    # (no launch happens: the arguments are refused on the host)
+    assert lib.kda_debug_wait_timeout(None, 1000, None) == -1
+    assert lib.kda_debug_wait_timeout(ctypes.c_void_p(16), 0, None) == -1
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.kda_status_string(code)
