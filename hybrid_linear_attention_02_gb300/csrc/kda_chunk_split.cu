@@ -438,9 +438,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
         *reinterpret_cast<uint4*>(base + sw128_off(row, 8 * cg, rows)) =
             make_uint4(v[0], v[1], v[2], v[3]);
       };
-      uint64_t kh[4][4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
+        uint64_t kh[4];
         const int r = row0 + m, rl = 4 * r4 + m;
         const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
         const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
@@ -456,9 +456,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
           oqp[w] = f2_to_bf16x2(q1);
           okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
           oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
-          kh[m][w] = f2_mul(kp, ei);
-          okh[w] = f2_to_bf16x2(kh[m][w]);
-          okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
+          kh[w] = f2_mul(kp, ei);
+          okh[w] = f2_to_bf16x2(kh[w]);
+          okb[w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
         }
         st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
         st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
@@ -466,20 +466,17 @@ __global__ void __launch_bounds__(kPThreads, 2)
         st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
         st4(rec + kRecWQ, r, 128, oqt);
         st4(rec + kRecKB, r, 64, okb);
-      }
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        const int a2 = ta + 1 + i;
-        if (a2 < 4) {
-          const int frow = ta == 0 ? a2 - 1 : ta == 1 ? a2 + 1 : 5;
-          uint64_t f[4];
-          ld8(facs + frow * kD, f);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
+        for (int i = 0; i < 3; ++i) {
+          const int a2 = ta + 1 + i;
+          if (a2 < 4) {
+            const int frow = ta == 0 ? a2 - 1 : ta == 1 ? a2 + 1 : 5;
+            uint64_t f[4];
+            ld8(facs + frow * kD, f);
             uint32_t ox[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[m][w], f[w]));
-            st4(smem + kPOffKH, khat_row0(a2) + row0 + m, 160, ox);
+            for (int w = 0; w < 4; ++w) ox[w] = f2_to_bf16x2(f2_mul(kh[w], f[w]));
+            st4(smem + kPOffKH, khat_row0(a2) + r, 160, ox);
           }
         }
       }
