@@ -24,6 +24,27 @@ using namespace sm100;
 
 __device__ __forceinline__ int khat_row0(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
 
+// fp32 -> tf32 (round to nearest, ties away), as the m16n8k8 MMA reads it.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// One warp: D (16 x 8, fp32) += A (16 x 8, tf32, row) * B (8 x 8, tf32, col),
+// in the m16n8k8 fragment layouts (group g = lane / 4, t = lane % 4): a0..a3
+// = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b0, b1 = B[t][g], B[t+4][g];
+// d0..d3 = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ void mma_m16n8k8_tf32(float& d0, float& d1, float& d2, float& d3,
+                                                 uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }

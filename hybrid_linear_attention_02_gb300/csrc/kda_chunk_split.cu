@@ -599,32 +599,29 @@ __global__ void __launch_bounds__(kPThreads, 2)
     // rows 4 i4 .. + 3 and columns 2 j2, 2 j2 + 1 of the output block.
     //   acc[i][jj] += X[4 i4 + i][k] Y[k][2 j2 + jj],  k = 0..15.
     const int i4 = lane >> 3, j2 = lane & 7;
+    // Tensor-core form: acc[i] holds row mg + 8 (i & 1), columns
+    // 8 (i >> 1) + 2 mt, + 1 of the block (the m16n8k8 accumulator layout).
+    const int mg = lane >> 2, mt = lane & 3;
     auto prod16 = [&](const float* X, int xs, const float* Y, int ys, float (&acc)[4][2]) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {   // k = 4 q .. 4 q + 3
-        float4 xv[4];
-        float2 yv[4];
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t a0 = tf32_rna(X[mg * xs + 8 * ks + mt]);
+        const uint32_t a1 = tf32_rna(X[(mg + 8) * xs + 8 * ks + mt]);
+        const uint32_t a2 = tf32_rna(X[mg * xs + 8 * ks + mt + 4]);
+        const uint32_t a3 = tf32_rna(X[(mg + 8) * xs + 8 * ks + mt + 4]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          xv[i] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          yv[kk] = *reinterpret_cast<const float2*>(Y + (4 * q + kk) * ys + 2 * j2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float xk[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            acc[i][0] = fmaf(xk[kk], yv[kk].x, acc[i][0]);
-            acc[i][1] = fmaf(xk[kk], yv[kk].y, acc[i][1]);
-          }
+        for (int nh = 0; nh < 2; ++nh) {
+          const uint32_t b0 = tf32_rna(Y[(8 * ks + mt) * ys + 8 * nh + mg]);
+          const uint32_t b1 = tf32_rna(Y[(8 * ks + mt + 4) * ys + 8 * nh + mg]);
+          mma_m16n8k8_tf32(acc[2 * nh][0], acc[2 * nh][1], acc[2 * nh + 1][0], acc[2 * nh + 1][1],
+                           a0, a1, a2, a3, b0, b1);
         }
       }
     };
     auto store_blk = [&](float* Z, const float (&acc)[4][2]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float2*>(Z + (4 * i4 + i) * kLdB + 2 * j2) =
+        *reinterpret_cast<float2*>(Z + (mg + 8 * (i & 1)) * kLdB + 8 * (i >> 1) + 2 * mt) =
             make_float2(acc[i][0], acc[i][1]);
     };
     // Off-diagonal block pairs (a, b), a > b: (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5.
@@ -711,12 +708,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
       float acc[4][2] = {};
       prod16(Nm + pw * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, acc);
       const float sg = pw == 5 ? -1.f : 1.f;
-      const float2 bv = *reinterpret_cast<const float2*>(&s_beta[16 * b + 2 * j2]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint32_t*>(smem + kPOffTB +
-                                     sw128_off(16 * a + 4 * i4 + i, 16 * b + 2 * j2, 64)) =
+      for (int i = 0; i < 4; ++i) {
+        const int row = mg + 8 * (i & 1), col = 8 * (i >> 1) + 2 * mt;
+        const float2 bv = *reinterpret_cast<const float2*>(&s_beta[16 * b + col]);
+        *reinterpret_cast<uint32_t*>(smem + kPOffTB + sw128_off(16 * a + row, 16 * b + col, 64)) =
             pack2(sg * acc[i][0] * bv.x, sg * acc[i][1] * bv.y);
+      }
     }
     fence_async_smem();
     named_bar(2, kPThreads);
