@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // N = D (strictly block-lower part of A), T = (I - N + N^2 - N^3) D.
       // Off-diagonal block pairs (a, b), a > b, are numbered
       // (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5.  Block products are
-      // 16 x 16 x 16, one 4 x 4 output tile per thread.
+      // 16 x 16 x 16, one warp each.
       if (p < 64) {
         // D_bb by forward substitution, one column per thread; the block's
         // rows are loaded first so the substitution runs from registers.
@@ -692,79 +692,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar(2, kPrepThreads);
       KDA_MARK(16);
-      // acc[i][j] += X[4 i4 + i][k] Y[k][4 j4 + j], k = 0..15, X rows xstride
-      // apart, Y rows ystride apart (Y rows 16-byte aligned).
-      // acc[i][j] += X[4 i4 + i][k] Y[k][4 j4 + j], k = 0..15; both operands are
-      // loaded (16-byte rows) before the FMAs.
-      auto tile16 = [&](const float* X, int xs, const float* Y, int ys, int i4, int j4,
-                        float (&acc)[4][4]) {
-        float4 yv[16], xv[4][4];
+      // Block products, one warp per 16 x 16 x 16 product on warp-level tf32
+      // tensor-core MMAs (m16n8k8, fp32 accumulate): acc[i] holds row
+      // mg + 8 (i & 1), columns 8 (i >> 1) + 2 mt, + 1 of the output block.
+      const int mg = (p & 31) >> 2, mt = p & 3;
+      auto prod16 = [&](const float* X, int xs, const float* Y, int ys, float (&acc)[4][2]) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) yv[k] = *reinterpret_cast<const float4*>(Y + k * ys + 4 * j4);
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint32_t a0 = tf32_rna(X[mg * xs + 8 * ks + mt]);
+          const uint32_t a1 = tf32_rna(X[(mg + 8) * xs + 8 * ks + mt]);
+          const uint32_t a2 = tf32_rna(X[mg * xs + 8 * ks + mt + 4]);
+          const uint32_t a3 = tf32_rna(X[(mg + 8) * xs + 8 * ks + mt + 4]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            xv[i][q] = *reinterpret_cast<const float4*>(X + (4 * i4 + i) * xs + 4 * q);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 xq = xv[i][k >> 2];
-            const float xk = (k & 3) == 0 ? xq.x : (k & 3) == 1 ? xq.y : (k & 3) == 2 ? xq.z : xq.w;
-            acc[i][0] = fmaf(xk, yv[k].x, acc[i][0]);
-            acc[i][1] = fmaf(xk, yv[k].y, acc[i][1]);
-            acc[i][2] = fmaf(xk, yv[k].z, acc[i][2]);
-            acc[i][3] = fmaf(xk, yv[k].w, acc[i][3]);
+          for (int nh = 0; nh < 2; ++nh) {
+            const uint32_t b0 = tf32_rna(Y[(8 * ks + mt) * ys + 8 * nh + mg]);
+            const uint32_t b1 = tf32_rna(Y[(8 * ks + mt + 4) * ys + 8 * nh + mg]);
+            mma_m16n8k8_tf32(acc[2 * nh][0], acc[2 * nh][1], acc[2 * nh + 1][0],
+                             acc[2 * nh + 1][1], a0, a1, a2, a3, b0, b1);
           }
         }
       };
-      auto store_tile = [&](float* Z, int i4, int j4, const float (&acc)[4][4]) {
+      auto store_blk = [&](float* Z, const float (&acc)[4][2]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(Z + (4 * i4 + i) * kLdB + 4 * j4) =
-              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+          *reinterpret_cast<float2*>(Z + (mg + 8 * (i & 1)) * kLdB + 8 * (i >> 1) + 2 * mt) =
+              make_float2(acc[i][0], acc[i][1]);
       };
-      const int tq = p & 15, i4 = tq >> 2, j4 = tq & 3;
-      // Step 1: N_ab = D_aa A_ab (96 threads); diagonal blocks of T' (128 threads).
-      if (p < 96) {
-        const int blk = p >> 4;
+      // Step 1: N_ab = D_aa A_ab (warps 0..5); diagonal blocks of T' (warps 6, 7).
+      if (pw < 6) {
+        const int blk = pw;
         const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
         const int b = blk - (a * (a - 1)) / 2;
-        float acc[4][4] = {};
-        tile16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, i4, j4, acc);
-        store_tile(Nm + blk * 16 * kLdB, i4, j4, acc);
-      } else if (p >= 128) {
-        const int e = p - 128, a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
-        float f8[8];
+        float acc[4][2] = {};
+        prod16(Dm + a * 16 * kLdB, kLdB, Am + 16 * a * kLdA + 16 * b, kLdA, acc);
+        store_blk(Nm + blk * 16 * kLdB, acc);
+      } else {
+        for (int e = p - 192; e < 128; e += 64) {
+          const int a = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+          float f8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int cc = 8 * h8 + u;
-          f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
+          for (int u = 0; u < 8; ++u) {
+            const int cc = 8 * h8 + u;
+            f8[u] = Dm[(a * 16 + rr) * kLdB + cc] * s_beta[16 * a + cc];
+          }
+          st_tile8(smem + kOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
         }
-        st_tile8(smem + kOffTB, 16 * a + rr, 16 * a + 8 * h8, 64, f8);
       }
       named_bar(2, kPrepThreads);
       KDA_MARK(17);
       // Step 2: N^2 blocks (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20.
-      if (p < 48) {
-        const int k2 = p >> 4;
-        float acc[4][4] = {};
+      if (pw < 3) {
+        const int k2 = pw;
+        float acc[4][2] = {};
         const int xa = k2 == 0 ? 2 : k2 == 1 ? 5 : 4, ya = k2 == 0 ? 0 : k2 == 1 ? 2 : 0;
-        tile16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, i4, j4, acc);
-        if (k2 == 2) tile16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, i4, j4, acc);
-        store_tile(N2m + k2 * 16 * kLdB, i4, j4, acc);
+        prod16(Nm + xa * 16 * kLdB, kLdB, Nm + ya * 16 * kLdB, kLdB, acc);
+        if (k2 == 2) prod16(Nm + 5 * 16 * kLdB, kLdB, Nm + 1 * 16 * kLdB, kLdB, acc);
+        store_blk(N2m + k2 * 16 * kLdB, acc);
       }
       named_bar(2, kPrepThreads);
       KDA_MARK(18);
-      // Step 3: N^3 block (3,0) = N32 (N^2)_20 (16 threads), and M = -N + N^2
-      // in place of N for blocks (1,0) (2,0) (2,1) (3,1); N32, which the N^3
-      // threads read, is negated in step 4 and M_30 is finished there too.
-      if (p < 16) {
-        float acc[4][4] = {};
-        tile16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, i4, j4, acc);
-        store_tile(N3m, i4, j4, acc);
-      } else if (p >= 32) {
+      // Step 3: N^3 block (3,0) = N32 (N^2)_20 (warp 0), and M = -N + N^2 in
+      // place of N for blocks (1,0) (2,0) (2,1) (3,1) (warps 1..7); N32, which
+      // warp 0 reads, is negated in step 4 and M_30 is finished there too.
+      if (pw == 0) {
+        float acc[4][2] = {};
+        prod16(Nm + 5 * 16 * kLdB, kLdB, N2m, kLdB, acc);
+        store_blk(N3m, acc);
+      } else {
         for (int e = p - 32; e < 4 * 64; e += kPrepThreads - 32) {
           const int bsel = e >> 6;                          // blocks 0, 1, 2, 4
           const int blk = bsel < 3 ? bsel : 4;
@@ -782,40 +776,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar(2, kPrepThreads);
       KDA_MARK(19);
-      // Step 4: T_ab = M_ab D_bb, times beta, into T' (M_30 = -N30 + N^2_30 - N^3_30).
-      if (p < 96) {
-        const int blk = p >> 4;
+      // Step 4: T_ab = M_ab D_bb, times beta, into T' (warps 0..5; M_30 =
+      // -N30 + N^2_30 - N^3_30 first, M_32 = -N_32).
+      if (pw < 6) {
+        const int blk = pw;
         const int a = blk < 1 ? 1 : blk < 3 ? 2 : 3;
         const int b = blk - (a * (a - 1)) / 2;
         if (blk == 3) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int row = 4 * i4 + i;
-            float4* nv = reinterpret_cast<float4*>(Nm + (3 * 16 + row) * kLdB + 4 * j4);
-            const float4 n2 = *reinterpret_cast<const float4*>(N2m + (2 * 16 + row) * kLdB + 4 * j4);
-            const float4 n3 = *reinterpret_cast<const float4*>(N3m + row * kLdB + 4 * j4);
-            float4 m = *nv;
-            m.x = n2.x - m.x - n3.x; m.y = n2.y - m.y - n3.y;
-            m.z = n2.z - m.z - n3.z; m.w = n2.w - m.w - n3.w;
+            const int row = mg + 8 * (i & 1), col = 8 * (i >> 1) + 2 * mt;
+            float2* nv = reinterpret_cast<float2*>(Nm + (3 * 16 + row) * kLdB + col);
+            const float2 n2 = *reinterpret_cast<const float2*>(N2m + (2 * 16 + row) * kLdB + col);
+            const float2 n3 = *reinterpret_cast<const float2*>(N3m + row * kLdB + col);
+            float2 m = *nv;
+            m.x = n2.x - m.x - n3.x;
+            m.y = n2.y - m.y - n3.y;
             *nv = m;
           }
-          __syncwarp(0x0000FFFFu << (16 * (lane >> 4)));
+          __syncwarp();
         }
-        float acc[4][4] = {};
-        tile16(Nm + blk * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, i4, j4, acc);
-        if (blk == 5) {   // M_32 = -N_32
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jq = 0; jq < 4; ++jq) acc[i][jq] = -acc[i][jq];
-        }
-        const float4 bv = *reinterpret_cast<const float4*>(&s_beta[16 * b + 4 * j4]);
+        float acc[4][2] = {};
+        prod16(Nm + blk * 16 * kLdB, kLdB, Dm + b * 16 * kLdB, kLdB, acc);
+        const float sg = blk == 5 ? -1.f : 1.f;   // M_32 = -N_32
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint2 pk = make_uint2(pack2(acc[i][0] * bv.x, acc[i][1] * bv.y),
-                                      pack2(acc[i][2] * bv.z, acc[i][3] * bv.w));
-          *reinterpret_cast<uint2*>(smem + kOffTB +
-                                    sw128_off(16 * a + 4 * i4 + i, 16 * b + 4 * j4, 64)) = pk;
+          const int row = mg + 8 * (i & 1), col = 8 * (i >> 1) + 2 * mt;
+          const float2 bv = *reinterpret_cast<const float2*>(&s_beta[16 * b + col]);
+          *reinterpret_cast<uint32_t*>(smem + kOffTB + sw128_off(16 * a + row, 16 * b + col, 64)) =
+              pack2(sg * acc[i][0] * bv.x, sg * acc[i][1] * bv.y);
         }
       }
       fence_async_smem();
