@@ -95,7 +95,8 @@ constexpr uint32_t kOffD = kOffA + 64 * kLdA * 4;        // D     4 x 16 x 20
 constexpr uint32_t kOffN = kOffD + 4 * 16 * kLdB * 4;    // N     6 x 16 x 20
 constexpr uint32_t kOffN2 = kOffN + 6 * 16 * kLdB * 4;   // N^2   3 x 16 x 20
 constexpr uint32_t kOffN3 = kOffN2 + 3 * 16 * kLdB * 4;  // N^3   16 x 20
-static_assert(kOffN3 + 16 * kLdB * 4 <= kOffKH + 40960, "inverse scratch fits");
+constexpr uint32_t kOffAt = kOffN3 + 16 * kLdB * 4;      // A_aa^T 4 x 16 x 20
+static_assert(kOffAt + 4 * 16 * kLdB * 4 <= kOffKH + 40960, "inverse scratch fits");
 
 // TMEM columns (512 allocated).
 constexpr uint32_t kColAP = 0;     // 160 fp32: AP;  W^T reuses columns 0..63
@@ -365,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* Nm = reinterpret_cast<float*>(smem + kOffN);      // [6][16][kLdB]  T_aa A_ab
     float* N2m = reinterpret_cast<float*>(smem + kOffN2);    // [3][16][kLdB]
     float* N3m = reinterpret_cast<float*>(smem + kOffN3);    // [16][kLdB]
+    float* Atm = reinterpret_cast<float*>(smem + kOffAt);    // [4][16][kLdB]  A_aa^T
     float* tile_tot = reinterpret_cast<float*>(smem + kOffTileTot);  // [4][128]
     float* tabR = reinterpret_cast<float*>(smem + kOffTabR);  // e^{R_a}, e^{G_C - R_a}: [2][4][128]
 
@@ -602,6 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- P4: A (x beta, strictly lower; fp32) and P (lower inclusive; bf16).
+      // A's blocks above the diagonal are never read and are not written; its
+      // diagonal blocks go out transposed, and the warp that holds one also
+      // inverts it (P5's diagonal blocks).  Warps 4..7 zero the blocks of T'
+      // above the diagonal meanwhile (the factor tables there are dead).
       if (pw < 4 && ok_ap) {
         // TMEM lane quarter pw holds rows [K'_pw; Q'_pw].
         const int a = pw, rl = lane & 15, r = 16 * a + rl;
@@ -633,12 +639,51 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
               st_tile8(ptile, r, 16 * blk + 8 * h8, 64, f8);
             }
-          } else {
+          } else if (blk == a) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) Atm[(16 * a + u) * kLdB + rl] = v[u];
+          } else if (blk < a) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
               *reinterpret_cast<float4*>(&Am[r * kLdA + 16 * blk + 4 * q4]) =
                   make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
           }
+        }
+        // D_aa = (I + A_aa)^-1, column jj = lane by right-looking substitution:
+        // once x_i is final it is taken off every later row, so the dependent
+        // chain is one FMA per row.  Column i of A_aa is row i of its
+        // transposed copy (the 16 lanes read the same words).
+        __syncwarp();
+        if (lane < 16) {
+          const int jj = lane;
+          const float* At = Atm + 16 * a * kLdB;
+          float y[16];
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) y[rr] = rr == jj ? 1.f : 0.f;
+#pragma unroll
+          for (int i = 0; i < 15; ++i) {
+            const float xi = y[i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (4 * q + 3 > i) {
+                const float4 w4 = *reinterpret_cast<const float4*>(At + i * kLdB + 4 * q);
+                const float a4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (4 * q + u > i) y[4 * q + u] = fmaf(-a4[u], xi, y[4 * q + u]);
+              }
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) Dm[(a * 16 + rr) * kLdB + jj] = y[rr];
+        }
+      } else if (pw >= 4) {
+        for (int e = p - 128; e < 192; e += kPrepThreads - 128) {
+          const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+          const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
+          const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
+          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          st_tile8(smem + kOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
         }
       }
       tc_fence_before();
@@ -649,48 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // With D = blockdiag of the inverted 16 x 16 diagonal blocks and
       // N = D (strictly block-lower part of A), T = (I - N + N^2 - N^3) D.
       // Off-diagonal block pairs (a, b), a > b, are numbered
-      // (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5.  Block products are
-      // 16 x 16 x 16, one warp each.
-      if (p < 64) {
-        // D_bb by forward substitution, one column per thread; the block's
-        // rows are loaded first so the substitution runs from registers.
-        const int blk = p >> 4, jj = p & 15;
-        const float* Ab = Am + 16 * blk * kLdA + 16 * blk;
-        float ar[16][16];
-#pragma unroll
-        for (int rr = 1; rr < 16; ++rr)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (4 * q < rr) {
-              const float4 v = *reinterpret_cast<const float4*>(Ab + rr * kLdA + 4 * q);
-              ar[rr][4 * q] = v.x; ar[rr][4 * q + 1] = v.y;
-              ar[rr][4 * q + 2] = v.z; ar[rr][4 * q + 3] = v.w;
-            }
-          }
-        float x[16];
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int i = 0; i < rr; ++i) {
-            if (i & 1) acc1 = fmaf(ar[rr][i], x[i], acc1);
-            else acc0 = fmaf(ar[rr][i], x[i], acc0);
-          }
-          x[rr] = rr == jj ? 1.f : (rr < jj ? 0.f : -(acc0 + acc1));
-        }
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Dm[(blk * 16 + rr) * kLdB + jj] = x[rr];
-      } else {
-        // Zero the blocks of T' strictly above the diagonal (192 vectors).
-        for (int e = p - 64; e < 192; e += kPrepThreads - 64) {
-          const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
-          const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
-          const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
-          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          st_tile8(smem + kOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
-        }
-      }
-      named_bar(2, kPrepThreads);
+      // (1,0)=0 (2,0)=1 (2,1)=2 (3,0)=3 (3,1)=4 (3,2)=5; D is done (P4).  Block
+      // products are 16 x 16 x 16, one warp each.
       KDA_MARK(16);
       // Block products, one warp per 16 x 16 x 16 product on warp-level tf32
       // tensor-core MMAs (m16n8k8, fp32 accumulate): acc[i] holds row
