@@ -1024,13 +1024,17 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     // store per 64-column half; a sequence's ragged last chunk is written
     // row by row (the tile's tail rows belong to the next sequence).  Every
     // state thread calls it (it holds barriers); `live` is false once a wait
-    // has failed.
+    // has failed.  With `defer`, a gated full chunk is only staged and the
+    // call returns true: its epilogue pass (gated_finish) is still to run.
     float ov[32];
-    // A full chunk with the output epilogue: raw outputs to the staging tile,
-    // then 8 threads per row (16 columns each, 16-byte vectors) take the
-    // row's sum of squares with 3 shuffles and scale it in place by
-    // 1 / rms times the gate tile's w * sigmoid(z), then the TMA stores.
-    auto emit_gated_full = [&](int cl, long long c0, bool live, bool odd) {
+    // A full chunk with the output epilogue, in two parts.  Part one: the raw
+    // outputs (bf16) to the staging tile, while MMA1 of the next chunk runs.
+    // Part two, during the next chunk's MMA2 (the U^T hand-off's barrier has
+    // made every thread's staged rows visible by then): 8 threads per row
+    // (16 columns each, 16-byte vectors) take the row's sum of squares with 3
+    // shuffles and scale it in place by 1 / rms times the gate tile's
+    // w * sigmoid(z), then the TMA stores.
+    auto gated_stage = [&](bool odd) {
       uint32_t pk[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
@@ -1046,9 +1050,12 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
         *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(r, j & ~1, 64)) = pk[k];
       }
+    };
+    // Part two (after a barrier since part one).
+    auto gated_finish = [&](int cl, bool live) {
+      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
       // The gate tile holds w * sigmoid(z) once the gate warps are done with it.
       if (!sync.wait(kSBarZReady0 + (cl & 1), (cl >> 1) & 1)) live = false;
-      named_bar(1, kSStateThreads);
       const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
       const int sg = tid & 7;
 #pragma unroll
@@ -1096,14 +1103,17 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         bulk_commit();
       }
     };
-    auto emit_out = [&](int cl, bool live) {
+    auto emit_out = [&](int cl, bool live, bool defer) -> bool {
       const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
       const bool odd = lane & 1;
       if constexpr (kGate) {
         if (L == kC) {
-          emit_gated_full(cl, c0, live, odd);
-          return;
+          gated_stage(odd);
+          if (defer) return true;
+          named_bar(1, kSStateThreads);
+          gated_finish(cl, live);
+          return false;
         }
         // (A sequence's ragged last chunk.)  Row sums of squares: a butterfly over the warp's 32 columns leaves
         // lane l with row 32 hf + l; the four warps of a column half meet in
@@ -1161,7 +1171,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
           named_bar(1, kSStateThreads);   // every gate-tile read is done
           if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);
         }
-        return;
+        return false;
       }
       // The previous TMA store has read the staging tile.
       if (tid == 0) bulk_wait_read_all();
@@ -1181,6 +1191,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
         bulk_commit();
       }
+      return false;
     };
 
     // The fp32 state carries the first chunk's decay Diag(e^{G_C}) before
@@ -1215,6 +1226,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
 #endif
     if (tid == 0) mbar_arrive(&s_bars[kSBarSB]);
     bool prev_ok = false;
+    bool pend = false;   // gated: chunk c - 1 staged, its epilogue pass still to run
 #ifdef KDA_PHASE_PROFILE
     unsigned long long hand[4] = {};   // SB->MMA1 issue, MMA1 exec, UT->MMA2 issue, MMA2 exec
 #endif
@@ -1226,7 +1238,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
       // (B) While MMA1 runs: the previous chunk's outputs.
-      if (c > 0 && tmode == 0) emit_out(c - 1, prev_ok);
+      if (c > 0 && tmode == 0) pend = emit_out(c - 1, prev_ok, true);
       KDA_SMARK(0);
       // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
       bool ok1 = ok && sync.wait(kSBarMMA1, c & 1);
@@ -1261,6 +1273,12 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       if (tid == 0) s_ts[3] = clock64();
 #endif
       if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
+      // While MMA2 runs: the staged chunk's epilogue (the barrier above made
+      // its rows visible).
+      if constexpr (kGate) {
+        if (pend) gated_finish(c - 1, prev_ok);
+        pend = false;
+      }
       KDA_SMARK(3);
       KDA_SMARK(4);
       // (E) Outputs to registers; new state -> bf16 operand copy (the serial
@@ -1341,7 +1359,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       }
     }
 #endif
-    if (tmode == 0) emit_out(nck - 1, prev_ok);
+    if (tmode == 0) emit_out(nck - 1, prev_ok, false);
     if (tid == 0) bulk_wait_all();
     if (!s_abort && dst) {
       // After the last chunk the fp32 state carries no further decay.
