@@ -422,7 +422,8 @@ def run_gpu(args):
     prologue = {"value": job_throughput(world, T, p_ms) / 1e6, "unit": "Mtok/s",
                 "ms_per_step": p_ms, "steps": ck_steps, "algorithmic_bytes_per_launch": p_bytes,
                 "achieved_gbs": p_bytes / (p_ms * 1e-3) / 1e9,
-                "frac": p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, "bound": "hbm"}
+                "frac": p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, "bound": "hbm",
+                "traffic": kernel_traffic("kda_prologue.cu", "prologue_T8192_H96.md")}
     del d, args_pf, out, fin, px, pq, pk, pg
     torch.cuda.empty_cache()
     decode = None
