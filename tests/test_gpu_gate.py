@@ -78,3 +78,28 @@ def test_gated_decode_chain():
         assert_close(state, ref_state, "bf16", f"decode state step {step}")
         assert torch.equal(state, plain_state)
         _epilogue_only(out, o0, gate, "bf16")
+
+
+def test_gated_split_windows():
+    """The split form's gated state pass across several windows (a workspace
+    three records per pair above the minimum), overlapped with the next
+    window's preparation: inside a window a full chunk's epilogue runs during
+    the next chunk's MMA2, and every window's last chunk finishes in place."""
+    lengths = [700, 64, 1, 450, 0, 513, 129, 300]
+    N, H = len(lengths), 3
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=34, device=DEV,
+                            lengths=lengths, heads=H)
+    assert kda.algorithm(N, sum(lengths), H, 128, 128) == "tcgen05_split"
+    order = (N * 4 + 255) // 256 * 256
+    ws = torch.empty(order + N * H * 128 * 128 * 4 + 3 * N * H * 66048, dtype=torch.uint8,
+                     device=DEV)
+    gate = inputs.make_output_gate(sum(lengths), H, 128, d["v"].dtype, seed=4, device=DEV)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    o0, _ = kda.chunk_fwd(*x, d["init_state"], d["cu_seqlens"], chunk=64, workspace=ws)
+    out, fin = kda.chunk_fwd(*x, d["init_state"], d["cu_seqlens"], chunk=64, workspace=ws,
+                             gate=gate)
+    torch.cuda.synchronize()
+    ro, rf = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
+    assert_close_gated(out, ro, gate, "bf16", "gated out")
+    assert_close(fin, rf, "bf16", "final_state")
+    _epilogue_only(out, o0, gate, "bf16")
