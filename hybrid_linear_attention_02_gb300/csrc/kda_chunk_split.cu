@@ -595,12 +595,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
     // ---- P5: T = (I + A)^-1 = (I - N + N^2 - N^3) D in fp32 with N = D A
     // (strictly block-lower, N^4 = 0), written as T' = T diag(beta) in bf16.
     KDA_SMARK(7);
-    // Block products, one warp per 16 x 16 x 16 product: lane (i4, j2) owns
-    // rows 4 i4 .. + 3 and columns 2 j2, 2 j2 + 1 of the output block.
-    //   acc[i][jj] += X[4 i4 + i][k] Y[k][2 j2 + jj],  k = 0..15.
+    // Block products, one warp per 16 x 16 x 16 product on warp-level tf32
+    // tensor-core MMAs (m16n8k8, fp32 accumulate): acc[i] holds row
+    // mg + 8 (i & 1), columns 8 (i >> 1) + 2 mt, + 1 of the output block.
+    // Elementwise block work (step 4's M_30) has lane (i4, j2) take rows
+    // 4 i4 .. + 3 and columns 2 j2, 2 j2 + 1.
     const int i4 = lane >> 3, j2 = lane & 7;
-    // Tensor-core form: acc[i] holds row mg + 8 (i & 1), columns
-    // 8 (i >> 1) + 2 mt, + 1 of the block (the m16n8k8 accumulator layout).
     const int mg = lane >> 2, mt = lane & 3;
     auto prod16 = [&](const float* X, int xs, const float* Y, int ys, float (&acc)[4][2]) {
 #pragma unroll
