@@ -193,7 +193,7 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   a.gate_eps = x.gate_eps;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (need > 0 && cu_seqlens) {
+  if (need > 0 && cu_seqlens && N > 1) {   // one sequence: no order needed
     int* order = static_cast<int*>(workspace);
     if (kda::launch_length_order(cu_seqlens, N, order, s) != cudaSuccess) return KDA_ERR_CUDA;
     a.order = order;
@@ -309,7 +309,7 @@ int kda_chunk_transition(const void* q, const void* k, const void* v, const void
   a.trans_H = trans_H;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (need > 0 && cu_seqlens) {
+  if (need > 0 && cu_seqlens && N > 1) {   // one sequence: no order needed
     if (kda::launch_length_order(cu_seqlens, N, reinterpret_cast<int*>(ws), s) != cudaSuccess)
       return KDA_ERR_CUDA;
     a.order = reinterpret_cast<int*>(ws);

@@ -5,9 +5,12 @@
 // ShortConv is a depthwise causal convolution of 4 taps along each sequence
 // (tap 3 on the current token, zero before the sequence's first token);
 // L2norm(y) = y / sqrt(sum(y^2) + 1e-6) over the dk channels of a head.
-// One warp per head and 8 consecutive tokens, each lane dk / 32 consecutive
-// channels; the warp loads the 11 rows its taps read once per branch, so HBM
-// sees each input and output row about once.
+// One warp per head and 4 consecutive tokens, each lane dk / 32 consecutive
+// channels; the warp loads the 7 rows its taps read once per branch (the rows
+// shared with the neighbouring warps come from L2), so HBM sees each input and
+// output row about once.  Blocks whose tap rows all lie inside one sequence and
+// inside the tensor (nearly all) run a path without per-tap masking or row
+// clamping.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -18,7 +21,7 @@ namespace kda {
 namespace {
 
 constexpr int kWarps = 8;         // heads per block
-constexpr int kRowsPerWarp = 8;   // consecutive tokens per warp
+constexpr int kRowsPerWarp = 4;   // consecutive tokens per warp
 constexpr int kTaps = 4;
 constexpr float kGMin = -5.f;
 constexpr float kNormEps = 1e-6f;
@@ -81,8 +84,7 @@ __device__ __forceinline__ long long seq_start(const PrologueArgs& a, long long 
   return static_cast<long long>(static_cast<unsigned>(t) / sl) * sl;
 }
 
-// Warp w of block (b, hb) handles head 8 hb + w and tokens 8 b .. 8 b + 7: the
-// 11 rows its taps read are loaded once per branch.
+// Warp w of block (b, hb) handles head 8 hb + w and tokens 4 b .. 4 b + 3.
 // Raw PER-element vectors (kept packed until used).
 template <typename T, int PER>
 struct Raw;
@@ -101,22 +103,22 @@ __device__ __forceinline__ void unpack(const R& v, float (&y)[PER]) {
                sizeof(R) == 2 * PER, __nv_bfloat16, float>::type*>(&v), y);
 }
 
-template <typename T, int DK>
-__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
+// Rows of one warp: tokens tb .. tb + R - 1 of head h.  kInterior: every tap
+// row lies inside the tensor and inside the sequence of the block's last
+// token, so no tap is masked and no row index is clamped (the common case).
+template <typename T, int DK, bool kInterior>
+__device__ __forceinline__ void prologue_rows(const PrologueArgs& a, int h, long long tb) {
   constexpr int PER = DK / 32;
   constexpr int R = kRowsPerWarp;
   constexpr int WIN = R + kTaps - 1;
   using RawT = typename Raw<T, PER>::type;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kWarps + (threadIdx.x >> 5);
-  if (h >= a.heads) return;
-  const long long tb = static_cast<long long>(blockIdx.x) * R;   // first token
   const long long n_tok = a.total_tokens;
   const int c0 = PER * lane;
   const long long rs = static_cast<long long>(a.heads) * DK;      // row stride
   const long long col = static_cast<long long>(h) * DK + c0;
-  // Every load first: the tap windows of q and k (rows tb - 3 .. tb + R - 1,
-  // clamped into the tensor) and the z rows.
+  // Every load first: the tap windows of q and k (rows tb - 3 .. tb + R - 1)
+  // and the z rows.
   RawT xw[2][WIN], zr[R];
 #pragma unroll
   for (int br = 0; br < 2; ++br) {
@@ -124,17 +126,20 @@ __global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
 #pragma unroll
     for (int i = 0; i < WIN; ++i) {
       long long src = tb - (kTaps - 1) + i;
-      src = src < 0 ? 0 : src >= n_tok ? n_tok - 1 : src;
+      if (!kInterior) src = src < 0 ? 0 : src >= n_tok ? n_tok - 1 : src;
       xw[br][i] = *reinterpret_cast<const RawT*>(x + src * rs + col);
     }
   }
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    zr[r] = *reinterpret_cast<const RawT*>(static_cast<const T*>(a.z) +
-                                           (tb + r < n_tok ? tb + r : n_tok - 1) * rs + col);
+  for (int r = 0; r < R; ++r) {
+    const long long src = kInterior || tb + r < n_tok ? tb + r : n_tok - 1;
+    zr[r] = *reinterpret_cast<const RawT*>(static_cast<const T*>(a.z) + src * rs + col);
+  }
   long long t0[R];
+  if (!kInterior) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) t0[r] = tb + r < n_tok ? seq_start(a, tb + r) : tb + r;
+    for (int r = 0; r < R; ++r) t0[r] = tb + r < n_tok ? seq_start(a, tb + r) : tb + r;
+  }
 
 #pragma unroll
   for (int br = 0; br < 2; ++br) {
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
       float y[PER] = {};
 #pragma unroll
       for (int i = 0; i < kTaps; ++i) {
-        const bool on = t - (kTaps - 1) + i >= t0[r];
+        const bool on = kInterior || t - (kTaps - 1) + i >= t0[r];
         float xv[PER];
         unpack<PER>(xw[br][r + i], xv);
 #pragma unroll
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
       const float rinv = rsqrtf(ss + kNormEps);
 #pragma unroll
       for (int u = 0; u < PER; ++u) y[u] *= rinv;
-      if (t < n_tok) stv<PER>(y_out + t * rs, y);
+      if (kInterior || t < n_tok) stv<PER>(y_out + t * rs, y);
     }
   }
   const float scale = __expf(__ldg(a.a_log + h));
@@ -179,8 +184,21 @@ __global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
     unpack<PER>(zr[r], zv);
 #pragma unroll
     for (int u = 0; u < PER; ++u) zv[u] = __fdividef(kGMin, 1.f + __expf(-scale * zv[u]));
-    if (tb + r < n_tok) stv<PER>(static_cast<T*>(a.g) + (tb + r) * rs + col, zv);
+    if (kInterior || tb + r < n_tok) stv<PER>(static_cast<T*>(a.g) + (tb + r) * rs + col, zv);
   }
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
+  constexpr int R = kRowsPerWarp;
+  const int h = blockIdx.y * kWarps + (threadIdx.x >> 5);
+  if (h >= a.heads) return;
+  const long long tb = static_cast<long long>(blockIdx.x) * R;   // first token
+  const long long n_tok = a.total_tokens;
+  const bool interior = tb >= kTaps - 1 && tb + R <= n_tok &&
+                        seq_start(a, tb + R - 1) <= tb - (kTaps - 1);
+  if (interior) prologue_rows<T, DK, true>(a, h, tb);
+  else prologue_rows<T, DK, false>(a, h, tb);
 }
 
 template <typename T, int DK>
