@@ -188,8 +188,10 @@ __device__ __forceinline__ void prologue_rows(const PrologueArgs& a, int h, long
   }
 }
 
+// bf16: four blocks per SM (measured faster than the three that 77 registers
+// allow, despite a few spilled bytes); fp32 keeps its registers.
 template <typename T, int DK>
-__global__ void __launch_bounds__(32 * kWarps) prologue_kernel(PrologueArgs a) {
+__global__ void __launch_bounds__(32 * kWarps, sizeof(T) == 2 ? 4 : 1) prologue_kernel(PrologueArgs a) {
   constexpr int R = kRowsPerWarp;
   const int h = blockIdx.y * kWarps + (threadIdx.x >> 5);
   if (h >= a.heads) return;
