@@ -604,21 +604,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- P4: A (x beta, strictly lower; fp32) and P (lower inclusive; bf16).
-      // A's blocks above the diagonal are never read and are not written; its
-      // diagonal blocks go out transposed, and the warp that holds one also
-      // inverts it (P5's diagonal blocks).  Warps 4..7 zero the blocks of T'
-      // above the diagonal meanwhile (the factor tables there are dead).
-      if (pw < 4 && ok_ap) {
-        // TMEM lane quarter pw holds rows [K'_pw; Q'_pw].
-        const int a = pw, rl = lane & 15, r = 16 * a + rl;
+      // Warps pw and pw + 4 share row tile pw & 3 (the same TMEM lanes): the
+      // first takes column blocks 0 and 2, the second 1 and 3.  A's blocks
+      // above the diagonal are never read, so only P's are written (as zeros);
+      // A's diagonal blocks go out transposed, and the warp that holds one also
+      // inverts it (P5's diagonal blocks).  The blocks of T' above the diagonal
+      // are zeroed first (the factor tables there are dead).
+      for (int e = p; e < 192; e += kPrepThreads) {
+        const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
+        const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
+        const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st_tile8(smem + kOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
+      }
+      if (ok_ap) {
+        // TMEM lane quarter pw & 3 holds rows [K'_a; Q'_a].
+        const int a = pw & 3, b0 = pw >> 2, rl = lane & 15, r = 16 * a + rl;
         const bool isP = lane >= 16;
         const float br = s_beta[r];
         uint8_t* ptile = smem + kOffP + s * 8192;
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
+        for (int jb = 0; jb < 2; ++jb) {
+          const int blk = b0 + 2 * jb;
           float v[16];
           if (blk <= a) {
-            tmem_ld16(tbase + (static_cast<uint32_t>(32 * pw) << 16) + kColAP + khat_row0(a) +
+            tmem_ld16(tbase + (static_cast<uint32_t>(32 * a) << 16) + kColAP + khat_row0(a) +
                           16 * blk,
                       v);
             tmem_ld_wait();
@@ -654,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chain is one FMA per row.  Column i of A_aa is row i of its
         // transposed copy (the 16 lanes read the same words).
         __syncwarp();
-        if (lane < 16) {
+        if (b0 == (a & 1) && lane < 16) {
           const int jj = lane;
           const float* At = Atm + 16 * a * kLdB;
           float y[16];
@@ -676,14 +686,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) Dm[(a * 16 + rr) * kLdB + jj] = y[rr];
-        }
-      } else if (pw >= 4) {
-        for (int e = p - 128; e < 192; e += kPrepThreads - 128) {
-          const int pb = e >> 5, rr = (e >> 1) & 15, h8 = e & 1;
-          const int a = pb < 3 ? 0 : pb < 5 ? 1 : 2;
-          const int b = pb < 3 ? pb + 1 : pb < 5 ? pb - 1 : 3;
-          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          st_tile8(smem + kOffTB, 16 * a + rr, 16 * b + 8 * h8, 64, z);
         }
       }
       tc_fence_before();
