@@ -129,6 +129,30 @@ def test_orthonormal_key_recall():
     np.testing.assert_allclose(fin[0, 0].T @ keys.T, vals.T, atol=1e-12)
 
 
+def test_delta_rule_shrinks_the_error_on_the_written_key():
+    """The erase-then-write update is the delta rule's error-correcting step:
+    with S' = Diag(alpha_t) S_{t-1}, the prediction error on the written key
+    after the update is (1 - beta_t |k_t|^2) times the error before it,
+    S_t^T k_t - v_t = (1 - beta_t |k_t|^2) (S'^T k_t - v_t).  States before and
+    after each token come from separate oracle runs over the two prefixes;
+    keys are not normalised, so |k|^2 enters too."""
+    rng = np.random.default_rng(41)
+    T, dk, dv = 9, 6, 5
+    q, k, v, g, beta = _rand_case(rng, T, 1, dk, dv, unit_k=False)
+    S0 = rng.standard_normal((1, 1, dk, dv)) * 0.3
+    prev = S0[0, 0]
+    for t in range(T):
+        _, fin = oracle.prefill(q[:t + 1], k[:t + 1], v[:t + 1], g[:t + 1], beta[:t + 1],
+                                init_state=S0)
+        cur = fin[0, 0]
+        decayed = np.exp(g[t, 0])[:, None] * prev
+        kt, vt, bt = k[t, 0], v[t, 0], beta[t, 0]
+        before = decayed.T @ kt - vt
+        after = cur.T @ kt - vt
+        np.testing.assert_allclose(after, (1.0 - bt * (kt @ kt)) * before, rtol=1e-10, atol=1e-12)
+        prev = cur
+
+
 @pytest.mark.parametrize("split", [1, 7, 16, 31])
 def test_split_carry(split):
     """Running [0, T) equals [0, t) then [t, T) with the state carried over."""
