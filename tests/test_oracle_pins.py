@@ -280,7 +280,9 @@ def test_generator_recipe_shapes_and_norms():
     w = inputs.WORKLOADS["varlen_32seq_H96_d128_bf16"]
     lens = inputs.seq_lengths(w, 0)
     assert len(lens) == 32 and min(lens) >= 512 and max(lens) <= 16384
-    assert 200_000 < sum(lens) < 340_000
+    assert sum(lens) == 284_058                      # the recipe's seed-0 total
+    assert list(inputs.seq_lengths(w, 0)) == list(lens)
+    assert list(inputs.seq_lengths(w, 1)) != list(lens)
     d = inputs.make_prefill(w, seed=0, lengths=[70, 3], heads=3)
     assert d["q"].shape == (73, 3, 128) and d["beta"].shape == (73, 3)
     assert d["init_state"] is None
