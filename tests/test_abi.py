@@ -153,6 +153,29 @@ def test_workspace_size(lib):
     assert size(_dims(dk=7)) == 0
 
 
+def test_dispatch_boundaries(lib, monkeypatch):
+    """The split form serves up to 304 sequence-head pairs, or any pair count
+    from at most 32 sequences, and never more than 1024 sequences; its record
+    buffer is capped at 2 GiB up to 76 pairs (overlapped windows) and at
+    16 GiB above."""
+    monkeypatch.delenv("KDA_CHUNK_PATH", raising=False)
+    algo = lambda d: lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64)
+    size = lambda d: lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), 64)
+    assert algo(_dims(n=38, t=38 * 512, h=8)) == 2      # 304 pairs
+    assert algo(_dims(n=39, t=39 * 512, h=8)) == 1      # 312 pairs, 39 sequences
+    assert algo(_dims(n=32, t=32 * 512, h=64)) == 2     # 2048 pairs, 32 sequences
+    assert algo(_dims(n=33, t=33 * 512, h=64)) == 1     # 33 sequences
+    assert algo(_dims(n=1024, t=1024 * 64, h=1)) == 1   # more than 304 pairs
+    assert algo(_dims(n=1025, t=1025 * 64, h=1)) == 1   # over the sequence cap
+    order = lambda n: (n * 4 + 255) // 256 * 256
+    states = lambda n, h: n * h * 128 * 128 * 4
+    cap = lambda gib: ((gib << 30) // REC) * REC
+    t = 1 << 20
+    assert size(_dims(n=1, t=t, h=76)) == states(1, 76) + cap(2)
+    assert size(_dims(n=1, t=t, h=77)) == states(1, 77) + cap(16)
+    assert size(_dims(n=2, t=t, h=38)) == order(2) + states(2, 38) + cap(2)
+
+
 def test_path_override(lib, monkeypatch):
     d = _dims(n=1, t=8192, h=96)
     monkeypatch.setenv("KDA_CHUNK_PATH", "fused")
