@@ -373,10 +373,17 @@ def _transition(x, cu):
 
 
 def test_kcp_transition_is_the_segment_map():
+    # Slow decay (g in [-0.05, 0]) and weak erasure keep M of order one over
+    # the 37 tokens, so a wrong M cannot hide below the tolerances (at the
+    # generator's decay M shrinks below 1e-15).
     w = inputs.Workload("kcp", heads=2, dk=8, dv=8, dtype="f32", init_state=True)
     d = inputs.make_prefill(w, seed=41, device="cpu", lengths=[37])
+    gen = torch.Generator().manual_seed(410)
+    d["g"] = -0.05 * torch.rand(d["g"].shape, generator=gen, dtype=torch.float32)
+    d["beta"] = 0.2 * d["beta"]          # weak erasure: the product of 37 steps stays O(1)
     x = [d[n] for n in ("q", "k", "v", "g", "beta")]
     M, Hs = _transition(x, d["cu_seqlens"])
+    assert np.abs(M).max() > 0.3, "M must be of order one for this pin to mean anything"
     _, fin = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
     s0 = d["init_state"].double().numpy()
     np.testing.assert_allclose(M @ s0 + Hs, fin, rtol=1e-12, atol=1e-12)
