@@ -31,8 +31,17 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA prefill Mtok/s & decode tok/s (H=96,d=128); % of GB300 roofline"
 PREFILL = "prefill_T8192_H96_d128_bf16"
 DECODE = "decode_256seq_H96_d128_64steps"
+VARLEN = "varlen_32seq_H96_d128_bf16"
+PREFILL_1M = "prefill_T1M_H32_d128_bf16"
 FALLBACK_HBM_GBS = 6800.0
 STATE_BYTES = 128 * 128 * 4
+
+
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+# Chunkwise prefill flops per (token, head) at chunk 64, d = 128, triangles
+# counted exactly: 3 (C-1) d [A, W, U0] + 2 (C+1) d [P, P U] + C^2 / 3 [T]
+# + 6 d^2 [W S0, Qtil S0, Kbar^T U] + d^2 / C [decay].
+PREFILL_FLOP_PER_TOKEN_HEAD = 140757
 
 
 def peaks():
@@ -45,11 +54,38 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def prefill_bytes(T, H, dk, dv, elt=2, n_states=1):
+def tensor_peak():
+    """Dense bf16 tensor-core rate for a kernel timed inside a long step."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured bf16_tflops_sustained"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def prefill_bytes(T, H, dk, dv, elt=2, n_states=1, states_read=None, states_written=None):
     """Algorithmic bytes: read q, k, g (dk each), v (dv), beta once, write out
-    (dv) once, plus one fp32 state read and one written per (sequence, head)."""
+    (dv) once, plus 64 KiB per fp32 state read or written (by default one of
+    each per head: n_states sequences with an initial and a final state)."""
     per_token_head = elt * (3 * dk + dv + 1 + dv)
-    return T * H * per_token_head + n_states * H * 2 * dk * dv * 4
+    r = n_states * H if states_read is None else states_read
+    w = n_states * H if states_written is None else states_written
+    return T * H * per_token_head + (r + w) * dk * dv * 4
+
+
+def tensor_block(T, H, kern_ms, hbm_peak):
+    """The chunkwise prefill's flops against the tensor-core peak, and the
+    share of that peak the HBM roof allows (flop per byte x HBM peak)."""
+    peak, src = tensor_peak()
+    flops = PREFILL_FLOP_PER_TOKEN_HEAD * T * H
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    per_byte = PREFILL_FLOP_PER_TOKEN_HEAD / prefill_bytes(1, 1, 128, 128, n_states=0)
+    return {"bound": "hbm (intensity below the ridge)", "achieved": achieved, "peak": peak,
+            "peak_source": src, "unit": "TFLOP/s", "frac": achieved / peak,
+            "flop_per_token_head": PREFILL_FLOP_PER_TOKEN_HEAD,
+            "ceiling_frac_at_hbm_peak": per_byte * hbm_peak / 1e3 / peak,
+            "north_star_goal_frac": 0.5}
 
 
 def decode_bytes(N, H, dk, dv, elt=2):
@@ -426,6 +462,14 @@ def run_gpu(args):
                 "traffic": kernel_traffic("kda_prologue.cu", "prologue_T8192_H96.md")}
     del d, args_pf, out, fin, px, pq, pk, pg
     torch.cuda.empty_cache()
+    # ------- the packed varlen and the million-token prefill workloads -------
+    big = {}
+    if args.only == "all" and not args.no_big_prefill:
+        for key, wname, steps in (("varlen", VARLEN, min(args.steps, 10)),
+                                  ("prefill_1m", PREFILL_1M, min(args.steps, 5))):
+            big[key] = run_prefill_leg(wname, max(1, steps), dev, rank, world, start, end,
+                                       stream, barrier, max_over_ranks, hbm_peak)
+            torch.cuda.empty_cache()
     decode = None
     if args.only != "prefill":
         decode = run_decode_leg(args, dev, rank, world, start, end, stream, barrier,
@@ -470,12 +514,64 @@ def run_gpu(args):
             "prefill_gated": gated,
             "kcp": kcp,
             "prologue": prologue,
+            "tensor": tensor_block(T, H, kern_ms, hbm_peak),
+            "varlen": big.get("varlen"),
+            "prefill_1m": big.get("prefill_1m"),
             "decode": decode,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_prefill_leg(wname, steps, dev, rank, world, start, end, stream, barrier,
+                    max_over_ranks, hbm_peak):
+    """One kda_chunk_fwd per step over a whole workload (inputs resident in
+    HBM, far larger than L2), timed with CUDA events on the launching stream."""
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    w = inputs.WORKLOADS[wname]
+    d = inputs.make_prefill(w, seed=rank, device=dev)
+    T, H = d["q"].shape[:2]
+    N = d["cu_seqlens"].numel() - 1
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    cu = d["cu_seqlens"] if w.varlen is not None else None
+    out = torch.empty((T, H, w.dv), dtype=w.torch_dtype, device=dev)
+    fin = torch.empty((N, H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, kda.workspace_size(N, T, H, w.dk, w.dv, w.torch_dtype, w.chunk)),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.chunk_fwd(*x, d["init_state"], cu, chunk=w.chunk, n_seqs=N, out=out,
+                      final_state=fin, workspace=ws)
+
+    for _ in range(3):
+        step()
+    barrier()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(end)) / steps
+    n_init = N * H if d["init_state"] is not None else 0
+    alg = prefill_bytes(T, H, w.dk, w.dv, states_read=n_init, states_written=N * H)
+    gbs = alg / (ms * 1e-3) / 1e9
+    algo = kda.algorithm(N, T, H, w.dk, w.dv, w.torch_dtype, w.chunk)
+    res = {"workload": wname, "n_seqs": N, "tokens": T, "heads": H,
+           "value": job_throughput(world, T, ms) / 1e6, "unit": "Mtok/s",
+           "ms_per_step": ms, "steps": steps, "algorithm": algo,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": alg,
+                        "traffic": None,
+                        "kernel": "kda_chunk_split" if algo == "tcgen05_split" else
+                                  "kda_chunk_tc"},
+           "tensor": tensor_block(T, H, ms, hbm_peak)}
+    del d, x, out, fin, ws
+    return res
 
 
 def run_decode_leg(args, dev, rank, world, start, end, stream, barrier, max_over_ranks,
@@ -543,6 +639,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-big-prefill", action="store_true",
+                    help="skip the varlen and million-token prefill legs")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
                     help="profiling aid: run one part only (no JSON line unless 'all')")
     ap.add_argument("--decode-seqs", type=int, default=None,

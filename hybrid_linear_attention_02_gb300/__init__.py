@@ -23,6 +23,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libkda.so"
 _lock = threading.Lock()
 _lib = None
+_lib_debug = None
 
 KDA_F32, KDA_BF16 = 0, 1
 _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
@@ -55,50 +56,70 @@ def load():
                 raise RuntimeError(
                     f"{path} not found: build the CUDA library first "
                     "(python -c 'import __graft_entry__ as g; g.build()')")
-            lib = ctypes.CDLL(path)
-            vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-            dp = ctypes.POINTER(_Dims)
-            lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ip]
-            lib.kda_chunk_fwd_workspace_size.restype = sz
-            lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
-                                          vp]
-            lib.kda_chunk_fwd.restype = ip
-            lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, dp, vp, vp]
-            lib.kda_decode_step.restype = ip
-            lib.kda_status_string.argtypes = [ip]
-            lib.kda_status_string.restype = ctypes.c_char_p
-            lib.kda_version.restype = ip
-            lib.kda_chunk_fwd_checkpoints.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp,
-                                                      vp, sz, vp, vp, vp, vp, ip]
-            lib.kda_chunk_fwd_checkpoints.restype = ip
-            fl = ctypes.c_float
-            lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, fl, vp, vp,
-                                                ip, dp, vp, sz, vp, vp]
-            lib.kda_chunk_fwd_gated.restype = ip
-            lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, fl, vp, vp, dp, vp,
-                                                  vp]
-            lib.kda_decode_step_gated.restype = ip
-            ll = ctypes.c_longlong
-            lib.kda_chunk_transition_workspace_size.argtypes = [dp]
-            lib.kda_chunk_transition_workspace_size.restype = sz
-            lib.kda_chunk_transition.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz,
-                                                 vp, vp]
-            lib.kda_chunk_transition.restype = ip
-            lib.kda_transition_apply.argtypes = [vp, vp, vp, vp, ll, ip, ip, vp]
-            lib.kda_transition_apply.restype = ip
-            lib.kda_debug_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
-            lib.kda_debug_wait_timeout.restype = ip
-            lib.kda_chunk_fwd_kcp_workspace_size.argtypes = [dp, ip]
-            lib.kda_chunk_fwd_kcp_workspace_size.restype = sz
-            lib.kda_chunk_fwd_kcp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
-                                              vp]
-            lib.kda_chunk_fwd_kcp.restype = ip
-            lib.kda_prologue.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
-            lib.kda_prologue.restype = ip
-            lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
-            lib.kda_chunk_fwd_algorithm.restype = ip
-            _lib = lib
+            _lib = _declare(ctypes.CDLL(path))
     return _lib
+
+
+def load_debug_bounds():
+    """The KDA_DEBUG_BOUNDS build of the library (libkda_debug.so, built on
+    first use): every prefill and decode call given a dev_status first checks
+    g in [-5, 0] and beta in [0, 1] on the device (KDA_ERR_RANGE).  Same
+    entry points as ``load()``."""
+    global _lib_debug
+    with _lock:
+        if _lib_debug is None:
+            from . import build as _build
+            _lib_debug = _declare(ctypes.CDLL(_build.build(debug_bounds=True)))
+    return _lib_debug
+
+
+def _declare(lib):
+    """Argument and result types of every entry point of kda.h."""
+    vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    dp = ctypes.POINTER(_Dims)
+    lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ip]
+    lib.kda_chunk_fwd_workspace_size.restype = sz
+    lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
+                                  vp]
+    lib.kda_chunk_fwd.restype = ip
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, dp, vp, vp]
+    lib.kda_decode_step.restype = ip
+    lib.kda_status_string.argtypes = [ip]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_version.restype = ip
+    lib.kda_chunk_fwd_checkpoints.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, dp,
+                                              vp, sz, vp, vp, vp, vp, ip]
+    lib.kda_chunk_fwd_checkpoints.restype = ip
+    fl = ctypes.c_float
+    lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, fl, vp, vp,
+                                        ip, dp, vp, sz, vp, vp]
+    lib.kda_chunk_fwd_gated.restype = ip
+    lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, fl, vp, vp, dp, vp,
+                                          vp]
+    lib.kda_decode_step_gated.restype = ip
+    ll = ctypes.c_longlong
+    lib.kda_chunk_transition_workspace_size.argtypes = [dp]
+    lib.kda_chunk_transition_workspace_size.restype = sz
+    lib.kda_chunk_transition.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz,
+                                         vp, vp]
+    lib.kda_chunk_transition.restype = ip
+    lib.kda_transition_apply.argtypes = [vp, vp, vp, vp, ll, ip, ip, vp]
+    lib.kda_transition_apply.restype = ip
+    lib.kda_debug_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
+    lib.kda_debug_wait_timeout.restype = ip
+    lib.kda_chunk_fwd_kcp_workspace_size.argtypes = [dp, ip]
+    lib.kda_chunk_fwd_kcp_workspace_size.restype = sz
+    lib.kda_chunk_fwd_kcp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, dp, vp, sz, vp,
+                                      vp]
+    lib.kda_chunk_fwd_kcp.restype = ip
+    lib.kda_prologue.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp]
+    lib.kda_prologue.restype = ip
+    lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
+    lib.kda_chunk_fwd_algorithm.restype = ip
+    lib.kda_check_inputs.argtypes = [vp, vp, dp, vp, vp]
+    lib.kda_check_inputs.restype = ip
+    lib.kda_debug_bounds_build.restype = ip
+    return lib
 
 
 def _ptr(t):
@@ -319,6 +340,24 @@ def chunk_transition(q, k, v, g, beta, cu_seqlens=None, *, n_seqs: int | None = 
     if rc != 0:
         raise KDAError(rc, "kda_chunk_transition")
     return M, Hs
+
+
+def check_inputs(g, beta, dev_status, *, stream=None, lib=None):
+    """Range precondition of the inputs (``kda_check_inputs``): sets the device
+    int dev_status to KDA_ERR_RANGE if any g [T, H, dk] lies outside [-5, 0] or
+    any beta [T, H] outside [0, 1] (NaN included), unless it is non-zero
+    already.  Asynchronous; read dev_status after synchronising."""
+    lib = lib or load()
+    T, H, dk = g.shape
+    dev, dt = g.device, g.dtype
+    _check_input("beta", beta, (T, H), dt, dev)
+    _check_input("dev_status", dev_status, (1,), torch.int32, dev)
+    d = _dims(1, T, H, dk, dk, dt)
+    with torch.cuda.device(dev):
+        rc = lib.kda_check_inputs(_ptr(g), _ptr(beta), ctypes.byref(d), _ptr(dev_status),
+                                  _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_check_inputs")
 
 
 def debug_wait_timeout(dev_status, timeout_us: int, *, stream=None):

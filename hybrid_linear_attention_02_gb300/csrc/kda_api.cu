@@ -11,21 +11,14 @@
 
 namespace {
 
-using kda::LaunchArgs;
-
-constexpr size_t kWorkspaceAlign = 256;
-
 bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 
-size_t order_bytes(int n_seqs) {
-  if (n_seqs <= 1) return 0;
-  const size_t b = sizeof(int) * static_cast<size_t>(n_seqs);
-  return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
-}
+}  // namespace
 
-// Shared shape checks for prefill and decode.
+namespace kda {
+
 int check_dims(const kda_dims* d) {
   if (!d) return KDA_ERR_INVALID;
   if (d->n_seqs < 0 || d->heads < 0 || d->total_tokens < 0 || d->dk <= 0 || d->dv <= 0)
@@ -45,6 +38,49 @@ int check_io_pointers(const void* q, const void* k, const void* v, const void* g
       !aligned(out, 16))
     return KDA_ERR_ALIGNMENT;
   return KDA_OK;
+}
+
+int check_prefill_head(const void* q, const void* k, const void* v, const void* g,
+                       const void* beta, const void* out, int chunk, const kda_dims* d) {
+  int rc = check_dims(d);
+  if (rc != KDA_OK) return rc;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+  return check_io_pointers(q, k, v, g, beta, out, d);
+}
+
+int check_prefill_tail(const float* init_state, const float* final_state,
+                       const int* cu_seqlens, const kda_dims* d, long long* seq_len,
+                       bool* nothing_to_do) {
+  *nothing_to_do = false;
+  *seq_len = 0;
+  const int N = d->n_seqs;
+  if (N == 0 || d->heads == 0) {
+    *nothing_to_do = true;
+    return d->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
+  }
+  if (!cu_seqlens) {
+    if (d->total_tokens % N != 0) return KDA_ERR_INVALID;
+    *seq_len = d->total_tokens / N;
+  }
+  if ((init_state && !aligned(init_state, 16)) || (final_state && !aligned(final_state, 16)))
+    return KDA_ERR_ALIGNMENT;
+  return KDA_OK;
+}
+
+}  // namespace kda
+
+namespace {
+
+using kda::LaunchArgs;
+using kda::check_dims;
+using kda::check_io_pointers;
+
+constexpr size_t kWorkspaceAlign = 256;
+
+size_t order_bytes(int n_seqs) {
+  if (n_seqs <= 1) return 0;
+  const size_t b = sizeof(int) * static_cast<size_t>(n_seqs);
+  return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
 }
 
 size_t align_up(size_t b) { return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign; }
@@ -92,6 +128,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_SCRATCH_LIMIT: return "more sequences than the no-alloc scratch array holds";
+    case KDA_ERR_RANGE: return "input out of range: g outside [-5, 0] or beta outside [0, 1]";
     default: return "unknown status";
   }
 }
@@ -144,10 +181,7 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   float* ckpt = x.ckpt;
   const int* ckpt_offsets = x.ckpt_offsets;
   const int ckpt_interval = x.ckpt_interval;
-  int rc = check_dims(dims);
-  if (rc != KDA_OK) return rc;
-  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
-  rc = check_io_pointers(q, k, v, g, beta, out, dims);
+  int rc = kda::check_prefill_head(q, k, v, g, beta, out, chunk, dims);
   if (rc != KDA_OK) return rc;
   if (ckpt) {
     if (!ckpt_offsets || ckpt_interval <= 0) return KDA_ERR_INVALID;
@@ -161,14 +195,11 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
     }
   }
   const int N = dims->n_seqs;
-  if (N == 0 || dims->heads == 0) return dims->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
   long long seq_len = 0;
-  if (!cu_seqlens) {
-    if (dims->total_tokens % N != 0) return KDA_ERR_INVALID;
-    seq_len = dims->total_tokens / N;
-  }
-  if ((init_state && !aligned(init_state, 16)) || (final_state && !aligned(final_state, 16)))
-    return KDA_ERR_ALIGNMENT;
+  bool nothing_to_do = false;
+  rc = kda::check_prefill_tail(init_state, final_state, cu_seqlens, dims, &seq_len,
+                               &nothing_to_do);
+  if (rc != KDA_OK || nothing_to_do) return rc;
   const size_t need = order_bytes(N);
   if (need > 0 && cu_seqlens && (!workspace || workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
@@ -193,6 +224,13 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   a.gate_eps = x.gate_eps;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+#ifdef KDA_DEBUG_BOUNDS
+  // Debug build: the inputs' range precondition is checked on the device
+  // before the prefill runs (reported through dev_status, never trapped).
+  if (dev_status && kda::launch_range_check(g, beta, dims->total_tokens, dims->heads, dims->dk,
+                                            dims->dtype, dev_status, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+#endif
   if (need > 0 && cu_seqlens && N > 1) {   // one sequence: no order needed
     int* order = static_cast<int*>(workspace);
     if (kda::launch_length_order(cu_seqlens, N, order, s) != cudaSuccess) return KDA_ERR_CUDA;
@@ -457,6 +495,28 @@ int kda_prologue(const void* q_pre, const void* k_pre, const void* z, const floa
              : KDA_ERR_CUDA;
 }
 
+int kda_check_inputs(const void* g, const void* beta, const kda_dims* dims, int* dev_status,
+                     void* stream) {
+  const int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (!dev_status) return KDA_ERR_INVALID;
+  if (dims->total_tokens == 0 || dims->heads == 0) return KDA_OK;
+  if (!g || !beta) return KDA_ERR_INVALID;
+  if (!aligned(g, 16)) return KDA_ERR_ALIGNMENT;
+  return kda::launch_range_check(g, beta, dims->total_tokens, dims->heads, dims->dk, dims->dtype,
+                                 dev_status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
+int kda_debug_bounds_build(void) {
+#ifdef KDA_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 int kda_decode_step_gated(const void* q, const void* k, const void* v, const void* g,
                           const void* beta, const void* gate, const float* norm_weight,
                           float eps, float* state, void* out, const kda_dims* dims,
@@ -505,6 +565,12 @@ int decode_impl(const void* q, const void* k, const void* v, const void* g, cons
   a.dev_status = dev_status;
   a.n_seqs = dims->n_seqs; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
   a.dtype = dims->dtype; a.chunk = 1; a.total_tokens = dims->total_tokens;
+#ifdef KDA_DEBUG_BOUNDS
+  if (dev_status && kda::launch_range_check(g, beta, dims->n_seqs, dims->heads, dims->dk,
+                                            dims->dtype, dev_status,
+                                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KDA_ERR_CUDA;
+#endif
   return kda::launch_recurrent(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KDA_OK
              : KDA_ERR_CUDA;

@@ -912,9 +912,12 @@ bool make_token_map(CUtensorMap* map, const void* base, int heads, long long tok
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A requested chunk of 16 or 32 tokens is served by the 64-token chunks of
+// the tensor-core kernels (each made of the same 16-token tiles): the chunk
+// size only blocks the computation, the result is the same function.
 bool chunk_tc_supported(const LaunchArgs& a) {
-  return a.dtype == KDA_BF16 && a.dk == kD && a.dv == kD && a.chunk == kC &&
-         a.total_tokens < (1ll << 31);
+  return a.dtype == KDA_BF16 && a.dk == kD && a.dv == kD &&
+         (a.chunk == 16 || a.chunk == 32 || a.chunk == kC) && a.total_tokens < (1ll << 31);
 }
 
 cudaError_t launch_chunk_tc(const LaunchArgs& a, cudaStream_t stream) {

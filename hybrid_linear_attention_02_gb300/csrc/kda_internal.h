@@ -9,6 +9,22 @@
 
 namespace kda {
 
+// Host-side argument checks shared by the entry points (kda_api.cu); each
+// returns a kda_status.  check_dims: the shape record.  check_io_pointers:
+// q, k, v, g, beta, out present and 16-byte aligned (unless there is no
+// token).  check_prefill_head: check_dims, the chunk size, then the pointers.
+// check_prefill_tail: an empty call (no sequence or no head) sets
+// *nothing_to_do; otherwise the equal-length split when cu_seqlens is NULL
+// (*seq_len) and the states' alignment.
+int check_dims(const kda_dims* d);
+int check_io_pointers(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const void* out, const kda_dims* d);
+int check_prefill_head(const void* q, const void* k, const void* v, const void* g,
+                       const void* beta, const void* out, int chunk, const kda_dims* d);
+int check_prefill_tail(const float* init_state, const float* final_state,
+                       const int* cu_seqlens, const kda_dims* d, long long* seq_len,
+                       bool* nothing_to_do);
+
 // Arguments of one prefill or decode launch, already validated on the host.
 struct LaunchArgs {
   const void *q, *k, *v, *g, *beta;
@@ -76,6 +92,12 @@ struct PrologueArgs {
   long long total_tokens;
 };
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream);
+
+// Sets *dev_status to KDA_ERR_RANGE (unless it holds an error already) when
+// any g of [tokens, heads, dk] lies outside [-5, 0] or any beta of
+// [tokens, heads] outside [0, 1] (NaN included).  g is 16-byte aligned.
+cudaError_t launch_range_check(const void* g, const void* beta, long long tokens, int heads,
+                               int dk, int dtype, int* dev_status, cudaStream_t stream);
 
 // Writes order[0..N) = sequence indices by decreasing length (ties by index).
 cudaError_t launch_length_order(const int* cu_seqlens, int n_seqs, int* order,

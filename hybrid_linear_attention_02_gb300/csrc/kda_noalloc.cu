@@ -13,41 +13,27 @@
 // The array holds kNoAllocMaxSeqs sequence indices (256 KiB).  Every GPU that
 // loads the library keeps it until the process exits.  Host code must not
 // hand the array's symbol to a kernel (on the host it is only a stand-in);
-// its device address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current.
-#include <mutex>
-
+// each call looks up its device address with cudaGetSymbolAddress for the
+// device current at the call.  The lookup is repeated on every call rather
+// than cached, so a new context on the device (after cudaDeviceReset, say),
+// where the module may load at another address, never sees a stale pointer.
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
 constexpr int kNoAllocMaxSeqs = KDA_NOALLOC_MAX_SEQS;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int g_seq_order[kNoAllocMaxSeqs];
 
-std::mutex g_setup_mutex;
-int* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_seq_order on the current device (set up once per device).
+// Device address of g_seq_order in the current device's context.
 cudaError_t scratch_for_current_device(int** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_seq_order);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_seq_order);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<int*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<int*>(p);
   return cudaSuccess;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 }  // namespace kda
@@ -57,29 +43,16 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                                      const int* cu_seqlens, void* out, float* final_state,
                                      int chunk, const kda_dims* d, int* dev_status,
                                      void* stream) {
-  if (!d) return KDA_ERR_INVALID;
-  if (d->n_seqs < 0 || d->heads < 0 || d->total_tokens < 0 || d->dk <= 0 || d->dv <= 0)
-    return KDA_ERR_INVALID;
-  if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
-  if ((d->dk != 64 && d->dk != 128) || (d->dv != 64 && d->dv != 128)) return KDA_ERR_UNSUPPORTED;
-  if (d->heads > 65535 && d->n_seqs > 0) return KDA_ERR_UNSUPPORTED;
-  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+  // The same checks, in the same order, as kda_chunk_fwd; only the scratch
+  // limit is this entry point's own.
+  int rc = kda::check_prefill_head(q, k, v, g, beta, out, chunk, d);
+  if (rc != KDA_OK) return rc;
   if (d->n_seqs > kda::kNoAllocMaxSeqs) return KDA_ERR_SCRATCH_LIMIT;
-  if (d->n_seqs == 0 || d->heads == 0) return d->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID;
-  if (d->total_tokens > 0) {
-    if (!q || !k || !v || !g || !beta || !out) return KDA_ERR_INVALID;
-    if (!kda::aligned16(q) || !kda::aligned16(k) || !kda::aligned16(v) || !kda::aligned16(g) ||
-        !kda::aligned16(out))
-      return KDA_ERR_ALIGNMENT;
-  }
-  if ((init_state && !kda::aligned16(init_state)) ||
-      (final_state && !kda::aligned16(final_state)))
-    return KDA_ERR_ALIGNMENT;
   long long seq_len = 0;
-  if (!cu_seqlens) {
-    if (d->total_tokens % d->n_seqs != 0) return KDA_ERR_INVALID;
-    seq_len = d->total_tokens / d->n_seqs;
-  }
+  bool nothing_to_do = false;
+  rc = kda::check_prefill_tail(init_state, final_state, cu_seqlens, d, &seq_len,
+                               &nothing_to_do);
+  if (rc != KDA_OK || nothing_to_do) return rc;
 
   kda::LaunchArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;

@@ -58,7 +58,9 @@ typedef enum {
   KDA_ERR_TIMEOUT = -4,     /* device: a bounded wait expired (via dev_status)  */
   KDA_ERR_ALIGNMENT = -5,   /* a buffer is not 16-byte aligned where required   */
   KDA_ERR_WORKSPACE = -6,   /* workspace missing or smaller than required       */
-  KDA_ERR_SCRATCH_LIMIT = -7 /* more sequences than kda_chunk_fwd_noalloc holds */
+  KDA_ERR_SCRATCH_LIMIT = -7, /* more sequences than kda_chunk_fwd_noalloc holds */
+  KDA_ERR_RANGE = -8         /* device: g outside [-5, 0] or beta outside [0, 1]
+                                (kda_check_inputs; via dev_status)               */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -99,9 +101,12 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  *   dev_status        optional device int, set non-zero by a kernel whose
  *                     bounded wait expired (KDA_ERR_TIMEOUT); never cleared.
  *   stream            cudaStream_t to enqueue on.
- * Paths: bf16 with dk = dv = 128 and chunk = 64 runs on tcgen05 tensor cores
- * (requires q, k, v, g, out 16-byte aligned); every other supported case runs
- * the fp32 CUDA-core kernel that walks the recurrence.  On tensor cores, few
+ * Paths: bf16 with dk = dv = 128 runs on tcgen05 tensor cores (requires q,
+ * k, v, g, out 16-byte aligned); a requested chunk of 16 or 32 tokens is
+ * served there by 64-token chunks made of the same 16-token tiles (the chunk
+ * size blocks the computation and does not change the result).  Every other
+ * supported case runs the fp32 CUDA-core kernel that walks the recurrence.
+ * On tensor cores, few
  * (sequence, head) pairs (N x H <= 304) or few sequences (N <= 32) run the
  * split form, given a workspace of kda_chunk_fwd_workspace_size() bytes: a
  * preparation kernel over every chunk at once, which writes a 66,048-byte
@@ -114,7 +119,9 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  * one record per pair runs the split form in more, smaller windows; below
  * that, and otherwise, one fused kernel per pair runs.  The
  * environment variable KDA_CHUNK_PATH=fused|split overrides the choice.
- * Inputs with g outside [-5, 0] are outside the tensor-core path's contract.
+ * Inputs with g outside [-5, 0] are outside the tensor-core path's contract;
+ * kda_check_inputs (below) checks it on the device, and a KDA_DEBUG_BOUNDS
+ * build of the library runs that check inside the call.
  */
 KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
                   const float* init_state, const int* cu_seqlens, void* out, float* final_state,
@@ -271,18 +278,20 @@ KDA_API int kda_decode_step_gated(const void* q, const void* k, const void* v, c
  * fragments a pool sized once at start-up.  The paper has no counterpart to
  * this entry point; it exists for those callers only.
  *
- * Arguments, layouts and results are those of kda_chunk_fwd; bf16 with
- * dk = dv = 128 and chunk 64 always runs the fused tensor-core kernel (the
- * split form needs a workspace for its records).  The only
+ * Arguments, layouts, checks and results are those of kda_chunk_fwd; bf16
+ * with dk = dv = 128 always runs the fused tensor-core kernel (the split
+ * form needs a workspace for its records).  The only
  * scratch (the longest-first order of the packed sequences) lives in a fixed
  * device array inside libkda.so that holds KDA_NOALLOC_MAX_SEQS entries
  * (256 KiB); every GPU that loads the library keeps it until the process
  * exits.  No call allocates or frees memory.
  *   - More than KDA_NOALLOC_MAX_SEQS sequences: returns KDA_ERR_SCRATCH_LIMIT
  *     before any launch.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture.
+ *   - Every call looks up the array's device address for the device
+ *     current at the call (cudaGetSymbolAddress, which allocates nothing),
+ *     so a new context on the device (after cudaDeviceReset) is handled.
+ *     The first call on a device may load the library's device code there;
+ *     make that first call before any stream capture.
  *   - All calls share the one array and each call rewrites the entries it
  *     uses before reading them, so nothing carries over between calls.  Calls
  *     that overlap on the GPU (different streams, no ordering between them)
@@ -307,6 +316,25 @@ typedef enum {
  * kda_status for dims kda_chunk_fwd would reject.
  */
 KDA_API int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk);
+
+/*
+ * Input precondition check.  The chunked tensor-core path relies on the
+ * lower-bounded decay of "[Paper Review] Kimi K3: Open Frontier
+ * Intelligence", section "Kimi Delta Attention (KDA)": g = g_min sigmoid(.)
+ * with g_min = -5 keeps every g in [-5, 0], so a 16-token tile's log-decay
+ * stays above -80 and its in-tile factors below e^80; beta lies in [0, 1].
+ * This call enqueues one pass over g [T_total, H, dk] and beta [T_total, H]
+ * (dtype and sizes from dims; g 16-byte aligned) and sets *dev_status
+ * (device int, required) to KDA_ERR_RANGE if any g is outside [-5, 0] or any
+ * beta outside [0, 1] (NaN counts as outside), unless *dev_status already
+ * holds a non-zero code.  Nothing traps.  A library built with
+ * KDA_DEBUG_BOUNDS defined runs this check inside every prefill and decode
+ * call that is given a dev_status (kda_debug_bounds_build() returns 1 for
+ * such a build, 0 otherwise).
+ */
+KDA_API int kda_check_inputs(const void* g, const void* beta, const kda_dims* dims,
+                             int* dev_status, void* stream);
+KDA_API int kda_debug_bounds_build(void);
 
 /* Static description of a status code (never NULL). */
 KDA_API const char* kda_status_string(int status);

@@ -3,12 +3,22 @@
 fp32 inputs: max|x - ref| / max|ref| <= 1e-4 per tensor (normwise max).
 bf16 inputs: |x - ref| <= 2e-2 |ref| + 1e-2 elementwise.
 Both apply to outputs and final states.
+
+The fp32 bound is read normwise: "max relative error 1e-4" taken over the
+whole tensor, with the tensor's largest magnitude as the scale.  The stricter
+elementwise reading (|x - ref| / |ref| per element) is also measured, without
+asserting on it, over the elements with |ref| above F32_ELEM_FLOOR times the
+tensor's largest magnitude (below that, relative error measures rounding of
+near-cancelled sums rather than the kernel); the worst value seen in a test
+run is printed in the session summary.
 """
 import numpy as np
 import torch
 
 F32_REL = 1e-4
 BF16_REL, BF16_ABS = 2e-2, 1e-2
+F32_ELEM_FLOOR = 1e-3
+F32_ELEMENTWISE = []     # (what, normwise error, worst elementwise relative error)
 
 
 def to64(x):
@@ -24,6 +34,9 @@ def assert_close(got, ref, dtype, what=""):
     if dtype in ("f32", torch.float32):
         scale = max(np.abs(ref).max(), 1e-30)
         err = np.abs(got - ref).max() / scale
+        big = np.abs(ref) > F32_ELEM_FLOOR * scale
+        elem = float((np.abs(got - ref)[big] / np.abs(ref)[big]).max()) if big.any() else 0.0
+        F32_ELEMENTWISE.append((what, float(err), elem))
         assert err <= F32_REL, f"{what}: normwise max rel err {err:.3e} > {F32_REL}"
         return err
     excess = np.abs(got - ref) - (BF16_REL * np.abs(ref) + BF16_ABS)

@@ -43,10 +43,46 @@ def test_wait_timeout_self_test_rejects_bad_arguments(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert lib.kda_status_string(code)
+    assert b"[-5, 0]" in lib.kda_status_string(-8)      # KDA_ERR_RANGE
     assert lib.kda_status_string(12345) == b"unknown status"
     assert lib.kda_version() >= 10000
+
+
+def test_range_check_host_validation(lib):
+    """kda_check_inputs refuses bad arguments on the host (no launch); the
+    default build does not run it inside the prefill and decode calls."""
+    d = _dims(n=1, t=64)
+    assert lib.kda_check_inputs(FAKE, FAKE, ctypes.byref(d), None, None) == -1   # no status
+    assert lib.kda_check_inputs(None, FAKE, ctypes.byref(d), FAKE, None) == -1   # no g
+    assert lib.kda_check_inputs(MISALIGNED, FAKE, ctypes.byref(d), FAKE, None) == -5
+    assert lib.kda_check_inputs(FAKE, FAKE, ctypes.byref(_dims(dk=96)), FAKE, None) == -2
+    assert lib.kda_check_inputs(FAKE, FAKE, ctypes.byref(_dims(n=0, t=0)), FAKE, None) == 0
+    assert lib.kda_debug_bounds_build() == 0
+
+
+def test_noalloc_validates_like_kda_chunk_fwd(lib):
+    """Both prefill entry points share their argument checks: the same status
+    for the same arguments (only the scratch limit is the no-alloc call's)."""
+    vp = ctypes.c_void_p
+    fn = lib.kda_chunk_fwd_noalloc
+    fn.argtypes = [vp] * 9 + [ctypes.c_int, ctypes.POINTER(kda._Dims), vp, vp]
+    fn.restype = ctypes.c_int
+    cases = [
+        (_dims(n=0, t=0), FAKE, MISALIGNED, 64),   # empty call, misaligned state: fine
+        (_dims(), FAKE, MISALIGNED, 64),           # misaligned state
+        (_dims(), MISALIGNED, None, 64),           # misaligned input
+        (_dims(), FAKE, None, 48),                 # unsupported chunk
+        (_dims(n=3, t=64), FAKE, None, 64),        # not divisible
+        (_dims(dk=96), FAKE, None, 64),
+    ]
+    for d, q, s0, chunk in cases:
+        a = lib.kda_chunk_fwd(q, FAKE, FAKE, FAKE, FAKE, s0, None, FAKE, None, chunk,
+                              ctypes.byref(d), None, 0, None, None)
+        b = fn(q, FAKE, FAKE, FAKE, FAKE, s0, None, FAKE, None, chunk, ctypes.byref(d), None,
+               None)
+        assert a == b, (d.n_seqs, d.total_tokens, chunk, a, b)
 
 
 def _dims(n=1, t=64, h=2, dk=128, dv=128, dtype=1):
@@ -148,8 +184,13 @@ def test_workspace_size(lib):
     # Many pairs from many sequences: one fused kernel per pair, order array only.
     d = _dims(n=64, t=270000, h=96)
     assert algo(d) == 1 and size(d) == 256
-    # chunk 16 or 32 runs the CUDA-core path.
-    assert algo(_dims(n=1, t=8192, h=96), 32) == 0
+    # bf16 chunk 16 or 32 is served by the tensor-core kernels' 64-token
+    # chunks (no silent fall back to the CUDA-core path).
+    for c in (16, 32):
+        assert algo(_dims(n=1, t=8192, h=96), c) == 2
+        assert size(_dims(n=1, t=8192, h=96), c) == size(_dims(n=1, t=8192, h=96), 64)
+        assert algo(_dims(n=64, t=270000, h=96), c) == 1
+    assert algo(_dims(n=1, t=8192, h=96, dtype=0), 32) == 0   # fp32: the recurrence
     assert size(_dims(dk=7)) == 0
 
 

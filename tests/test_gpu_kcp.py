@@ -70,3 +70,64 @@ def test_kcp_prefill_matches_oracle(n_seqs, segments):
     ro, rf = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
     assert_close(out, ro, "bf16", "kcp out")
     assert_close(fin, rf, "bf16", "kcp final_state")
+
+
+def _slow_decay(d, seed):
+    """g in [-0.05, 0]: over segments of up to 64 tokens M stays of order one
+    (at the generator's decay it falls below 1e-10 and any small M passes)."""
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    d["g"] = (-0.05 * torch.rand(d["g"].shape, generator=gen, device=DEV)).to(d["g"].dtype)
+    return d
+
+
+def _assert_scaled(got, ref, what):
+    """bf16 bound with the absolute floor scaled to the tensor's size:
+    |x - ref| <= 2e-2 |ref| + 1e-2 max|ref|."""
+    got, ref = to64(got), to64(ref)
+    scale = float(np.abs(ref).max())
+    assert scale > 0.5, f"{what}: max|ref| = {scale:.3e}, the check would be vacuous"
+    err = np.abs(got - ref)
+    excess = err - (2e-2 * np.abs(ref) + 1e-2 * scale)
+    assert excess.max() <= 0, f"{what}: max |err| {err.max():.3e} (max|ref| {scale:.3e})"
+    return float(err.max())
+
+
+@pytest.mark.parametrize("lengths", [[1, 17, 64, 33, 0, 50], [64, 2, 63]])
+def test_transitions_at_slow_decay_match_oracle_elementwise(lengths):
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=54, device=DEV,
+                            lengths=lengths, heads=2)
+    _slow_decay(d, 540)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    M, Hs = kda.chunk_transition(*x, d["cu_seqlens"])
+    torch.cuda.synchronize()
+    rM, rH = _oracle_transition(x, d["cu_seqlens"])
+    for n, L in enumerate(lengths):
+        if L == 0:
+            continue
+        eM = _assert_scaled(M[n], rM[n], f"M of segment {n} ({L} tokens)")
+        eH = _assert_scaled(Hs[n], rH[n], f"H of segment {n} ({L} tokens)")
+        print(f"segment {n} ({L} tokens): M err {eM:.3e}, H err {eH:.3e}, "
+              f"max|M| {np.abs(rM[n]).max():.3f}")
+    # A wrong M would move the composed state: M S + H against the oracle's end state.
+    s0 = torch.randn((len(lengths), 2, 128, 128), device=DEV) * 0.02
+    y = kda.transition_apply(M, Hs, s0)
+    _, rf = oracle.prefill(*x, s0, d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert_close(y, rf, "bf16", "M S0 + H vs the oracle's end state")
+
+
+@pytest.mark.parametrize("segments", [3, 8])
+def test_kcp_prefill_at_slow_decay_matches_oracle(segments):
+    """At slow decay every segment's entry state depends on all earlier ones
+    through M, so the composition is exercised."""
+    T = 2048
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=55, device=DEV,
+                            lengths=[T], heads=3)
+    _slow_decay(d, 550)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    out, fin = kda.chunk_fwd_kcp(*x, d["init_state"], n_seqs=1, segments=segments)
+    torch.cuda.synchronize()
+    ro, rf = oracle.prefill(*x, d["init_state"], d["cu_seqlens"])
+    eo = assert_close(out, ro, "bf16", "kcp slow-decay out")
+    ef = assert_close(fin, rf, "bf16", "kcp slow-decay final_state")
+    print(f"kcp {segments} segments, slow decay: out err {eo:.3e}, final err {ef:.3e}")

@@ -1,8 +1,11 @@
 """kda_chunk_fwd_noalloc, the prefill entry point for callers that cannot
 allocate device memory (an engine plugin that only receives pre-planned
-buffers, a serving loop that must not call cudaMalloc).  It is checked against
-kda_chunk_fwd on the same inputs, on two calls in a row, because every call
-shares one scratch array inside the library.
+buffers, a serving loop that must not call cudaMalloc).  Its outputs are
+checked against the fp64 oracle, on two calls in a row, because every call
+shares one scratch array inside the library: with several packed sequences
+(the longest-first order in the array), with one sequence (no order needed),
+and with 8,193 sequences (above the 8,192 that the longest-first sort serves,
+the order written there is the identity).
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -13,6 +16,7 @@ import pytest
 import torch
 
 import hybrid_linear_attention_02_gb300 as kda
+import oracle
 from hybrid_linear_attention_02_gb300 import inputs
 from parity import assert_close
 
@@ -45,8 +49,13 @@ def _call_noalloc(fn, d, chunk=64):
     return out, fin
 
 
+def _oracle(d):
+    return oracle.prefill(*(d[n] for n in ("q", "k", "v", "g", "beta")), d["init_state"],
+                          d["cu_seqlens"])
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_noalloc_matches_workspace_entry_point_twice(dtype):
+def test_noalloc_matches_oracle_twice(dtype):
     fn = _noalloc_fn()
     tag = "bf16" if dtype == torch.bfloat16 else "f32"
     w = inputs.Workload("noalloc", heads=3, dk=128, dv=128, dtype=tag, init_state=True)
@@ -55,11 +64,43 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype):
     for seed, lengths in ((11, [130, 7, 0, 64, 300]), (12, [5, 65, 1, 190, 0, 64, 33, 129, 2])):
         d = inputs.make_prefill(w, seed=seed, device=DEV, lengths=lengths)
         out, fin = _call_noalloc(fn, d)
-        ref_out, ref_fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                         d["init_state"], d["cu_seqlens"], chunk=64)
         torch.cuda.synchronize()
-        assert_close(out, ref_out, tag, "noalloc out vs kda_chunk_fwd")
-        assert_close(fin, ref_fin, tag, "noalloc final_state vs kda_chunk_fwd")
+        ro, rf = _oracle(d)
+        assert_close(out, ro, tag, "noalloc out vs oracle")
+        assert_close(fin, rf, tag, "noalloc final_state vs oracle")
+
+
+def test_noalloc_one_sequence():
+    fn = _noalloc_fn()
+    w = inputs.Workload("noalloc1", heads=2, dk=128, dv=128, dtype="bf16", init_state=True)
+    d = inputs.make_prefill(w, seed=13, device=DEV, lengths=[517])
+    out, fin = _call_noalloc(fn, d)
+    torch.cuda.synchronize()
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "noalloc one-sequence out")
+    assert_close(fin, rf, "bf16", "noalloc one-sequence final_state")
+
+
+def test_noalloc_many_sequences_then_a_small_call():
+    """8,193 sequences of 1 to 3 tokens (one head), one more than the
+    longest-first sort serves; the next call, with few sequences, must not
+    read what the big one left in the array."""
+    fn = _noalloc_fn()
+    w = inputs.Workload("noalloc_many", heads=1, dk=128, dv=128, dtype="bf16", init_state=True)
+    rng = torch.Generator().manual_seed(14)
+    lengths = (torch.randint(1, 4, (8193,), generator=rng)).tolist()
+    d = inputs.make_prefill(w, seed=14, device=DEV, lengths=lengths)
+    out, fin = _call_noalloc(fn, d)
+    torch.cuda.synchronize()
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "noalloc 8193-sequence out")
+    assert_close(fin, rf, "bf16", "noalloc 8193-sequence final_state")
+    d = inputs.make_prefill(w, seed=15, device=DEV, lengths=[40, 3, 90])
+    out, fin = _call_noalloc(fn, d)
+    torch.cuda.synchronize()
+    ro, rf = _oracle(d)
+    assert_close(out, ro, "bf16", "noalloc small call after the big one: out")
+    assert_close(fin, rf, "bf16", "noalloc small call after the big one: final_state")
 
 
 def test_noalloc_rejects_too_many_sequences():
