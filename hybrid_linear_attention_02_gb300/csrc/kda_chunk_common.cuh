@@ -63,6 +63,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), for a pair (x0, x1),
+// packed low half first: x is carried to about 2^-17 relative.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack2(x0, x1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+  lo = pack2(x0 - h0, x1 - h1);
+}
+
 __device__ __forceinline__ void st_tile8(uint8_t* tile, int row, int col, int rows,
                                          const float (&f)[8]) {
   *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =

@@ -101,7 +101,7 @@ static_assert(kOffAt + 4 * 16 * kLdB * 4 <= kOffKH + 40960, "inverse scratch fit
 // TMEM columns (512 allocated).
 constexpr uint32_t kColAP = 0;     // 160 fp32: AP;  W^T reuses columns 0..63
 constexpr uint32_t kColW = 0;
-constexpr uint32_t kColU = 160;    // 64 fp32: U0^T, then U^T
+constexpr uint32_t kColU = 160;    // 64 fp32: U0^T, then U^T; then bf16 U_lo^T (32)
 constexpr uint32_t kColO = 224;    // 64 fp32: O^T
 constexpr uint32_t kColS = 288;    // 128 fp32: S^T (lane j = value column, col = key row)
 constexpr uint32_t kColSB = 416;   // 64: bf16 S^T, A operand
@@ -257,25 +257,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       KDA_MARK(2);
       tc_fence_after();
       if (ok1) {
-        // U^T (fp32) -> bf16 A operand.
+        // U^T (fp32) -> bf16 A operands: U_hi to its own columns, U_lo over
+        // the first half of the fp32 U (read above), so U = U_hi + U_lo enters
+        // the fp32 state to about 2^-17 relative.  Where a write replaces an
+        // old value (beta = 1), U = v_new - v_old can be much larger than the
+        // state it leaves; one bf16 rounding of it would be an error on the
+        // scale of the old value.
+        // (Half h's U_lo lands on fp32 columns that half 0 has already read.)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
           tmem_ld32(tbase + lane_base + kColU + 32 * half, v);
           tmem_ld_wait();
-          uint32_t b[16];
+          uint32_t b[16], bl[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          for (int u = 0; u < 16; ++u) split_bf16x2(v[2 * u], v[2 * u + 1], b[u], bl[u]);
           tmem_st16(tbase + lane_base + kColUT + 16 * half, b);
+          tmem_st16(tbase + lane_base + kColU + 16 * half, bl);
         }
       }
       tmem_st_wait();
       tc_fence_before();
       named_bar(1, kStateThreads);
       if (j == 0 && ok1 && !s_abort) {
-        mbar_arrive(&s_bars[kBarUFree]);
         tc_fence_after();
-        // S^T += U^T Kbar (K = 64 tokens) ;  O^T += U^T P^T
+        // S^T += U_hi^T Kbar + U_lo^T Kbar (K = 2 x 64 tokens) ;  O^T += U_hi^T P^T
         const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
         const uint32_t bK = smem_u32(smem + kOffKB + s * 16384),
                        bP = smem_u32(smem + kOffP + s * 8192);
@@ -285,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_tmem_a(tbase + kColS, aU, umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
           umma_bf16_tmem_a(tbase + kColO, aU, umma_desc(bP + t * 32, 16, 1024), iO, 1);
         }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          umma_bf16_tmem_a(tbase + kColS, tbase + kColU + 8 * t,
+                           umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
         umma_commit(&s_bars[kBarEmpty0 + s]);
         umma_commit(&s_bars[kBarMMA2]);
       }
@@ -292,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok2 = sync.wait(kBarMMA2, c & 1);
       KDA_MARK(4);
       tc_fence_after();
+      // The U columns (U_lo) are read: the next chunk's U0^T may land there.
+      if (j == 0 && ok2) mbar_arrive(&s_bars[kBarUFree]);
       if (ok2) {
         // Prefix-cache checkpoint after this chunk (full chunks whose end is a
         // multiple of the checkpoint interval).

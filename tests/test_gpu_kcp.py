@@ -85,7 +85,9 @@ def _assert_scaled(got, ref, what):
     |x - ref| <= 2e-2 |ref| + 1e-2 max|ref|."""
     got, ref = to64(got), to64(ref)
     scale = float(np.abs(ref).max())
-    assert scale > 0.5, f"{what}: max|ref| = {scale:.3e}, the check would be vacuous"
+    # At the generator's decay max|M| falls below 1e-10; at this decay it is
+    # of order 0.1 - 1, so the scaled floor is a real bound.
+    assert scale > 0.05, f"{what}: max|ref| = {scale:.3e}, the check would be vacuous"
     err = np.abs(got - ref)
     excess = err - (2e-2 * np.abs(ref) + 1e-2 * scale)
     assert excess.max() <= 0, f"{what}: max |err| {err.max():.3e} (max|ref| {scale:.3e})"
