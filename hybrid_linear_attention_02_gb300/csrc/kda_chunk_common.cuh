@@ -84,6 +84,12 @@ struct Sync {
   __device__ __forceinline__ bool wait(int b, uint32_t parity) {
     return wait_for(b, parity, 2000000000ull);
   }
+  // As wait, called by all 32 lanes of a warp: the result is the same on
+  // every lane (one lane that gave up makes the warp give up), so it may
+  // guard warp-collective work (.sync.aligned TMEM loads, __syncwarp).
+  __device__ __forceinline__ bool wait_warp(int b, uint32_t parity) {
+    return __all_sync(0xFFFFFFFFu, wait_for(b, parity, 2000000000ull));
+  }
   // As wait, giving up after limit_ns of wall time (a compile-time constant
   // in the kernels, so it costs them no register).
   __device__ __forceinline__ bool wait_for(int b, uint32_t parity, uint64_t limit_ns) {

@@ -100,7 +100,7 @@ constexpr uint32_t kPOffN3 = kPOffN2 + 3 * 16 * kLdB * 4;  // N^3 16 x 20
 constexpr uint32_t kPOffAt = kPOffN3 + 16 * kLdB * 4;     // A_bb^T 4 x 16 x 20
 static_assert(kPOffAt + 4 * 16 * kLdB * 4 <= kPOffKH + 40960, "inverse scratch fits");
 constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W (lanes 0..63) reuses 0..127
-enum { kPBarAP = 0, kPBarW, kPBarRaw, kPNumBars };
+enum { kPBarAP = 0, kPBarW, kPBarRaw, kPBarDrain, kPNumBars };
 
 // ---------------------------------------------------------------- state kernel
 // Roles: warps 0..7 run the serial chain (U^T and S^T between fp32 in TMEM and
@@ -126,7 +126,7 @@ constexpr uint32_t kSSmem = kSTiles + 1024;
 constexpr uint32_t kSOffZ = kSTiles;           // gated variant: 2 gate tiles 64 x 128
 constexpr uint32_t kSSmemGated = kSTiles + 2 * 16384 + 1024;
 // TMEM columns (lane = value column j throughout).
-constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (column = key row)
+constexpr uint32_t kSColS = 0;     // 128 fp32: the chunk's Kbar^T U part of S^T (column = key row)
 constexpr uint32_t kSColO = 128;   // 2 x 64 fp32: O^T of a chunk, buffer = chunk parity
 constexpr uint32_t kSColU = 256;   // 64 fp32: U0^T, then U^T
 constexpr uint32_t kSColSB = 320;  // 64: bf16 S^T, A operand
@@ -134,7 +134,9 @@ constexpr uint32_t kSColUT = 384;  // 2 x 32: bf16 U^T = hi + lo, A operands
 constexpr uint32_t kSTmemCols = 512;
 // Mbarriers.  Counts: Full/Z* by transaction or one arrival; U, S, O, Drain
 // by one MMA commit; UT and SB by the eight chain warps (one arrival each);
-// OFree by the four output warps; ZReady by the gate warps.
+// Empty by one MMA commit and the eight chain warps (they read the record's
+// e^{G_C}); OFree by the four output warps; ZReady by the gate warps.
+constexpr int kSPrefetch = 3;      // records (and v tiles) pulled into L2 this many chunks ahead
 enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarU, kSBarUT, kSBarS, kSBarSB,
        kSBarO0, kSBarO1, kSBarOFree0, kSBarOFree1, kSBarZFull0, kSBarZFull1, kSBarZEmpty0,
        kSBarZEmpty1, kSBarZReady0, kSBarZReady1, kSBarDrain, kSNumBars };
@@ -312,12 +314,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
   };
 
   Item cur = decode_item(args, win, s_cum, it0);
+  int last_raw = -1;   // loader: the last raw-tile phase it issued copies for
   if (loader) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_g);
     issue_raw_kq(cur);
     issue_raw_g(cur);
+    last_raw = 0;
   }
   load_beta(cur);
 
@@ -337,12 +341,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
     Item nxt = cur;
     if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
 
+    // beta of this item: every reader of the previous item's (P4 and the
+    // inverse) has passed the inverse's last barrier, and the readers of
+    // this one come after the P1 barrier below.
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
-    named_bar(2, kPThreads);
     KDA_SMARK(0);
-    const bool ok_raw = sync.wait(kPBarRaw, par);
+    const bool ok_raw = sync.wait_warp(kPBarRaw, par);
     KDA_SMARK(1);
 
     uint4 rq[4], rk[4];
@@ -415,7 +421,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
     named_bar(2, kPThreads);
     KDA_SMARK(3);
 
-    // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
+    // ---- P2: scaled operand tiles.  The masked-product MMA's operands
+    // ([K';Q'] and Khat) are stored first; Ktil and the record's Qtil and
+    // Kbar are held in registers and stored while that MMA runs.
+    uint32_t hold_kt[4][4], hold_qt[4][4], hold_kb[4][4];
     {
       const int sc0 = 4 * cg;
       auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const int r = row0 + m, rl = 4 * r4 + m;
         const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
         const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
-        uint32_t okp[4], oqp[4], okt[4], okh[4], oqt[4], okb[4];
+        uint32_t okp[4], oqp[4], okh[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
@@ -449,18 +458,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const uint64_t k1 = f2_mul(kp, e1), q1 = f2_mul(qp, e1);
           okp[w] = f2_to_bf16x2(k1);
           oqp[w] = f2_to_bf16x2(q1);
-          okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
-          oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
+          hold_kt[m][w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
+          hold_qt[m][w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
           kh[w] = f2_mul(kp, ei);
           okh[w] = f2_to_bf16x2(kh[w]);
-          okb[w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
+          hold_kb[m][w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
         }
         st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
         st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
-        st4(smem + kPOffKT, r, 64, okt);
         st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
-        st4(rec + kRecWQ, r, 128, oqt);
-        st4(rec + kRecKB, r, 64, okb);
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int a2 = ta + 1 + i;
@@ -491,11 +497,39 @@ __global__ void __launch_bounds__(kPThreads, 2)
                   umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarAP]);
     }
+    // While it runs: Ktil (the W product's operand, read after later
+    // barriers and a proxy fence) and the record's Qtil and Kbar.
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int r = row0 + m;
+      *reinterpret_cast<uint4*>(smem + kPOffKT + sw128_off(r, 8 * cg, 64)) =
+          make_uint4(hold_kt[m][0], hold_kt[m][1], hold_kt[m][2], hold_kt[m][3]);
+      *reinterpret_cast<uint4*>(rec + kRecWQ + sw128_off(r, 8 * cg, 128)) =
+          make_uint4(hold_qt[m][0], hold_qt[m][1], hold_qt[m][2], hold_qt[m][3]);
+      *reinterpret_cast<uint4*>(rec + kRecKB + sw128_off(r, 8 * cg, 64)) =
+          make_uint4(hold_kb[m][0], hold_kb[m][1], hold_kb[m][2], hold_kb[m][3]);
+    }
     if (it_next < it_end) load_beta(nxt);
-    const bool ok_ap = sync.wait(kPBarAP, par);
+    const bool ok_ap = sync.wait_warp(kPBarAP, par);
     tc_fence_after();
     // [K';Q'] is dead: the next item's raw k and q may land.
-    if (loader && ok_ap && it_next < it_end) issue_raw_kq(nxt);
+    if (loader && ok_ap && it_next < it_end) {
+      issue_raw_kq(nxt);
+      last_raw = static_cast<int>(k_iter) + 1;
+      // The item after next: its raw tiles to L2 now, so their copies into
+      // shared memory (one item from now) wait on L2 rather than DRAM.
+      const int it_nn = it_next + it_step;
+      if (it_nn < it_end) {
+        const Item x = decode_item(args, win, s_cum, it_nn);
+        const int cx = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_prefetch_3d(&tm_k, 64 * hf, x.h, cx);
+          tma_prefetch_3d(&tm_q, 64 * hf, x.h, cx);
+          tma_prefetch_3d(&tm_g, 64 * hf, x.h, cx);
+        }
+      }
+    }
     KDA_SMARK(5);
 
     // ---- P4: A (x beta, strictly lower; fp32, shared) and P (lower inclusive;
@@ -734,7 +768,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
                   umma_desc(bKT + t * 2048, 64 * 128, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarW]);
     }
-    const bool ok_w = sync.wait(kPBarW, par);
+    const bool ok_w = sync.wait_warp(kPBarW, par);
     tc_fence_after();
     KDA_SMARK(12);
 
@@ -770,6 +804,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
   }
 #endif
   if (leader) bulk_wait_all();
+  // After an abort: raw-tile copies nobody waited for and MMAs whose commit
+  // nobody waited for land before the block frees its memory (bounded).
+  if (s_abort) {
+    if (loader && last_raw >= 0) mbar_wait(&s_bars[kPBarRaw], last_raw & 1, 100000000ull);
+    if (leader) {
+      umma_commit(&s_bars[kPBarDrain]);
+      mbar_wait(&s_bars[kPBarDrain], 0, 100000000ull);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (s_abort && p == 0 && args.dev_status) atomicExch(args.dev_status, KDA_ERR_TIMEOUT);
@@ -784,12 +827,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
 // Per chunk c (record slot s = c & 1, O buffer b = c & 1):
 //   MMA warp:  U^T += S^T (-W)^T            (N = 64, onto U0^T; commit U)
 //              O_b^T = S^T Qtil^T           (N = 64, once O_b is free)
-//              S^T += [U_hi^T | U_lo^T] [Kbar; Kbar]
+//              D^T = [U_hi^T | U_lo^T] [Kbar; Kbar]
 //                                           (N = 128, K = 2 x 64; commit S)
 //              O_b^T += U_hi^T P^T          (N = 64; commit O_b, slot s free)
 //              U0^T = V^T T'^T of chunk c + 1 into the U columns
-//   chain:     U^T -> bf16 hi + lo (arrive UT); S^T -> bf16 (arrive SB);
-//              then, off the chain, S <- Diag(e^{G_C}) S for chunk c + 1
+//   chain:     U^T -> bf16 hi + lo (arrive UT);
+//              S^T <- Diag(e^{G_C}) S^T + D^T in registers, its bf16 copy
+//              to TMEM (arrive SB)
+// The fp32 state lives in the chain warps' registers (64 values a thread),
+// so the decay is one FMA per element in the pass that makes the bf16 copy.
 // U enters the fp32 state as two bf16 parts (U = U_hi + U_lo to about 2^-17
 // relative), so the state's update carries no bf16 rounding of U itself:
 // where a write replaces an old value (beta = 1), U = v_new - v_old can be
@@ -856,6 +902,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
   if (tid == 0) {
     for (int b = 0; b < kSNumBars; ++b) {
       const uint32_t cnt = (b == kSBarUT || b == kSBarSB)             ? kSChainWarps
+                           : (b == kSBarEmpty0 || b == kSBarEmpty1)   ? kSChainWarps + 1
                            : (b == kSBarOFree0 || b == kSBarOFree1)   ? kSOutWarps
                            : (b == kSBarZReady0 || b == kSBarZReady1) ? kSGateWarps
                                                                       : 1;
@@ -888,7 +935,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < nck; ++c) {
         const int zs = c & 1;
-        if (!sync.wait(kSBarZFull0 + zs, (c >> 1) & 1)) break;
+        if (!sync.wait_warp(kSBarZFull0 + zs, (c >> 1) & 1)) break;
         uint8_t* zt = smem + kSOffZ + zs * 16384;
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
@@ -914,9 +961,21 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_v);
       int last[2] = {-1, -1}, zlast[2] = {-1, -1};   // last chunk loaded into each slot
+      // Records and v tiles of chunk c go to L2 a few chunks before their
+      // copies into shared memory, so those copies wait on L2, not on DRAM.
+      auto prefetch = [&](int c) {
+        bulk_prefetch_l2(win.rec + static_cast<size_t>(rbase + c) * kRecBytes, kRecBytes);
+        if (!vzero) {
+          const int c0 = static_cast<int>(t0 + static_cast<long long>(win.cw0 + c) * kC);
+          tma_prefetch_3d(&tm_v, 0, h, c0);
+          tma_prefetch_3d(&tm_v, 64, h, c0);
+        }
+      };
+      for (int c = 0; c < kSPrefetch && c < nck; ++c) prefetch(c);
 #pragma unroll 1
       for (int c = 0; c < nck; ++c) {
         const int s = c & 1;
+        if (c + kSPrefetch < nck) prefetch(c + kSPrefetch);
         if (c >= 2 && !sync.wait(kSBarEmpty0 + s, ((c - 2) >> 1) & 1)) break;
         uint64_t* bar = &s_bars[kSBarFull0 + s];
         mbar_arrive_expect_tx(bar, kRecBytes + (vzero ? 0 : 16384));
@@ -979,6 +1038,9 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         const int s = c & 1, ob = c & 1;
         const uint8_t* slot = smem + kSOffRec + s * kRecSlot;
         const uint32_t bWQ = smem_u32(slot + kRecWQ);
+        // The chunk's record is in its slot (already waited for with U0^T
+        // unless v = 0), and the state's bf16 copy is written.
+        if (!sync.wait(kSBarFull0 + s, (c >> 1) & 1)) break;
         if (!sync.wait(kSBarSB, c & 1)) break;
         tc_fence_after();
         // U^T (+)= S^T (-W)^T: rows 64..127 of the [Qtil; -W] image (K = dk = 128).
@@ -998,8 +1060,8 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
                              umma_desc(bWQ + (t >> 2) * 16384 + (t & 3) * 32, 16, 1024), i64,
                              t > 0);
         }
-        // S^T += U_hi^T Kbar + U_lo^T Kbar (M = 128, N = 128, K = 2 x 64
-        // tokens; Kbar MN-major, read twice).
+        // D^T = U_hi^T Kbar + U_lo^T Kbar (M = 128, N = 128, K = 2 x 64
+        // tokens; Kbar MN-major, read twice; the chain adds it to the state).
         if (!sync.wait(kSBarUT, c & 1)) break;
         tc_fence_after();
         {
@@ -1007,7 +1069,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
 #pragma unroll
           for (int t = 0; t < 8; ++t)
             umma_bf16_tmem_a(tbase + kSColS, tbase + kSColUT + 8 * t,
-                             umma_desc(bKB + (t & 3) * 2048, 64 * 128, 1024), i128mn, 1);
+                             umma_desc(bKB + (t & 3) * 2048, 64 * 128, 1024), i128mn, t > 0);
           umma_commit(&s_bars[kSBarS]);
         }
         if (outputs) {
@@ -1038,7 +1100,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     const int q = warp & 3, hf = warp >> 2;
     const int j = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    float sv[64];   // S^T[j][64 hf + u]: this thread's part of the state
+    float sv[64];   // S^T[j][64 hf + u]: this thread's part of the fp32 state
     auto pack_sb = [&]() {
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -1048,35 +1110,18 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         tmem_st16(tbase + lane_base + kSColSB + 32 * hf + 16 * h2, b);
       }
     };
-    auto store_decayed = [&](const float* gam) {
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t f[32];
-#pragma unroll
-        for (int u = 0; u < 32; u += 4) {
-          const float4 gm = *reinterpret_cast<const float4*>(&gam[64 * hf + 32 * h2 + u]);
-          f[u] = __float_as_uint(sv[32 * h2 + u] * gm.x);
-          f[u + 1] = __float_as_uint(sv[32 * h2 + u + 1] * gm.y);
-          f[u + 2] = __float_as_uint(sv[32 * h2 + u + 2] * gm.z);
-          f[u + 3] = __float_as_uint(sv[32 * h2 + u + 3] * gm.w);
-        }
-        tmem_st32(tbase + lane_base + kSColS + 64 * hf + 32 * h2, f);
-      }
-    };
-    // The entering state: bf16 copy as it is, fp32 copy with the first
-    // chunk's decay Diag(e^{G_C}) (MMA2 adds onto the decayed state).
+    // The entering state and its bf16 copy.
 #pragma unroll
     for (int u = 0; u < 64; ++u) {
       const int c = 64 * hf + u;
       sv[u] = src ? __ldcs(src + soff + c * kD + j) : (src_identity && c == j ? 1.f : 0.f);
     }
     pack_sb();
-    bool ok = sync.wait(kSBarFull0, 0);
-    if (ok) store_decayed(reinterpret_cast<const float*>(smem + kSOffRec + kRecG));
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0 && ok) mbar_arrive(&s_bars[kSBarSB]);
+    if (lane == 0) mbar_arrive(&s_bars[kSBarSB]);
+    bool ok = true;
 
 #ifdef KDA_PHASE_PROFILE
     unsigned long long prof_acc[10] = {}, prof_t = clock64();
@@ -1085,7 +1130,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
       // U^T (fp32, U0^T included by the MMA) -> bf16 A operands hi and lo.
-      const bool ok1 = ok && sync.wait(kSBarU, c & 1);
+      const bool ok1 = ok && sync.wait_warp(kSBarU, c & 1);
       KDA_SMARK(0);
       tc_fence_after();
       if (ok1) {
@@ -1098,34 +1143,48 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         tmem_st16(tbase + lane_base + kSColUT + 16 * hf, b);
         tmem_st16(tbase + lane_base + kSColUT + 32 + 16 * hf, bl);
       }
-      tmem_st_wait();   // also the decayed state stored after the previous chunk
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
       KDA_SMARK(1);
-      // The new state: its bf16 copy for the next chunk's first product.
+      // The new state S_C = Diag(e^{G_C}) S_0 + Kbar^T U, and its bf16 copy
+      // for the next chunk's first product.
       const bool has_next = c + 1 < nck;
-      const bool ok_next = !has_next || sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1);
-      KDA_SMARK(2);
-      const bool ok2 = ok1 && sync.wait(kSBarS, c & 1);
+      // (The record's arrival is also waited for here, so that this warp
+      // sees its e^{G_C}; the phase completed before the products began.)
+      const bool ok2 = ok1 && sync.wait_warp(kSBarFull0 + s, (c >> 1) & 1) &&
+                       sync.wait_warp(kSBarS, c & 1);
       KDA_SMARK(3);
       tc_fence_after();
       if (ok2) {
-        float* sp = sv;
-        tmem_ld32(tbase + lane_base + kSColS + 64 * hf, *reinterpret_cast<float(*)[32]>(sp));
-        tmem_ld32(tbase + lane_base + kSColS + 64 * hf + 32,
-                  *reinterpret_cast<float(*)[32]>(sp + 32));
-        tmem_ld_wait();
-        pack_sb();
+        const float* gam =
+            reinterpret_cast<const float*>(smem + kSOffRec + s * kRecSlot + kRecG) + 64 * hf;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float d[32];
+          tmem_ld32(tbase + lane_base + kSColS + 64 * hf + 32 * h2, d);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 32; u += 4) {
+            const float4 gm = *reinterpret_cast<const float4*>(&gam[32 * h2 + u]);
+            sv[32 * h2 + u] = fmaf(gm.x, sv[32 * h2 + u], d[u]);
+            sv[32 * h2 + u + 1] = fmaf(gm.y, sv[32 * h2 + u + 1], d[u + 1]);
+            sv[32 * h2 + u + 2] = fmaf(gm.z, sv[32 * h2 + u + 2], d[u + 2]);
+            sv[32 * h2 + u + 3] = fmaf(gm.w, sv[32 * h2 + u + 3], d[u + 3]);
+          }
+        }
+        if (has_next) pack_sb();
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && ok2 && ok_next && has_next) mbar_arrive(&s_bars[kSBarSB]);
+      if (lane == 0) {
+        if (ok2 && has_next) mbar_arrive(&s_bars[kSBarSB]);
+        if (ok2) mbar_arrive(&s_bars[kSBarEmpty0 + s]);   // e^{G_C} of slot s is read
+      }
       KDA_SMARK(4);
-      // Off the chain: prefix-cache checkpoint, then the next chunk's decay
-      // (stored while its first product runs; the next U^T hand-off waits
-      // for the stores).
+      // Off the chain: prefix-cache checkpoint.
       if (ok2) {
         const long long done = static_cast<long long>(win.cw0 + c + 1) * kC;
         if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
@@ -1134,11 +1193,8 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
 #pragma unroll
           for (int u = 0; u < 64; ++u) __stcs(ck + (64 * hf + u) * kD, sv[u]);
         }
-        if (has_next && ok_next)
-          store_decayed(reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot +
-                                                       kRecG));
       }
-      ok = ok2 && ok_next;
+      ok = ok2;
       KDA_SMARK(5);
     }
 #ifdef KDA_PHASE_PROFILE
@@ -1147,7 +1203,6 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       if (tid == 0) kda_split_clocks[30] = nck;
     }
 #endif
-    tmem_st_wait();
     // After the last chunk the state carries no further decay.
     if (!s_abort && ok && dst) {
 #pragma unroll
@@ -1172,7 +1227,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       const int ob = c & 1;
       const long long c0 = t0 + static_cast<long long>(win.cw0 + c) * kC;
       const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
-      bool live = sync.wait(kSBarO0 + ob, (c >> 1) & 1);
+      bool live = sync.wait_warp(kSBarO0 + ob, (c >> 1) & 1);
       tc_fence_after();
       uint32_t pk[32];
       if (live) {
@@ -1203,7 +1258,7 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       named_bar(1, kSOutThreads);
       if constexpr (kGate) {
         // The gate tile holds w * sigmoid(z) once the gate warps are done with it.
-        if (!sync.wait(kSBarZReady0 + ob, (c >> 1) & 1)) live = false;
+        if (!sync.wait_warp(kSBarZReady0 + ob, (c >> 1) & 1)) live = false;
         const uint8_t* zt = smem + kSOffZ + ob * 16384;
         const int sg = ot & 7;
 #pragma unroll 1

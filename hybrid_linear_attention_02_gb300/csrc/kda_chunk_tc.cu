@@ -109,7 +109,7 @@ constexpr uint32_t kColUT = 480;   // 32: bf16 U^T, A operand
 constexpr uint32_t kTmemCols = 512;
 
 enum { kBarAP = 0, kBarWU, kBarFull0, kBarFull1, kBarEmpty0, kBarEmpty1, kBarMMA1, kBarUFree,
-       kBarMMA2, kBarRaw, kBarRawV, kNumBars };
+       kBarMMA2, kBarRaw, kBarRawV, kBarDrainS, kBarDrainP, kNumBars };
 
 #ifdef KDA_PHASE_PROFILE
 __device__ unsigned long long kda_phase_clocks[32];
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
-      const bool ok_full = sync.wait(kBarFull0 + s, (c >> 1) & 1);
+      const bool ok_full = sync.wait_warp(kBarFull0 + s, (c >> 1) & 1);
       KDA_MARK(0);
       tc_fence_after();
       if (j == 0 && ok_full) {
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tbase + lane_base + kColS + 16 * cb, f);
         }
       }
-      const bool ok1 = sync.wait(kBarMMA1, c & 1);
+      const bool ok1 = sync.wait_warp(kBarMMA1, c & 1);
       KDA_MARK(2);
       tc_fence_after();
       if (ok1) {
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s_bars[kBarMMA2]);
       }
       KDA_MARK(3);
-      const bool ok2 = sync.wait(kBarMMA2, c & 1);
+      const bool ok2 = sync.wait_warp(kBarMMA2, c & 1);
       KDA_MARK(4);
       tc_fence_after();
       // The U columns (U_lo) are read: the next chunk's U0^T may land there.
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kda_phase_clocks[28] = n_chunks;
     }
 #endif
-    if (!s_abort && args.final_state) {
+    if (__all_sync(0xFFFFFFFFu, !s_abort) && args.final_state) {
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         float v[32];
@@ -360,6 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) __stcs(args.final_state + soff + (32 * cb + u) * kD + j, v[u]);
       }
+    }
+    // After an abort, MMAs whose commit nobody waited for complete before
+    // the block frees its TMEM (bounded).
+    if (s_abort && j == 0) {
+      umma_commit(&s_bars[kBarDrainS]);
+      mbar_wait(&s_bars[kBarDrainS], 0, 100000000ull);
     }
   } else {
     // ================================== prep ==================================
@@ -419,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rb[m] = (cg == 0 && r < L) ? __bfloat162float(gb[(c0 + r) * H + h]) : 0.f;
       }
     };
+    int last_raw = -1, last_rawv = -1;   // loader: last chunk its raw copies were issued for
     if (n_chunks > 0) {
       if (loader) {
         prefetch_tmap(&tm_q);
@@ -427,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_g);
         issue_raw(0);
         issue_raw_v(0);
+        last_raw = last_rawv = 0;
       }
       load_beta(0);
     }
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int m = 0; m < 4; ++m)
         if (cg == 0) s_beta[row0 + m] = rb[m];
       if (c + 1 < n_chunks) load_beta(c + 1);
-      const bool ok_raw = sync.wait(kBarRaw, c & 1);
+      const bool ok_raw = sync.wait_warp(kBarRaw, c & 1);
       KDA_MARK(8);
       // Raw rows of this chunk (rows past the end of the sequence read as 0).
       uint4 rq[4], rk[4];
@@ -604,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
         umma_commit(&s_bars[kBarAP]);
       }
-      const bool ok_ap = sync.wait(kBarAP, c & 1);
+      const bool ok_ap = sync.wait_warp(kBarAP, c & 1);
       KDA_MARK(10);
       tc_fence_after();
       // Prefetch the next chunk's raw k, q, g: AP has read [K';Q'], and the
@@ -612,7 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // c - 1 has finished its last MMA.
       if (loader && c + 1 < n_chunks && ok_ap) {
         const bool ok_e = c < 1 || sync.wait(kBarEmpty0 + ((c + 1) & 1), ((c - 1) >> 1) & 1);
-        if (ok_e) issue_raw(c + 1);
+        if (ok_e) {
+          issue_raw(c + 1);
+          last_raw = c + 1;
+        }
       }
 
       // ---- P4: A (x beta, strictly lower; fp32) and P (lower inclusive; bf16).
@@ -832,8 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       KDA_MARK(12);
       // ---- P6: W^T = Ktil^T T'^T and U0^T = V^T T'^T (U0 goes where the state
       // pass accumulates U, once it has read the previous chunk's U).
-      const bool ok_u = c < 1 || sync.wait(kBarUFree, (c - 1) & 1);
-      const bool ok_v = sync.wait(kBarRawV, c & 1);
+      const bool ok_u = c < 1 || sync.wait_warp(kBarUFree, (c - 1) & 1);
+      const bool ok_v = sync.wait_warp(kBarRawV, c & 1);
       if (leader && ok_u && ok_v && !s_abort) {
         tc_fence_after();
         const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
@@ -847,12 +858,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&s_bars[kBarWU]);
       }
-      const bool ok_wu = sync.wait(kBarWU, c & 1);
+      const bool ok_wu = sync.wait_warp(kBarWU, c & 1);
       // The V tile is free: fetch the next chunk's v.
-      if (loader && c + 1 < n_chunks && ok_wu) issue_raw_v(c + 1);
+      if (loader && c + 1 < n_chunks && ok_wu) {
+        issue_raw_v(c + 1);
+        last_rawv = c + 1;
+      }
       // -W^T may overwrite the shared tile once the state pass's first MMA of
       // the previous chunk is done.
-      const bool ok_m1 = c < 1 || sync.wait(kBarMMA1, (c - 1) & 1);
+      const bool ok_m1 = c < 1 || sync.wait_warp(kBarMMA1, (c - 1) & 1);
       KDA_MARK(13);
       tc_fence_after();
 
@@ -884,6 +898,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 8; i < 24; ++i) kda_phase_clocks[i] = prof_acc[i];
     if (blockIdx.x == 0 && blockIdx.y == 0 && p == 0) kda_phase_clocks[28] = n_chunks;
 #endif
+    // After an abort: raw copies nobody waited for, and MMAs whose commit
+    // nobody waited for, land before the block frees its memory (bounded).
+    if (s_abort) {
+      if (loader && last_raw >= 0) mbar_wait(&s_bars[kBarRaw], last_raw & 1, 100000000ull);
+      if (loader && last_rawv >= 0) mbar_wait(&s_bars[kBarRawV], last_rawv & 1, 100000000ull);
+      if (leader) {
+        umma_commit(&s_bars[kBarDrainP]);
+        mbar_wait(&s_bars[kBarDrainP], 0, 100000000ull);
+      }
+    }
   }
 
   tc_fence_before();

@@ -133,3 +133,19 @@ def test_kcp_prefill_at_slow_decay_matches_oracle(segments):
     eo = assert_close(out, ro, "bf16", "kcp slow-decay out")
     ef = assert_close(fin, rf, "bf16", "kcp slow-decay final_state")
     print(f"kcp {segments} segments, slow decay: out err {eo:.3e}, final err {ef:.3e}")
+
+
+def test_transitions_full_headline_size_sampled():
+    """One 8192-token sequence x 96 heads (the launch configuration the bench's
+    transition leg times: 192 state CTAs for the M and H maps, more than the
+    SMs hold at once): two heads' maps against the oracle."""
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=56, device=DEV)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    M, Hs = kda.chunk_transition(*x, d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(M).all() and torch.isfinite(Hs).all()
+    heads = [7, 90]
+    hs = torch.tensor(heads, device=DEV)
+    rM, rH = _oracle_transition([t[:, hs] for t in x], d["cu_seqlens"])
+    assert_close(M[:, hs], rM, "bf16", "M (8192 tokens)")
+    assert_close(Hs[:, hs], rH, "bf16", "H (8192 tokens)")
