@@ -116,6 +116,9 @@ def _declare(lib):
     lib.kda_prologue.restype = ip
     lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
     lib.kda_chunk_fwd_algorithm.restype = ip
+    lib.kda_debug_chunk_fwd_withhold.argtypes = [ip, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp, sz,
+                                                 vp, vp]
+    lib.kda_debug_chunk_fwd_withhold.restype = ip
     lib.kda_check_inputs.argtypes = [vp, vp, dp, vp, vp]
     lib.kda_check_inputs.restype = ip
     lib.kda_debug_bounds_build.restype = ip
@@ -358,6 +361,33 @@ def check_inputs(g, beta, dev_status, *, stream=None, lib=None):
                                   _stream_handle(stream))
     if rc != 0:
         raise KDAError(rc, "kda_check_inputs")
+
+
+def debug_chunk_fwd_withhold(which: int, q, k, v, g, beta, init_state, dev_status, *,
+                             stream=None):
+    """Failure-detection self-test of the prefill kernels
+    (``kda_debug_chunk_fwd_withhold``): one copy is never issued (which = 1:
+    the split state kernel's first record; 2: the split preparation kernel's
+    first raw tiles; 3: the fused kernel's first raw tiles), so a production
+    kernel's bounded wait expires and it reports KDA_ERR_TIMEOUT through
+    dev_status.  One sequence; returns the (meaningless) outputs."""
+    lib = load()
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    fin = torch.empty((1, H, dk, dv), dtype=torch.float32, device=dev)
+    d = _dims(1, T, H, dk, dv, dt)
+    need = int(lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), 64))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.kda_debug_chunk_fwd_withhold(int(which), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                              _ptr(beta), _ptr(init_state), _ptr(out), _ptr(fin),
+                                              ctypes.byref(d), _ptr(ws), need, _ptr(dev_status),
+                                              _stream_handle(stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_debug_chunk_fwd_withhold")
+    return out, fin
 
 
 def debug_wait_timeout(dev_status, timeout_us: int, *, stream=None):

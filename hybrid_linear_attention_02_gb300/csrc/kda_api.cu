@@ -165,6 +165,7 @@ struct Extras {
   const void* gate = nullptr;
   const float* gate_w = nullptr;
   float gate_eps = 0.f;
+  int withhold = 0;   // failure-detection self-test (see LaunchArgs::debug_withhold)
 };
 
 int check_gate(const void* gate, const float* gate_w, float eps) {
@@ -222,6 +223,7 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
   a.gate = x.gate;
   a.gate_w = x.gate_w;
   a.gate_eps = x.gate_eps;
+  a.debug_withhold = x.withhold;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 #ifdef KDA_DEBUG_BOUNDS
@@ -237,13 +239,19 @@ int chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, c
     a.order = order;
   }
   cudaError_t e;
-  const Path path = choose_path(dims, chunk);
+  Path path = choose_path(dims, chunk);
+  if (x.withhold) {
+    if (path == Path::kRecurrent) return KDA_ERR_UNSUPPORTED;
+    path = x.withhold == 3 ? Path::kFused : Path::kSplit;
+  }
   // The split form needs room for at least one record per pair after the
   // order array and the carried states; less room than the full size only
   // means more (smaller) windows.
   const size_t split_min = need + split_state_bytes(dims) +
                            static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;
   bool gate_done = path == Path::kRecurrent;   // the recurrence applies the epilogue itself
+  if (x.withhold && path == Path::kSplit && !(workspace && workspace_bytes >= split_min))
+    return KDA_ERR_WORKSPACE;
   if (path == Path::kSplit && workspace && workspace_bytes >= split_min) {
     gate_done = true;                          // so does the split form's state kernel
     uint8_t* ws = static_cast<uint8_t*>(workspace) + need;
@@ -493,6 +501,18 @@ int kda_prologue(const void* q_pre, const void* k_pre, const void* z, const floa
   return kda::launch_prologue(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KDA_OK
              : KDA_ERR_CUDA;
+}
+
+int kda_debug_chunk_fwd_withhold(int which, const void* q, const void* k, const void* v,
+                                 const void* g, const void* beta, const float* init_state,
+                                 void* out, float* final_state, const kda_dims* dims,
+                                 void* workspace, size_t workspace_bytes, int* dev_status,
+                                 void* stream) {
+  if (which < 1 || which > 3 || !dev_status) return KDA_ERR_INVALID;
+  Extras x;
+  x.withhold = which;
+  return chunk_fwd_impl(q, k, v, g, beta, init_state, nullptr, out, final_state, 64, dims,
+                        workspace, workspace_bytes, dev_status, stream, x);
 }
 
 int kda_check_inputs(const void* g, const void* beta, const kda_dims* dims, int* dev_status,

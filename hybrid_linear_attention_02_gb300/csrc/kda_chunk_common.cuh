@@ -63,18 +63,25 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), for a pair (x0, x1),
-// packed low half first: x is carried to about 2^-17 relative.
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack2(x0, x1);
-  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
-  lo = pack2(x0 - h0, x1 - h1);
+// (lo, hi) rounded to fp16 (nearest even, saturating at +-65504), packed
+// low half first.
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ void st_tile8(uint8_t* tile, int row, int col, int rows,
                                          const float (&f)[8]) {
   *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
       make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+__device__ __forceinline__ void st_tile8_f16(uint8_t* tile, int row, int col, int rows,
+                                             const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, col, rows)) =
+      make_uint4(pack2_f16(f[0], f[1]), pack2_f16(f[2], f[3]), pack2_f16(f[4], f[5]),
+                 pack2_f16(f[6], f[7]));
 }
 
 // Shared by all roles: a wait that also gives up once any thread has given up.

@@ -26,7 +26,7 @@
 //    resident in TMEM and the bf16 operands:
 //      U0^T = V^T T'^T                                     (MMA0, off the chain)
 //      [O^T | U^T] = S^T [Qtil; -W]^T,  U^T += U0^T         (MMA1, N = 128)
-//      S^T += U^T Kbar,  O^T += U^T P^T                      (MMA2, N = 128 + 64)
+//      S^T += U^T Kbar,  O^T += U^T P^T                      (MMA2, N = 128 + 64, fp16)
 //    The serial chain per chunk is MMA1 -> U^T to bf16 -> MMA2 -> S^T to
 //    bf16 (with the next chunk's decay Diag(e^{G_C}) applied to the fp32
 //    copy in the same pass); the previous chunk's output stores run while
@@ -58,9 +58,14 @@ using namespace chunk;
 // KB: Kbar, one row per token: an MN-major B operand (N = 128 key channels
 //     in two 64-channel panels, K = 64 tokens).
 // P:  K-major B operand, 64 rows (one per output token) by K = 64 tokens.
+// WQ and T' are bf16.  Kbar and P are fp16, like the U^T they multiply: the
+// state update S += Kbar^T U carries U = v_new - v_old where a write replaces
+// an old value (beta = 1), which can be far larger than the state it leaves;
+// fp16's 10-bit mantissa keeps that update's rounding 8x below bf16's, at no
+// extra MMA.  All three are bounded by 1 except U (saturated at +-65504).
 constexpr uint32_t kRecWQ = 0;       // [Qtil; -W]        128 x 128
-constexpr uint32_t kRecKB = 32768;   // Kbar              64 x 128
-constexpr uint32_t kRecP = 49152;    // P                 64 x 64
+constexpr uint32_t kRecKB = 32768;   // Kbar (fp16)       64 x 128
+constexpr uint32_t kRecP = 49152;    // P (fp16)          64 x 64
 constexpr uint32_t kRecT = 57344;    // T' = T diag(beta) 64 x 64  (K-major B)
 constexpr uint32_t kRecG = 65536;    // e^{G_C}, fp32 [128]
 constexpr uint32_t kRecBytes = 66048;
@@ -103,21 +108,14 @@ constexpr uint32_t kPTmemCols = 256;   // AP: 160 fp32 columns; W (lanes 0..63) 
 enum { kPBarAP = 0, kPBarW, kPBarRaw, kPBarDrain, kPNumBars };
 
 // ---------------------------------------------------------------- state kernel
-// Roles: warps 0..7 run the serial chain (U^T and S^T between fp32 in TMEM and
-// their bf16 A-operand copies, two warps per TMEM lane quarter, each on half
-// the columns); warp 8 streams records and v tiles; warp 9 issues every MMA;
-// warps 10..13 take each chunk's outputs out of TMEM and store them; in the
-// gated variant warps 14, 15 turn the gate tiles into w * sigmoid(z).
-constexpr int kSChainWarps = 8;
-constexpr int kSProducerWarp = 8;
-constexpr int kSMmaWarp = 9;
-constexpr int kSOutWarp = 10;
-constexpr int kSOutWarps = 4;
-constexpr int kSOutThreads = 32 * kSOutWarps;
-constexpr int kSThreads = 32 * (kSOutWarp + kSOutWarps);
-constexpr int kSGateWarp = kSOutWarp + kSOutWarps;
-constexpr int kSGateWarps = 2;             // gate tiles, 32 rows each
-constexpr int kSThreadsGated = kSThreads + 32 * kSGateWarps;
+constexpr int kSStateWarps = 8;            // warps 0..7: state pass (TMEM <-> registers)
+constexpr int kSStateThreads = 32 * kSStateWarps;
+constexpr int kSProducerWarp = 8;          // records and v tiles into the ring
+constexpr int kSMmaWarp = 9;               // issues every MMA
+constexpr int kSThreads = 32 * 10;
+constexpr int kSGateWarp = 10;             // gated variant: warps 10, 11 make the gate
+constexpr int kSGateWarps = 2;             // tiles w * sigmoid(z), 32 rows each
+constexpr int kSThreadsGated = 32 * (10 + kSGateWarps);
 constexpr uint32_t kSOffRec = 0;           // 2 record slots
 constexpr uint32_t kSOffV = 2 * kRecSlot;  // 2 v tiles 64 x 128
 constexpr uint32_t kSOffO = kSOffV + 2 * 16384;  // O staging 64 x 128 (TMA store image)
@@ -125,21 +123,16 @@ constexpr uint32_t kSTiles = kSOffO + 16384;
 constexpr uint32_t kSSmem = kSTiles + 1024;
 constexpr uint32_t kSOffZ = kSTiles;           // gated variant: 2 gate tiles 64 x 128
 constexpr uint32_t kSSmemGated = kSTiles + 2 * 16384 + 1024;
-// TMEM columns (lane = value column j throughout).
-constexpr uint32_t kSColS = 0;     // 128 fp32: the chunk's Kbar^T U part of S^T (column = key row)
-constexpr uint32_t kSColO = 128;   // 2 x 64 fp32: O^T of a chunk, buffer = chunk parity
-constexpr uint32_t kSColU = 256;   // 64 fp32: U0^T, then U^T
-constexpr uint32_t kSColSB = 320;  // 64: bf16 S^T, A operand
-constexpr uint32_t kSColUT = 384;  // 2 x 32: bf16 U^T = hi + lo, A operands
+constexpr uint32_t kSColS = 0;     // 128 fp32: S^T (lane = value column, column = key row)
+constexpr uint32_t kSColO = 128;   // 64 fp32: O^T  (MMA2 writes [S^T | O^T])
+constexpr uint32_t kSColU = 192;   // 64 fp32: U^T  (MMA1 writes [O^T | U^T])
+constexpr uint32_t kSColSB = 256;  // 64: bf16 S^T, A operand
+constexpr uint32_t kSColUT = 320;  // 32: fp16 U^T, A operand
+constexpr uint32_t kSColU0 = 352;  // 2 x 64 fp32: U0^T = V^T T'^T, by chunk parity
 constexpr uint32_t kSTmemCols = 512;
-// Mbarriers.  Counts: Full/Z* by transaction or one arrival; U, S, O, Drain
-// by one MMA commit; UT and SB by the eight chain warps (one arrival each);
-// Empty by one MMA commit and the eight chain warps (they read the record's
-// e^{G_C}); OFree by the four output warps; ZReady by the gate warps.
-constexpr int kSPrefetch = 3;      // records (and v tiles) pulled into L2 this many chunks ahead
-enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarU, kSBarUT, kSBarS, kSBarSB,
-       kSBarO0, kSBarO1, kSBarOFree0, kSBarOFree1, kSBarZFull0, kSBarZFull1, kSBarZEmpty0,
-       kSBarZEmpty1, kSBarZReady0, kSBarZReady1, kSBarDrain, kSNumBars };
+enum { kSBarFull0 = 0, kSBarFull1, kSBarEmpty0, kSBarEmpty1, kSBarMMA1, kSBarMMA2, kSBarSB,
+       kSBarUT, kSBarZFull0, kSBarZFull1, kSBarZEmpty0, kSBarZEmpty1, kSBarZReady0,
+       kSBarZReady1, kSBarDrain, kSNumBars };
 
 #ifdef KDA_PHASE_PROFILE
 // Per-phase SM-clock totals of two state-pass threads of CTA (0, 0)
@@ -155,6 +148,21 @@ __device__ unsigned long long kda_prep_clocks[32];
 #else
 #define KDA_SMARK(i) ((void)0)
 #endif
+
+// One step of a transposing butterfly sum across a warp: afterwards a[0..M)
+// hold, for the half of the rows this lane keeps (the upper half when lane
+// bit M is set), the sums over lane pairs M apart.  Steps 16 .. 1 over 32
+// rows leave lane l with row l summed over all 32 lanes.
+template <int M>
+__device__ __forceinline__ void butterfly_step(float (&a)[16], int lane) {
+  const bool up = lane & M;
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    const float send = up ? a[i] : a[i + M];
+    const float keep = up ? a[i + M] : a[i];
+    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, M);
+  }
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -319,9 +327,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_g);
-    issue_raw_kq(cur);
-    issue_raw_g(cur);
-    last_raw = 0;
+    if (!(args.debug_withhold == 2 && blockIdx.x == 0)) {
+      issue_raw_kq(cur);
+      issue_raw_g(cur);
+      last_raw = 0;
+    }
   }
   load_beta(cur);
 
@@ -341,12 +351,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
     Item nxt = cur;
     if (it_next < it_end) nxt = decode_item(args, win, s_cum, it_next);
 
-    // beta of this item: every reader of the previous item's (P4 and the
-    // inverse) has passed the inverse's last barrier, and the readers of
-    // this one come after the P1 barrier below.
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (cg == 0) s_beta[row0 + m] = rb[m];
+    named_bar(2, kPThreads);
     KDA_SMARK(0);
     const bool ok_raw = sync.wait_warp(kPBarRaw, par);
     KDA_SMARK(1);
@@ -421,10 +429,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     named_bar(2, kPThreads);
     KDA_SMARK(3);
 
-    // ---- P2: scaled operand tiles.  The masked-product MMA's operands
-    // ([K';Q'] and Khat) are stored first; Ktil and the record's Qtil and
-    // Kbar are held in registers and stored while that MMA runs.
-    uint32_t hold_kt[4][4], hold_qt[4][4], hold_kb[4][4];
+    // ---- P2: scaled operand tiles; Qtil and Kbar go straight to the record.
     {
       const int sc0 = 4 * cg;
       auto ld8 = [&](const float* t, uint64_t (&o)[4]) {
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const int r = row0 + m, rl = 4 * r4 + m;
         const uint32_t kw[4] = {rk[m].x, rk[m].y, rk[m].z, rk[m].w};
         const uint32_t qw[4] = {rq[m].x, rq[m].y, rq[m].z, rq[m].w};
-        uint32_t okp[4], oqp[4], okh[4];
+        uint32_t okp[4], oqp[4], okt[4], okh[4], oqt[4], okb[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint64_t kp = bf16x2_to_f2(kw[w]), qp = bf16x2_to_f2(qw[w]);
@@ -458,15 +463,18 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const uint64_t k1 = f2_mul(kp, e1), q1 = f2_mul(qp, e1);
           okp[w] = f2_to_bf16x2(k1);
           oqp[w] = f2_to_bf16x2(q1);
-          hold_kt[m][w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
-          hold_qt[m][w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
+          okt[w] = f2_to_bf16x2(f2_mul(k1, eR[w]));
+          oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
           kh[w] = f2_mul(kp, ei);
           okh[w] = f2_to_bf16x2(kh[w]);
-          hold_kb[m][w] = f2_to_bf16x2(f2_mul(kh[w], eC[w]));
+          okb[w] = f2_to_f16x2(f2_mul(kh[w], eC[w]));
         }
         st4(smem + kPOffKQ, 32 * ta + rl, 128, okp);
         st4(smem + kPOffKQ, 32 * ta + 16 + rl, 128, oqp);
+        st4(smem + kPOffKT, r, 64, okt);
         st4(smem + kPOffKH, khat_row0(ta) + r, 160, okh);
+        st4(rec + kRecWQ, r, 128, oqt);
+        st4(rec + kRecKB, r, 64, okb);
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int a2 = ta + 1 + i;
@@ -497,18 +505,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
                   umma_desc(bK + (t >> 2) * 160 * 128 + (t & 3) * 32, 16, 1024), idesc, t > 0);
       umma_commit(&s_bars[kPBarAP]);
     }
-    // While it runs: Ktil (the W product's operand, read after later
-    // barriers and a proxy fence) and the record's Qtil and Kbar.
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int r = row0 + m;
-      *reinterpret_cast<uint4*>(smem + kPOffKT + sw128_off(r, 8 * cg, 64)) =
-          make_uint4(hold_kt[m][0], hold_kt[m][1], hold_kt[m][2], hold_kt[m][3]);
-      *reinterpret_cast<uint4*>(rec + kRecWQ + sw128_off(r, 8 * cg, 128)) =
-          make_uint4(hold_qt[m][0], hold_qt[m][1], hold_qt[m][2], hold_qt[m][3]);
-      *reinterpret_cast<uint4*>(rec + kRecKB + sw128_off(r, 8 * cg, 64)) =
-          make_uint4(hold_kb[m][0], hold_kb[m][1], hold_kb[m][2], hold_kb[m][3]);
-    }
     if (it_next < it_end) load_beta(nxt);
     const bool ok_ap = sync.wait_warp(kPBarAP, par);
     tc_fence_after();
@@ -516,19 +512,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (loader && ok_ap && it_next < it_end) {
       issue_raw_kq(nxt);
       last_raw = static_cast<int>(k_iter) + 1;
-      // The item after next: its raw tiles to L2 now, so their copies into
-      // shared memory (one item from now) wait on L2 rather than DRAM.
-      const int it_nn = it_next + it_step;
-      if (it_nn < it_end) {
-        const Item x = decode_item(args, win, s_cum, it_nn);
-        const int cx = static_cast<int>(x.t0 + static_cast<long long>(x.c) * kC);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_prefetch_3d(&tm_k, 64 * hf, x.h, cx);
-          tma_prefetch_3d(&tm_q, 64 * hf, x.h, cx);
-          tma_prefetch_3d(&tm_g, 64 * hf, x.h, cx);
-        }
-      }
     }
     KDA_SMARK(5);
 
@@ -575,7 +558,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
             float f8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
-            st_tile8(rec + kRecP, r, 16 * blk + 8 * h8, 64, f8);
+            st_tile8_f16(rec + kRecP, r, 16 * blk + 8 * h8, 64, f8);
           }
         } else if (blk == a) {
 #pragma unroll
@@ -823,27 +806,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
 // the sigmoid gate) to every output row before it is stored, the gate tiles
 // arriving by TMA beside the records; kTrans computes segment transitions
 // (below) instead of outputs.  Each is its own instantiation.
-//
-// Per chunk c (record slot s = c & 1, O buffer b = c & 1):
-//   MMA warp:  U^T += S^T (-W)^T            (N = 64, onto U0^T; commit U)
-//              O_b^T = S^T Qtil^T           (N = 64, once O_b is free)
-//              D^T = [U_hi^T | U_lo^T] [Kbar; Kbar]
-//                                           (N = 128, K = 2 x 64; commit S)
-//              O_b^T += U_hi^T P^T          (N = 64; commit O_b, slot s free)
-//              U0^T = V^T T'^T of chunk c + 1 into the U columns
-//   chain:     U^T -> bf16 hi + lo (arrive UT);
-//              S^T <- Diag(e^{G_C}) S^T + D^T in registers, its bf16 copy
-//              to TMEM (arrive SB)
-// The fp32 state lives in the chain warps' registers (64 values a thread),
-// so the decay is one FMA per element in the pass that makes the bf16 copy.
-// U enters the fp32 state as two bf16 parts (U = U_hi + U_lo to about 2^-17
-// relative), so the state's update carries no bf16 rounding of U itself:
-// where a write replaces an old value (beta = 1), U = v_new - v_old can be
-// much larger than the state it leaves, and one bf16 rounding of it would be
-// an error on the scale of the old value.
-//   outputs:   O_b^T -> registers (arrive OFree_b) -> bf16 rows -> store
-// Only U^T and S^T and their conversions are on the serial chain; the O
-// halves of both products, U0 and the decay run in its shadow.
 template <bool kGate, bool kTrans>
 __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     chunk_state_kernel(LaunchArgs args, SplitWindow win, const __grid_constant__ CUtensorMap tm_v,
@@ -855,6 +817,11 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
   __shared__ uint64_t s_bars[kSNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+#ifdef KDA_PHASE_PROFILE
+  __shared__ volatile unsigned long long s_ts[4];   // MMA1 / MMA2 issue, SB / UT hand-off
+#endif
+  __shared__ __align__(16) float s_rsum[2][4][32];   // gated: row sums of squares, per warp
+  __shared__ __align__(16) float s_rinv[2][32];      // gated: 1 / rms of the chunk's rows
   __shared__ __align__(16) float s_gw[kD];           // gated: RMSNorm scale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -873,7 +840,6 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
   // two buffers carry the partial maps.
   const int tmode = kTrans ? 1 + static_cast<int>(blockIdx.z) : 0;   // 0 off, 1 H, 2 M
   const bool vzero = tmode == 2;
-  const bool outputs = tmode == 0;
   float* tbuf = tmode == 1 ? args.trans_H : args.trans_M;
   const float* src = tmode ? (win.first ? nullptr : tbuf)
                            : (win.first ? args.init_state : win.s_run);
@@ -900,14 +866,8 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < kSNumBars; ++b) {
-      const uint32_t cnt = (b == kSBarUT || b == kSBarSB)             ? kSChainWarps
-                           : (b == kSBarEmpty0 || b == kSBarEmpty1)   ? kSChainWarps + 1
-                           : (b == kSBarOFree0 || b == kSBarOFree1)   ? kSOutWarps
-                           : (b == kSBarZReady0 || b == kSBarZReady1) ? kSGateWarps
-                                                                      : 1;
-      mbar_init(&s_bars[b], cnt);
-    }
+    for (int b = 0; b < kSNumBars; ++b)
+      mbar_init(&s_bars[b], b == kSBarZReady0 || b == kSBarZReady1 ? kSGateWarps : 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -961,22 +921,13 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_v);
       int last[2] = {-1, -1}, zlast[2] = {-1, -1};   // last chunk loaded into each slot
-      // Records and v tiles of chunk c go to L2 a few chunks before their
-      // copies into shared memory, so those copies wait on L2, not on DRAM.
-      auto prefetch = [&](int c) {
-        bulk_prefetch_l2(win.rec + static_cast<size_t>(rbase + c) * kRecBytes, kRecBytes);
-        if (!vzero) {
-          const int c0 = static_cast<int>(t0 + static_cast<long long>(win.cw0 + c) * kC);
-          tma_prefetch_3d(&tm_v, 0, h, c0);
-          tma_prefetch_3d(&tm_v, 64, h, c0);
-        }
-      };
-      for (int c = 0; c < kSPrefetch && c < nck; ++c) prefetch(c);
 #pragma unroll 1
       for (int c = 0; c < nck; ++c) {
         const int s = c & 1;
-        if (c + kSPrefetch < nck) prefetch(c + kSPrefetch);
         if (c >= 2 && !sync.wait(kSBarEmpty0 + s, ((c - 2) >> 1) & 1)) break;
+        if (c == 0 && args.debug_withhold == 1 && win.first && blockIdx.x == 0 &&
+            blockIdx.y == 0 && blockIdx.z == 0)
+          continue;   // self-test: this record never arrives
         uint64_t* bar = &s_bars[kSBarFull0 + s];
         mbar_arrive_expect_tx(bar, kRecBytes + (vzero ? 0 : 16384));
         const uint8_t* rec = win.rec + static_cast<size_t>(rbase + c) * kRecBytes;
@@ -992,8 +943,8 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
         }
         last[s] = c;
         if constexpr (kGate) {
-          // The gate tile of chunk c is read when its outputs leave; its slot
-          // is free once chunk c - 2's outputs have left.
+          // The gate tile of chunk c is read when its outputs leave, during
+          // chunk c + 1; its slot is free once chunk c - 2's outputs have left.
           if (c >= 2 && !sync.wait(kSBarZEmpty0 + s, ((c - 2) >> 1) & 1)) break;
           uint64_t* zbar = &s_bars[kSBarZFull0 + s];
           mbar_arrive_expect_tx(zbar, 16384);
@@ -1016,16 +967,14 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
   } else if (warp == kSMmaWarp) {
     // ================================ MMA issue ===============================
     if (lane == 0) {
-      const uint32_t i64 = umma_idesc_bf16(128, 64, 0, 0);
-      const uint32_t i128mn = umma_idesc_bf16(128, 128, 0, 1);
-      // U0^T = V^T T'^T of the chunk in slot s, into the U columns (state-independent).
+      // U0^T = V^T T'^T of the chunk in slot s, into U0 buffer s (state-independent).
       auto issue_mma0 = [&](int s) {
         const uint32_t idesc = umma_idesc_bf16(128, 64, 1, 0);
         const uint32_t aV = smem_u32(smem + kSOffV + s * 16384);
         const uint32_t bT = smem_u32(smem + kSOffRec + s * kRecSlot + kRecT);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-          umma_bf16(tbase + kSColU, umma_desc(aV + t * 2048, 64 * 128, 1024),
+          umma_bf16(tbase + kSColU0 + 64 * s, umma_desc(aV + t * 2048, 64 * 128, 1024),
                     umma_desc(bT + t * 32, 16, 1024), idesc, t > 0);
       };
       bool ok = sync.wait(kSBarFull0, 0);
@@ -1035,54 +984,46 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       }
 #pragma unroll 1
       for (int c = 0; c < nck && ok; ++c) {
-        const int s = c & 1, ob = c & 1;
+        const int s = c & 1;
         const uint8_t* slot = smem + kSOffRec + s * kRecSlot;
-        const uint32_t bWQ = smem_u32(slot + kRecWQ);
-        // The chunk's record is in its slot (already waited for with U0^T
-        // unless v = 0), and the state's bf16 copy is written.
-        if (!sync.wait(kSBarFull0 + s, (c >> 1) & 1)) break;
+        // [O^T | U^T] = S^T [Qtil^T | -W^T]      (M = 128, N = 128, K = dk = 128)
         if (!sync.wait(kSBarSB, c & 1)) break;
         tc_fence_after();
-        // U^T (+)= S^T (-W)^T: rows 64..127 of the [Qtil; -W] image (K = dk = 128).
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-          umma_bf16_tmem_a(tbase + kSColU, tbase + kSColSB + 8 * t,
-                           umma_desc(bWQ + (t >> 2) * 16384 + 8192 + (t & 3) * 32, 16, 1024),
-                           i64, vzero ? t > 0 : 1);
-        umma_commit(&s_bars[kSBarU]);
-        if (outputs) {
-          // O_b^T = S^T Qtil^T, once the outputs of chunk c - 2 have left O_b.
-          if (c >= 2 && !sync.wait(kSBarOFree0 + ob, ((c - 2) >> 1) & 1)) break;
-          tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+        s_ts[0] = clock64();
+#endif
+        {
+          const uint32_t idesc = umma_idesc_bf16(128, 128, 0, 0);
+          const uint32_t bWQ = smem_u32(slot + kRecWQ);
 #pragma unroll
           for (int t = 0; t < 8; ++t)
-            umma_bf16_tmem_a(tbase + kSColO + 64 * ob, tbase + kSColSB + 8 * t,
-                             umma_desc(bWQ + (t >> 2) * 16384 + (t & 3) * 32, 16, 1024), i64,
+            umma_bf16_tmem_a(tbase + kSColO, tbase + kSColSB + 8 * t,
+                             umma_desc(bWQ + (t >> 2) * 16384 + (t & 3) * 32, 16, 1024), idesc,
                              t > 0);
+          umma_commit(&s_bars[kSBarMMA1]);
         }
-        // D^T = U_hi^T Kbar + U_lo^T Kbar (M = 128, N = 128, K = 2 x 64
-        // tokens; Kbar MN-major, read twice; the chain adds it to the state).
+        // S^T += U^T Kbar,  O^T += U^T P^T        (M = 128, N = 128 + 64, K = 64 tokens;
+        // fp16 operands: U^T, Kbar and P, see the record layout above)
         if (!sync.wait(kSBarUT, c & 1)) break;
         tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+        s_ts[1] = clock64();
+#endif
         {
-          const uint32_t bKB = smem_u32(slot + kRecKB);
+          const uint32_t idesc_s = umma_idesc_f16(128, 128, 0, 1);
+          const uint32_t idesc_o = umma_idesc_f16(128, 64, 0, 0);
+          const uint32_t bKB = smem_u32(slot + kRecKB), bP = smem_u32(slot + kRecP);
 #pragma unroll
-          for (int t = 0; t < 8; ++t)
+          for (int t = 0; t < 4; ++t) {
             umma_bf16_tmem_a(tbase + kSColS, tbase + kSColUT + 8 * t,
-                             umma_desc(bKB + (t & 3) * 2048, 64 * 128, 1024), i128mn, t > 0);
-          umma_commit(&s_bars[kSBarS]);
+                             umma_desc(bKB + t * 2048, 64 * 128, 1024), idesc_s, 1);
+            umma_bf16_tmem_a(tbase + kSColO, tbase + kSColUT + 8 * t,
+                             umma_desc(bP + t * 32, 16, 1024), idesc_o, 1);
+          }
+          umma_commit(&s_bars[kSBarEmpty0 + s]);
+          umma_commit(&s_bars[kSBarMMA2]);
         }
-        if (outputs) {
-          // O_b^T += U_hi^T P^T (the outputs keep one bf16 rounding of U).
-          const uint32_t bP = smem_u32(slot + kRecP);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            umma_bf16_tmem_a(tbase + kSColO + 64 * ob, tbase + kSColUT + 8 * t,
-                             umma_desc(bP + t * 32, 16, 1024), i64, 1);
-          umma_commit(&s_bars[kSBarO0 + ob]);
-        }
-        umma_commit(&s_bars[kSBarEmpty0 + s]);
-        // The next chunk's U0^T, into the U columns the chain has converted.
+        // The next chunk's U0^T runs while the state warps convert S^T.
         if (c + 1 < nck && !vzero) {
           if (!sync.wait(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1)) break;
           tc_fence_after();
@@ -1093,231 +1034,387 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
       umma_commit(&s_bars[kSBarDrain]);
       mbar_wait(&s_bars[kSBarDrain], 0, 100000000ull);
     }
-  } else if (warp < kSChainWarps) {
-    // ============================== serial chain ==============================
+  } else {
+    // =============================== state pass ===============================
     // Warp w reads TMEM lanes 32 (w & 3) .. + 31 (value columns j) and the
-    // column half hf = w >> 2 of S^T (key rows 64 hf .. 64 hf + 63).
+    // column half hf = w >> 2 of every TMEM matrix.
     const int q = warp & 3, hf = warp >> 2;
     const int j = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    float sv[64];   // S^T[j][64 hf + u]: this thread's part of the fp32 state
-    auto pack_sb = [&]() {
+    __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
+
+    // S^T[j][c] = S[c][j] for key rows c of this half: fp32 copy and bf16 copy.
+#pragma unroll 1
+    for (int cb = 0; cb < 2; ++cb) {
+      const int c0 = 64 * hf + 32 * cb;
+      uint32_t f[32], b[16];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t b[16];
+      for (int u = 0; u < 32; ++u)
+        f[u] = __float_as_uint(src ? __ldcs(src + soff + (c0 + u) * kD + j)
+                                   : (src_identity && c0 + u == j ? 1.f : 0.f));
 #pragma unroll
-        for (int u = 0; u < 16; ++u) b[u] = pack2(sv[32 * h2 + 2 * u], sv[32 * h2 + 2 * u + 1]);
-        tmem_st16(tbase + lane_base + kSColSB + 32 * hf + 16 * h2, b);
+      for (int u = 0; u < 16; ++u)
+        b[u] = pack2(__uint_as_float(f[2 * u]), __uint_as_float(f[2 * u + 1]));
+      tmem_st32(tbase + lane_base + kSColS + c0, f);
+      tmem_st16(tbase + lane_base + kSColSB + c0 / 2, b);
+    }
+    // Outputs of chunk cl, held as O^T column j, rows 32 hf .. + 31, in `ov`.
+    // Lane pairs swap values so each lane holds two adjacent columns of every
+    // other row.  A full chunk goes through the staging tile and one TMA
+    // store per 64-column half; a sequence's ragged last chunk is written
+    // row by row (the tile's tail rows belong to the next sequence).  Every
+    // state thread calls it (it holds barriers); `live` is false once a wait
+    // has failed.  With `defer`, a gated full chunk is only staged and the
+    // call returns true: its epilogue pass (gated_finish) is still to run.
+    float ov[32];
+    // A full chunk with the output epilogue, in two parts.  Part one: the raw
+    // outputs (bf16) to the staging tile, while MMA1 of the next chunk runs.
+    // Part two, during the next chunk's MMA2 (the U^T hand-off's barrier has
+    // made every thread's staged rows visible by then): 8 threads per row
+    // (16 columns each, 16-byte vectors) take the row's sum of squares with 3
+    // shuffles and scale it in place by 1 / rms times the gate tile's
+    // w * sigmoid(z), then the TMA stores.
+    auto gated_stage = [&](bool odd) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float a = ov[2 * k], b = ov[2 * k + 1];
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
+        pk[k] = odd ? pack2(other, b) : pack2(a, other);
+      }
+      // The previous TMA store has read the staging tile.
+      if (tid == 0) bulk_wait_read_all();
+      named_bar(1, kSStateThreads);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(r, j & ~1, 64)) = pk[k];
       }
     };
-    // The entering state and its bf16 copy.
+    // Part two (after a barrier since part one).
+    auto gated_finish = [&](int cl, bool live) {
+      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
+      // The gate tile holds w * sigmoid(z) once the gate warps are done with it.
+      if (!sync.wait_warp(kSBarZReady0 + (cl & 1), (cl >> 1) & 1)) live = false;
+      const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
+      const int sg = tid & 7;
 #pragma unroll
-    for (int u = 0; u < 64; ++u) {
-      const int c = 64 * hf + u;
-      sv[u] = src ? __ldcs(src + soff + c * kD + j) : (src_identity && c == j ? 1.f : 0.f);
+      for (int rh = 0; rh < 2; ++rh) {
+        const int r = (tid >> 3) + 32 * rh;
+        uint4* po[2];
+        uint4 ov4[2], gv4[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t off = sw128_off(r, 16 * sg + 8 * e, 64);
+          po[e] = reinterpret_cast<uint4*>(smem + kSOffO + off);
+          ov4[e] = *po[e];
+          gv4[e] = *reinterpret_cast<const uint4*>(zt + off);
+        }
+        float x[16];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          unpack8(ov4[e], *reinterpret_cast<float(*)[8]>(&x[8 * e]));
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) ss = fmaf(x[u], x[u], ss);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+        const float rinv = rsqrtf(ss * (1.f / kD) + args.gate_eps);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float gz[8];
+          unpack8(gv4[e], gz);
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w4[u] = pack2(x[8 * e + 2 * u] * rinv * gz[2 * u],
+                          x[8 * e + 2 * u + 1] * rinv * gz[2 * u + 1]);
+          *po[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      fence_async_smem();
+      named_bar(1, kSStateThreads);
+      if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);   // gate tile read
+      if (tid == 0 && live && !s_abort) {
+        tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
+        tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
+        bulk_commit();
+      }
+    };
+    auto emit_out = [&](int cl, bool live, bool defer) -> bool {
+      const long long c0 = t0 + static_cast<long long>(win.cw0 + cl) * kC;
+      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
+      const bool odd = lane & 1;
+      if constexpr (kGate) {
+        if (L == kC) {
+          gated_stage(odd);
+          if (defer) return true;
+          named_bar(1, kSStateThreads);
+          gated_finish(cl, live);
+          return false;
+        }
+        // (A sequence's ragged last chunk.)  Row sums of squares: a butterfly over the warp's 32 columns leaves
+        // lane l with row 32 hf + l; the four warps of a column half meet in
+        // shared memory.
+        float a[16];
+        {
+          const bool up = lane & 16;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo = ov[i] * ov[i], hi = ov[i + 16] * ov[i + 16];
+            a[i] = (up ? hi : lo) + __shfl_xor_sync(0xFFFFFFFFu, up ? lo : hi, 16);
+          }
+        }
+        butterfly_step<8>(a, lane);
+        butterfly_step<4>(a, lane);
+        butterfly_step<2>(a, lane);
+        butterfly_step<1>(a, lane);
+        s_rsum[hf][q][lane] = a[0];
+        named_bar(1, kSStateThreads);
+        if (q == 0) {
+          const float ss = s_rsum[hf][0][lane] + s_rsum[hf][1][lane] + s_rsum[hf][2][lane] +
+                           s_rsum[hf][3][lane];
+          s_rinv[hf][lane] = rsqrtf(ss * (1.f / kD) + args.gate_eps);
+        }
+        named_bar(1, kSStateThreads);
+        // The gate tile holds w * sigmoid(z) once the gate warp is done with it.
+        if (!sync.wait_warp(kSBarZReady0 + (cl & 1), (cl >> 1) & 1)) live = false;
+        const uint8_t* zt = smem + kSOffZ + (cl & 1) * 16384;
+#pragma unroll
+        for (int r = 0; r < 32; r += 4) {
+          const float4 ri = *reinterpret_cast<const float4*>(&s_rinv[hf][r]);
+          const float rr[4] = {ri.x, ri.y, ri.z, ri.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            ov[r + u] *= rr[u] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                     zt + sw128_off(32 * hf + r + u, j, 64)));
+        }
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float a = ov[2 * k], b = ov[2 * k + 1];
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
+        pk[k] = odd ? pack2(other, b) : pack2(a, other);
+      }
+      if (L < kC) {
+        __nv_bfloat16* base = gout + (c0 * H + h) * kD + (j & ~1);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+          if (live && r < L)
+            *reinterpret_cast<uint32_t*>(base + static_cast<long long>(r) * H * kD) = pk[k];
+        }
+        if constexpr (kGate) {
+          named_bar(1, kSStateThreads);   // every gate-tile read is done
+          if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);
+        }
+        return false;
+      }
+      // The previous TMA store has read the staging tile.
+      if (tid == 0) bulk_wait_read_all();
+      named_bar(1, kSStateThreads);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = 32 * hf + 2 * k + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(r, j & ~1, 64)) = pk[k];
+      }
+      fence_async_smem();
+      named_bar(1, kSStateThreads);
+      if constexpr (kGate) {
+        if (tid == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + (cl & 1)]);   // gate tile read
+      }
+      if (tid == 0 && live && !s_abort) {
+        tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
+        tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
+        bulk_commit();
+      }
+      return false;
+    };
+
+    // The fp32 state carries the first chunk's decay Diag(e^{G_C}) before
+    // MMA2 adds onto it (later chunks get theirs in step E).
+    bool ok = sync.wait_warp(kSBarFull0, 0);
+    tmem_st_wait();
+    if (ok) {
+      const float* gam = reinterpret_cast<const float*>(smem + kSOffRec + kRecG);
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        const int c0 = 64 * hf + 32 * cb;
+        float v[32];
+        tmem_ld32(tbase + lane_base + kSColS + c0, v);
+        tmem_ld_wait();
+        uint32_t f[32];
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 gm = *reinterpret_cast<const float4*>(&gam[c0 + u]);
+          f[u] = __float_as_uint(v[u] * gm.x);
+          f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
+          f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
+          f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
+        }
+        tmem_st32(tbase + lane_base + kSColS + c0, f);
+      }
     }
-    pack_sb();
     tmem_st_wait();
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_bars[kSBarSB]);
-    bool ok = true;
-
+    named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+    if (tid == 0) s_ts[2] = clock64();
+#endif
+    if (tid == 0) mbar_arrive(&s_bars[kSBarSB]);
+    bool prev_ok = false;
+    bool pend = false;   // gated: chunk c - 1 staged, its epilogue pass still to run
+#ifdef KDA_PHASE_PROFILE
+    unsigned long long hand[4] = {};   // SB->MMA1 issue, MMA1 exec, UT->MMA2 issue, MMA2 exec
+#endif
 #ifdef KDA_PHASE_PROFILE
     unsigned long long prof_acc[10] = {}, prof_t = clock64();
 #endif
+
 #pragma unroll 1
     for (int c = 0; c < nck; ++c) {
       const int s = c & 1;
-      // U^T (fp32, U0^T included by the MMA) -> bf16 A operands hi and lo.
-      const bool ok1 = ok && sync.wait_warp(kSBarU, c & 1);
+      // (B) While MMA1 runs: the previous chunk's outputs.
+      if (c > 0 && tmode == 0) pend = emit_out(c - 1, prev_ok, true);
       KDA_SMARK(0);
+      // (C) U^T + U0^T (fp32) -> bf16 A operand, then hand it to MMA2.
+      bool ok1 = ok && sync.wait_warp(kSBarMMA1, c & 1);
       tc_fence_after();
-      if (ok1) {
-        float v[32];
-        tmem_ld32(tbase + lane_base + kSColU + 32 * hf, v);
-        tmem_ld_wait();
-        uint32_t b[16], bl[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) split_bf16x2(v[2 * u], v[2 * u + 1], b[u], bl[u]);
-        tmem_st16(tbase + lane_base + kSColUT + 16 * hf, b);
-        tmem_st16(tbase + lane_base + kSColUT + 32 + 16 * hf, bl);
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) {
+        const unsigned long long now = clock64();
+        hand[0] += s_ts[0] - s_ts[2];
+        hand[1] += now - s_ts[0];
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
+#endif
       KDA_SMARK(1);
-      // The new state S_C = Diag(e^{G_C}) S_0 + Kbar^T U, and its bf16 copy
-      // for the next chunk's first product.
-      const bool has_next = c + 1 < nck;
-      // (The record's arrival is also waited for here, so that this warp
-      // sees its e^{G_C}; the phase completed before the products began.)
-      const bool ok2 = ok1 && sync.wait_warp(kSBarFull0 + s, (c >> 1) & 1) &&
-                       sync.wait_warp(kSBarS, c & 1);
-      KDA_SMARK(3);
-      tc_fence_after();
-      if (ok2) {
-        const float* gam =
-            reinterpret_cast<const float*>(smem + kSOffRec + s * kRecSlot + kRecG) + 64 * hf;
+      if (ok1) {
+        float v[32], w[32];
+        tmem_ld32(tbase + lane_base + kSColU + 32 * hf, v);
+        if (!vzero) tmem_ld32(tbase + lane_base + kSColU0 + 64 * s + 32 * hf, w);
+        tmem_ld_wait();
+        if (vzero) {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float d[32];
-          tmem_ld32(tbase + lane_base + kSColS + 64 * hf + 32 * h2, d);
-          tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 32; u += 4) {
-            const float4 gm = *reinterpret_cast<const float4*>(&gam[32 * h2 + u]);
-            sv[32 * h2 + u] = fmaf(gm.x, sv[32 * h2 + u], d[u]);
-            sv[32 * h2 + u + 1] = fmaf(gm.y, sv[32 * h2 + u + 1], d[u + 1]);
-            sv[32 * h2 + u + 2] = fmaf(gm.z, sv[32 * h2 + u + 2], d[u + 2]);
-            sv[32 * h2 + u + 3] = fmaf(gm.w, sv[32 * h2 + u + 3], d[u + 3]);
-          }
+          for (int u = 0; u < 32; ++u) w[u] = 0.f;
         }
-        if (has_next) pack_sb();
+        uint32_t b[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          b[u] = pack2_f16(v[2 * u] + w[2 * u], v[2 * u + 1] + w[2 * u + 1]);
+        tmem_st16(tbase + lane_base + kSColUT + 16 * hf, b);
       }
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (ok2 && has_next) mbar_arrive(&s_bars[kSBarSB]);
-        if (ok2) mbar_arrive(&s_bars[kSBarEmpty0 + s]);   // e^{G_C} of slot s is read
+      KDA_SMARK(2);
+      named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) s_ts[3] = clock64();
+#endif
+      if (tid == 0 && ok1) mbar_arrive(&s_bars[kSBarUT]);
+      // While MMA2 runs: the staged chunk's epilogue (the barrier above made
+      // its rows visible).
+      if constexpr (kGate) {
+        if (pend) gated_finish(c - 1, prev_ok);
+        pend = false;
       }
+      KDA_SMARK(3);
       KDA_SMARK(4);
-      // Off the chain: prefix-cache checkpoint.
+      // (E) Outputs to registers; new state -> bf16 operand copy (the serial
+      // step) and, for the next chunk, the decayed fp32 state; checkpoints;
+      // then hand the state to the next MMA1.
+      const bool has_next = c + 1 < nck;
+      const bool ok_next =
+          !has_next || sync.wait_warp(kSBarFull0 + (s ^ 1), ((c + 1) >> 1) & 1);
+      const bool ok2 = ok1 && sync.wait_warp(kSBarMMA2, c & 1);
+      tc_fence_after();
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) {
+        const unsigned long long now = clock64();
+        hand[2] += s_ts[1] - s_ts[3];
+        hand[3] += now - s_ts[1];
+      }
+#endif
+      KDA_SMARK(5);
       if (ok2) {
+        const bool decay = has_next && ok_next;
+        const float* gam =
+            reinterpret_cast<const float*>(smem + kSOffRec + (s ^ 1) * kRecSlot + kRecG);
         const long long done = static_cast<long long>(win.cw0 + c + 1) * kC;
+        float* ck = nullptr;
         if (args.ckpt && done <= t1 - t0 && done % args.ckpt_interval == 0) {
           const long long row = args.ckpt_offsets[n] + done / args.ckpt_interval - 1;
-          float* ck = args.ckpt + (row * H + h) * kD * kD + j;
+          ck = args.ckpt + (row * H + h) * kD * kD + j;
+        }
+        float sv[2][32];
+        tmem_ld32(tbase + lane_base + kSColO + 32 * hf, ov);
+        tmem_ld32(tbase + lane_base + kSColS + 64 * hf, sv[0]);
+        tmem_ld32(tbase + lane_base + kSColS + 64 * hf + 32, sv[1]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 64; ++u) __stcs(ck + (64 * hf + u) * kD, sv[u]);
+        for (int cb = 0; cb < 2; ++cb) {
+          const int c0 = 64 * hf + 32 * cb;
+          const float (&v)[32] = sv[cb];
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) b[u] = pack2(v[2 * u], v[2 * u + 1]);
+          tmem_st16(tbase + lane_base + kSColSB + c0 / 2, b);
+          if (decay) {
+            uint32_t f[32];
+#pragma unroll
+            for (int u = 0; u < 32; u += 4) {
+              const float4 gm = *reinterpret_cast<const float4*>(&gam[c0 + u]);
+              f[u] = __float_as_uint(v[u] * gm.x);
+              f[u + 1] = __float_as_uint(v[u + 1] * gm.y);
+              f[u + 2] = __float_as_uint(v[u + 2] * gm.z);
+              f[u + 3] = __float_as_uint(v[u + 3] * gm.w);
+            }
+            tmem_st32(tbase + lane_base + kSColS + c0, f);
+          }
+          if (ck) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) __stcs(ck + (c0 + u) * kD, v[u]);
+          }
         }
       }
-      ok = ok2;
-      KDA_SMARK(5);
+      KDA_SMARK(6);
+      tmem_st_wait();
+      tc_fence_before();
+      KDA_SMARK(7);
+      named_bar(1, kSStateThreads);
+#ifdef KDA_PHASE_PROFILE
+      if (tid == 0) s_ts[2] = clock64();
+#endif
+      if (tid == 0 && ok2 && ok_next && has_next) mbar_arrive(&s_bars[kSBarSB]);
+      KDA_SMARK(8);
+      prev_ok = ok2;
+      ok = ok2 && ok_next;
     }
 #ifdef KDA_PHASE_PROFILE
     if (blockIdx.x == 0 && blockIdx.y == 0 && (tid == 0 || tid == 64)) {
-      for (int i = 0; i < 6; ++i) kda_split_clocks[(tid ? 10 : 0) + i] = prof_acc[i];
-      if (tid == 0) kda_split_clocks[30] = nck;
+      for (int i = 0; i < 10; ++i) kda_split_clocks[(tid ? 10 : 0) + i] = prof_acc[i];
+      if (tid == 0) {
+        kda_split_clocks[30] = nck;
+        for (int i = 0; i < 4; ++i) kda_split_clocks[20 + i] = hand[i];
+      }
     }
 #endif
-    // After the last chunk the state carries no further decay.
-    if (!s_abort && ok && dst) {
-#pragma unroll
-      for (int u = 0; u < 64; ++u) __stcs(dst + soff + (64 * hf + u) * kD + j, sv[u]);
-    }
-  } else if (outputs) {
-    // ================================= outputs ================================
-    // Output thread ot holds value column j = 32 (warp & 3) + lane of a
-    // chunk's O^T (64 tokens).  Lane pairs swap values so each lane holds two
-    // adjacent columns of every other row; the rows go to the staging tile,
-    // then leave by TMA (a full chunk) or row by row (a sequence's ragged
-    // last chunk; the tile's tail rows belong to the next sequence).  With
-    // the epilogue, the staged rows are normalised and gated first (8
-    // threads per row, 16-byte vectors, 3 shuffles per row sum).
-    const int q = warp & 3, ot = tid - 32 * kSOutWarp;
-    const int j = 32 * q + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const bool odd = lane & 1;
-    __nv_bfloat16* __restrict__ gout = static_cast<__nv_bfloat16*>(args.out);
+    if (tmode == 0) emit_out(nck - 1, prev_ok, false);
+    if (tid == 0) bulk_wait_all();
+    if (__all_sync(0xFFFFFFFFu, !s_abort) && dst) {
+      // After the last chunk the fp32 state carries no further decay.
 #pragma unroll 1
-    for (int c = 0; c < nck; ++c) {
-      const int ob = c & 1;
-      const long long c0 = t0 + static_cast<long long>(win.cw0 + c) * kC;
-      const int L = static_cast<int>(t1 - c0 < kC ? t1 - c0 : kC);
-      bool live = sync.wait_warp(kSBarO0 + ob, (c >> 1) & 1);
-      tc_fence_after();
-      uint32_t pk[32];
-      if (live) {
-        float ov[64];
-        tmem_ld32(tbase + lane_base + kSColO + 64 * ob, *reinterpret_cast<float(*)[32]>(ov));
-        tmem_ld32(tbase + lane_base + kSColO + 64 * ob + 32,
-                  *reinterpret_cast<float(*)[32]>(ov + 32));
+      for (int cb = 0; cb < 2; ++cb) {
+        const int c0 = 64 * hf + 32 * cb;
+        float v[32];
+        tmem_ld32(tbase + lane_base + kSColS + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float a = ov[2 * k], b = ov[2 * k + 1];
-          const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a : b, 1);
-          pk[k] = odd ? pack2(other, b) : pack2(a, other);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && live) mbar_arrive(&s_bars[kSBarOFree0 + ob]);
-      // The previous chunk's TMA store has read the staging tile.
-      if (ot == 0) bulk_wait_read_all();
-      named_bar(1, kSOutThreads);
-      if (live) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          *reinterpret_cast<uint32_t*>(smem + kSOffO + sw128_off(2 * k + (odd ? 1 : 0), j & ~1,
-                                                                 64)) = pk[k];
-      }
-      named_bar(1, kSOutThreads);
-      if constexpr (kGate) {
-        // The gate tile holds w * sigmoid(z) once the gate warps are done with it.
-        if (!sync.wait_warp(kSBarZReady0 + ob, (c >> 1) & 1)) live = false;
-        const uint8_t* zt = smem + kSOffZ + ob * 16384;
-        const int sg = ot & 7;
-#pragma unroll 1
-        for (int rh = 0; rh < 4; ++rh) {
-          const int r = (ot >> 3) + 16 * rh;
-          uint4* po[2];
-          uint4 ov4[2], gv4[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint32_t off = sw128_off(r, 16 * sg + 8 * e, 64);
-            po[e] = reinterpret_cast<uint4*>(smem + kSOffO + off);
-            ov4[e] = *po[e];
-            gv4[e] = *reinterpret_cast<const uint4*>(zt + off);
-          }
-          float x[16];
-          float ss = 0.f;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) unpack8(ov4[e], *reinterpret_cast<float(*)[8]>(&x[8 * e]));
-#pragma unroll
-          for (int u = 0; u < 16; ++u) ss = fmaf(x[u], x[u], ss);
-          ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 4);
-          ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-          ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-          const float rinv = rsqrtf(ss * (1.f / kD) + args.gate_eps);
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float gz[8];
-            unpack8(gv4[e], gz);
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              w4[u] = pack2(x[8 * e + 2 * u] * rinv * gz[2 * u],
-                            x[8 * e + 2 * u + 1] * rinv * gz[2 * u + 1]);
-            *po[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-        }
-        named_bar(1, kSOutThreads);
-        if (ot == 0) mbar_arrive(&s_bars[kSBarZEmpty0 + ob]);   // gate tile read
-      }
-      if (L == kC) {
-        fence_async_smem();
-        named_bar(1, kSOutThreads);
-        if (ot == 0 && live && !s_abort) {
-          tma_store_3d(&tm_o, smem + kSOffO, 0, h, static_cast<int>(c0));
-          tma_store_3d(&tm_o, smem + kSOffO + 8192, 64, h, static_cast<int>(c0));
-          bulk_commit();
-        }
-      } else if (live) {
-        // Rows below L, 16 bytes at a time (128 threads x 8 pieces).
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int piece = ot + kSOutThreads * i, r = piece >> 4, c16 = piece & 15;
-          if (r < L)
-            *reinterpret_cast<uint4*>(gout + ((c0 + r) * H + h) * kD + 8 * c16) =
-                *reinterpret_cast<const uint4*>(smem + kSOffO + sw128_off(r, 8 * c16, 64));
-        }
+        for (int u = 0; u < 32; ++u) __stcs(dst + soff + (c0 + u) * kD + j, v[u]);
       }
     }
-    if (ot == 0) bulk_wait_all();
   }
 
   tc_fence_before();

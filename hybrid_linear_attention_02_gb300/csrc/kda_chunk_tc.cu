@@ -71,9 +71,9 @@ constexpr uint32_t kOffKT = kOffKH + 40960;    // Ktil = k e^G                 6
 constexpr uint32_t kOffV = kOffKT + 16384;     // V                            64 x 128
 constexpr uint32_t kOffTB = kOffV + 16384;     // T diag(beta)                 64 x 64
 constexpr uint32_t kOffQT = kOffTB + 8192;     // Qtil = q e^G, 2 slots        64 x 128
-constexpr uint32_t kOffKB = kOffQT + 32768;    // Kbar, 2 slots                64 x 128
+constexpr uint32_t kOffKB = kOffQT + 32768;    // Kbar (fp16), 2 slots         64 x 128
 constexpr uint32_t kOffWT = kOffKB + 32768;    // -W^T                        128 x 64
-constexpr uint32_t kOffP = kOffWT + 16384;     // P, 2 slots                   64 x 64
+constexpr uint32_t kOffP = kOffWT + 16384;     // P (fp16), 2 slots            64 x 64
 constexpr uint32_t kOffO = kOffP + 16384;      // O staging (row-major bf16)   64 x 128
 constexpr uint32_t kTileBytes = kOffO + 16384;
 // Raw tiles of the next chunk (TMA destinations, same swizzled layout): k in
@@ -101,11 +101,11 @@ static_assert(kOffAt + 4 * 16 * kLdB * 4 <= kOffKH + 40960, "inverse scratch fit
 // TMEM columns (512 allocated).
 constexpr uint32_t kColAP = 0;     // 160 fp32: AP;  W^T reuses columns 0..63
 constexpr uint32_t kColW = 0;
-constexpr uint32_t kColU = 160;    // 64 fp32: U0^T, then U^T; then bf16 U_lo^T (32)
+constexpr uint32_t kColU = 160;    // 64 fp32: U0^T, then U^T
 constexpr uint32_t kColO = 224;    // 64 fp32: O^T
 constexpr uint32_t kColS = 288;    // 128 fp32: S^T (lane j = value column, col = key row)
 constexpr uint32_t kColSB = 416;   // 64: bf16 S^T, A operand
-constexpr uint32_t kColUT = 480;   // 32: bf16 U^T, A operand
+constexpr uint32_t kColUT = 480;   // 32: fp16 U^T, A operand
 constexpr uint32_t kTmemCols = 512;
 
 enum { kBarAP = 0, kBarWU, kBarFull0, kBarFull1, kBarEmpty0, kBarEmpty1, kBarMMA1, kBarUFree,
@@ -257,32 +257,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       KDA_MARK(2);
       tc_fence_after();
       if (ok1) {
-        // U^T (fp32) -> bf16 A operands: U_hi to its own columns, U_lo over
-        // the first half of the fp32 U (read above), so U = U_hi + U_lo enters
-        // the fp32 state to about 2^-17 relative.  Where a write replaces an
-        // old value (beta = 1), U = v_new - v_old can be much larger than the
-        // state it leaves; one bf16 rounding of it would be an error on the
-        // scale of the old value.
-        // (Half h's U_lo lands on fp32 columns that half 0 has already read.)
+        // U^T (fp32) -> fp16 A operand (Kbar and P are fp16 too: the state
+        // update S += Kbar^T U carries U = v_new - v_old where a write
+        // replaces an old value, far larger than the state it leaves, and
+        // fp16 rounds it 8x finer than bf16).
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
           tmem_ld32(tbase + lane_base + kColU + 32 * half, v);
           tmem_ld_wait();
-          uint32_t b[16], bl[16];
+          uint32_t b[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) split_bf16x2(v[2 * u], v[2 * u + 1], b[u], bl[u]);
+          for (int u = 0; u < 16; ++u) b[u] = pack2_f16(v[2 * u], v[2 * u + 1]);
           tmem_st16(tbase + lane_base + kColUT + 16 * half, b);
-          tmem_st16(tbase + lane_base + kColU + 16 * half, bl);
         }
       }
       tmem_st_wait();
       tc_fence_before();
       named_bar(1, kStateThreads);
       if (j == 0 && ok1 && !s_abort) {
+        mbar_arrive(&s_bars[kBarUFree]);
         tc_fence_after();
-        // S^T += U_hi^T Kbar + U_lo^T Kbar (K = 2 x 64 tokens) ;  O^T += U_hi^T P^T
-        const uint32_t iS = umma_idesc_bf16(128, 128, 0, 1), iO = umma_idesc_bf16(128, 64, 0, 0);
+        // S^T += U^T Kbar (K = 64 tokens) ;  O^T += U^T P^T   (fp16 operands)
+        const uint32_t iS = umma_idesc_f16(128, 128, 0, 1), iO = umma_idesc_f16(128, 64, 0, 0);
         const uint32_t bK = smem_u32(smem + kOffKB + s * 16384),
                        bP = smem_u32(smem + kOffP + s * 8192);
 #pragma unroll
@@ -291,10 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_tmem_a(tbase + kColS, aU, umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
           umma_bf16_tmem_a(tbase + kColO, aU, umma_desc(bP + t * 32, 16, 1024), iO, 1);
         }
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          umma_bf16_tmem_a(tbase + kColS, tbase + kColU + 8 * t,
-                           umma_desc(bK + t * 2048, 64 * 128, 1024), iS, 1);
         umma_commit(&s_bars[kBarEmpty0 + s]);
         umma_commit(&s_bars[kBarMMA2]);
       }
@@ -302,8 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok2 = sync.wait_warp(kBarMMA2, c & 1);
       KDA_MARK(4);
       tc_fence_after();
-      // The U columns (U_lo) are read: the next chunk's U0^T may land there.
-      if (j == 0 && ok2) mbar_arrive(&s_bars[kBarUFree]);
       if (ok2) {
         // Prefix-cache checkpoint after this chunk (full chunks whose end is a
         // multiple of the checkpoint interval).
@@ -432,9 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
-        issue_raw(0);
+        if (!(args.debug_withhold == 3 && blockIdx.x == 0 && blockIdx.y == 0)) {
+          issue_raw(0);   // (self-test: withheld, so the first raw tiles never arrive)
+          last_raw = 0;
+        }
         issue_raw_v(0);
-        last_raw = last_rawv = 0;
+        last_rawv = 0;
       }
       load_beta(0);
     }
@@ -566,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             oqt[w] = f2_to_bf16x2(f2_mul(q1, eR[w]));
             kh[m][w] = f2_mul(kp, ei);
             okh[w] = f2_to_bf16x2(kh[m][w]);
-            okb[w] = f2_to_bf16x2(f2_mul(kh[m][w], eC[w]));
+            okb[w] = f2_to_f16x2(f2_mul(kh[m][w], eC[w]));
           }
           st4(kOffKQ, 32 * ta + rl, 128, okp);
           st4(kOffKQ, 32 * ta + 16 + rl, 128, oqp);
@@ -670,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float f8[8];
 #pragma unroll
               for (int u = 0; u < 8; ++u) f8[u] = v[8 * h8 + u];
-              st_tile8(ptile, r, 16 * blk + 8 * h8, 64, f8);
+              st_tile8_f16(ptile, r, 16 * blk + 8 * h8, 64, f8);
             }
           } else if (blk == a) {
 #pragma unroll

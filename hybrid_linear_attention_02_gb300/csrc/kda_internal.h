@@ -48,6 +48,12 @@ struct LaunchArgs {
   // head) M [dk, dk] and H [dk, dv] with S_end = M S_0 + H; no outputs.
   float* trans_M;
   float* trans_H;
+  // Failure-detection self-test only (0 in every production call): one copy
+  // is never issued, so the kernels' bounded waits expire.  1: the split
+  // state kernel's first record of pair (0, 0); 2: the split preparation
+  // kernel's first raw tiles in CTA 0; 3: the fused kernel's first raw tiles
+  // in CTA (0, 0).
+  int debug_withhold;
 };
 
 // fp32 CUDA-core kernel that walks the recurrence token by token with the

@@ -209,6 +209,15 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, i
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// The same for kind::f16 with fp16 A and B (format code 0), fp32 accumulator.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(a_mn) << 15)       // A major
+         | (static_cast<uint32_t>(b_mn) << 16)       // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T for one K-step of 16.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -358,6 +367,15 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t a) {
   f2_unpack(a, lo, hi);
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Round both halves to fp16 (nearest even, saturating at +-65504) and pack
+// them, low half first.
+__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t a) {
+  float lo, hi;
+  f2_unpack(a, lo, hi);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 // The two bf16 halves of a 32-bit word as an fp32 pair (exact).

@@ -351,6 +351,27 @@ KDA_API const char* kda_status_string(int status);
  */
 KDA_API int kda_debug_wait_timeout(int* dev_status, unsigned timeout_us, void* stream);
 
+/*
+ * Failure-detection self-test of the prefill kernels themselves (diagnostic).
+ * Runs kda_chunk_fwd (bf16, dk = dv = 128, chunk 64, N equal-length
+ * sequences, no cu_seqlens) with one copy deliberately never issued, so that
+ * a production kernel's bounded wait (2 s) expires and its abort path runs:
+ *   which = 1: the split form's state kernel, the first record of pair (0, 0);
+ *   which = 2: the split form's preparation kernel, the first raw tiles of
+ *              its first block;
+ *   which = 3: the fused kernel, the first raw tiles of block (0, 0).
+ * Every role of the affected block then gives up, waits (bounded) for its
+ * copies and MMAs in flight, frees its TMEM and returns; *dev_status (device
+ * int, required) receives KDA_ERR_TIMEOUT and the context stays usable.  The
+ * outputs of the call are not meaningful.  Forms 1 and 2 need the split
+ * form's workspace (kda_chunk_fwd_workspace_size), else KDA_ERR_WORKSPACE.
+ */
+KDA_API int kda_debug_chunk_fwd_withhold(int which, const void* q, const void* k, const void* v,
+                                         const void* g, const void* beta,
+                                         const float* init_state, void* out, float* final_state,
+                                         const kda_dims* dims, void* workspace,
+                                         size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 KDA_API int kda_version(void);
 

@@ -42,6 +42,18 @@ def test_wait_timeout_self_test_rejects_bad_arguments(lib):
     assert lib.kda_debug_wait_timeout(ctypes.c_void_p(16), 0, None) == -1
 
 
+def test_withhold_self_test_rejects_bad_arguments(lib):
+    d = _dims(n=1, t=128)
+    call = lambda which, st: lib.kda_debug_chunk_fwd_withhold(
+        which, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, ctypes.byref(d), None, 0, st, None)
+    assert call(0, FAKE) == -1 and call(4, FAKE) == -1     # unknown form
+    assert call(1, None) == -1                              # dev_status required
+    assert call(1, FAKE) == -6                              # the split form needs a workspace
+    dd = _dims(n=1, t=128, dtype=0)                         # fp32: no tensor-core kernel
+    assert lib.kda_debug_chunk_fwd_withhold(3, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
+                                            ctypes.byref(dd), None, 0, FAKE, None) == -2
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert lib.kda_status_string(code)
