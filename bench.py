@@ -248,6 +248,9 @@ def run_gpu(args):
     if args.only == "decode":
         run_decode_only(args, dev)
         return
+    if args.only == "headline":
+        run_headline_only(args, dev)
+        return
     # ---------------- prefill (headline) ----------------
     w = inputs.WORKLOADS[PREFILL]
     d = inputs.make_prefill(w, seed=rank, device=dev)
@@ -616,6 +619,22 @@ def run_decode_leg(args, dev, rank, world, start, end, stream, barrier, max_over
             "gpu_launches": wd.decode_steps}
 
 
+def run_headline_only(args, dev):
+    """Profiling aid: W + K calls of the headline prefill and nothing else."""
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_prefill(w, seed=0, device=dev)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    out = torch.empty((w.seq_len, w.heads, w.dv), dtype=w.torch_dtype, device=dev)
+    fin = torch.empty((1, w.heads, w.dk, w.dv), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        kda.chunk_fwd(*x, d["init_state"], None, chunk=w.chunk, out=out, final_state=fin)
+    torch.cuda.synchronize()
+
+
 def run_decode_only(args, dev):
     """Profiling aid: the decode kernel alone on N sequences x 96 heads."""
     import torch
@@ -641,7 +660,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-big-prefill", action="store_true",
                     help="skip the varlen and million-token prefill legs")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "headline"],
                     help="profiling aid: run one part only (no JSON line unless 'all')")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences (small ncu case)")
