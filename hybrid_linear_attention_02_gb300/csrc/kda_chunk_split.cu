@@ -424,7 +424,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
       facs[5 * kD + sc] = ex2_fast(R[3] - R[2]);
       reinterpret_cast<float*>(rec + kRecG)[cc] = ex2_fast(acc);
     }
-    // The previous item's T' store has read the T' rows before P4 rewrites them.
+    // The previous item's bulk stores have read their sources: the T' rows
+    // before P4 rewrites them, the staged -W before P2 rewrites Ktil.
     if (leader) bulk_wait_read_all();
     named_bar(2, kPThreads);
     KDA_SMARK(3);
@@ -755,26 +756,38 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_after();
     KDA_SMARK(12);
 
-    // ---- P7: -W (row = token, column = key channel) straight to the record,
-    // where its two 64-channel panels are rows 64..127 of the WQ panels (the
-    // same swizzled image a staged copy would have).  Warps 0, 1 take
-    // channels 0..63 and warps 4, 5 channels 64..127 of TMEM lanes 0..63.
-    if ((pw & 3) < 2 && ok_w) {
-      const int t = 32 * (pw & 3) + lane, q0 = 2 * (pw >> 2);
-      float w[2][32];
+    // ---- P7: -W (row = token, column = key channel) to the record, where
+    // its two 64-channel panels are rows 64..127 of the WQ panels.  Warps 0,
+    // 1 take channels 0..63 and warps 4, 5 channels 64..127 of TMEM lanes
+    // 0..63.  A lane holds one row, so the rows are staged in the Ktil tile
+    // (dead once W is done; the leader's read wait before the next item's P2
+    // orders its reuse) and leave as two 8 KB bulk copies, rather than as
+    // 16-byte stores that each touch a different 128-byte line.
+    if ((pw & 3) < 2) {
+      if (ok_w) {
+        const int t = 32 * (pw & 3) + lane, q0 = 2 * (pw >> 2);
+        float w[2][32];
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-        tmem_ld32(tbase + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + 32 * (q0 + j), w[j]);
-      tmem_ld_wait();
+        for (int j = 0; j < 2; ++j)
+          tmem_ld32(tbase + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + 32 * (q0 + j), w[j]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          float f8[8];
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float f8[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) f8[u] = -w[j][8 * q8 + u];
-          st_tile8(rec + kRecWQ, 64 + t, 32 * (q0 + j) + 8 * q8, 128, f8);
-        }
+            for (int u = 0; u < 8; ++u) f8[u] = -w[j][8 * q8 + u];
+            st_tile8(smem + kPOffKT, t, 32 * (q0 + j) + 8 * q8, 64, f8);
+          }
+        fence_async_smem();
+      }
+      named_bar(3, 128);   // the four -W warps, whatever the wait returned
+      if (leader && ok_w && !s_abort) {
+        bulk_store(rec + kRecWQ + 8192, smem + kPOffKT, 8192);
+        bulk_store(rec + kRecWQ + 16384 + 8192, smem + kPOffKT + 8192, 8192);
+        bulk_commit();
+      }
     }
     tc_fence_before();
     KDA_SMARK(13);
