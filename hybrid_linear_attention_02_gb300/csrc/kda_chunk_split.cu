@@ -247,6 +247,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
+  // The state pass may be scheduled on SMs this grid frees (its loads of
+  // the records wait for this grid's completion).
+  pdl_launch_dependents();
   const int p = threadIdx.x, pw = p >> 5, lane = p & 31;
   const int H = args.heads;
   window_prefix(args, win, s_cum);
@@ -933,6 +936,10 @@ __global__ void __launch_bounds__(kGate ? kSThreadsGated : kSThreads, 1)
     // ================================ producer ================================
     if (lane == 0) {
       prefetch_tmap(&tm_v);
+      // Launched as a programmatic dependent of the preparation grid: its
+      // records are complete and visible past this point.  Nothing else of
+      // this kernel reads what that grid writes.
+      pdl_wait();
       int last[2] = {-1, -1}, zlast[2] = {-1, -1};   // last chunk loaded into each slot
 #pragma unroll 1
       for (int c = 0; c < nck; ++c) {
@@ -1603,17 +1610,34 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       if ((e = cudaStreamWaitEvent(s_state, st->prep_done[w % kEvRing], 0)) != cudaSuccess)
         return e;
     }
-    dim3 grid_s(a.n_seqs, a.heads, a.trans_M ? 2 : 1);
-    if (a.trans_M)
-      chunk_state_kernel<false, true><<<grid_s, kSThreads, kSSmem, s_state>>>(
-          a, win, maps[2], maps[4], maps[5]);
-    else if (a.gate)
-      chunk_state_kernel<true, false><<<grid_s, kSThreadsGated, kSSmemGated, s_state>>>(
-          a, win, maps[2], maps[4], maps[5]);
-    else
-      chunk_state_kernel<false, false><<<grid_s, kSThreads, kSSmem, s_state>>>(
-          a, win, maps[2], maps[4], maps[5]);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // On the caller's stream the state pass is a programmatic dependent of
+    // the preparation just launched: its CTAs start on the SMs the
+    // preparation's tail frees and set up while it finishes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_seqs, a.heads, a.trans_M ? 2 : 1);
+    cfg.stream = s_state;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap || grid_p == 0 ? 0 : 1;
+    if (a.trans_M) {
+      cfg.blockDim = dim3(kSThreads);
+      cfg.dynamicSmemBytes = kSSmem;
+      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, true>, a, win, maps[2], maps[4],
+                             maps[5]);
+    } else if (a.gate) {
+      cfg.blockDim = dim3(kSThreadsGated);
+      cfg.dynamicSmemBytes = kSSmemGated;
+      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<true, false>, a, win, maps[2], maps[4],
+                             maps[5]);
+    } else {
+      cfg.blockDim = dim3(kSThreads);
+      cfg.dynamicSmemBytes = kSSmem;
+      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, false>, a, win, maps[2], maps[4],
+                             maps[5]);
+    }
+    if (e != cudaSuccess) return e;
     if (overlap && (e = cudaEventRecord(st->state_done[w % kEvRing], s_state)) != cudaSuccess)
       return e;
   }

@@ -342,6 +342,18 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the grid launched
+// after this one (with the programmatic-serialization attribute) be scheduled
+// once every CTA of this grid has executed it or exited; that grid's wait
+// returns when this grid has completed and its memory operations are visible.
+// Without such a dependency the wait returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Two fp32 values in one 64-bit register, for the packed f32x2 instructions.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
