@@ -251,6 +251,9 @@ def run_gpu(args):
     if args.only == "headline":
         run_headline_only(args, dev)
         return
+    if args.only == "prologue":
+        run_prologue_only(args, dev)
+        return
     # ---------------- prefill (headline) ----------------
     w = inputs.WORKLOADS[PREFILL]
     d = inputs.make_prefill(w, seed=rank, device=dev)
@@ -635,6 +638,22 @@ def run_headline_only(args, dev):
     torch.cuda.synchronize()
 
 
+def run_prologue_only(args, dev):
+    """Profiling aid: W + K calls of the input prologue on the headline's shape
+    (8192 tokens x 96 heads) and nothing else."""
+    import torch
+
+    import hybrid_linear_attention_02_gb300 as kda
+    from hybrid_linear_attention_02_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL]
+    px = inputs.make_prologue_inputs(w.seq_len, w.heads, w.dk, w.torch_dtype, seed=0,
+                                     device=dev)
+    pq, pk, pg = (torch.empty_like(px[0]) for _ in range(3))
+    for _ in range(args.warmup + args.steps):
+        kda.prologue(*px, None, q=pq, k=pk, g=pg)
+    torch.cuda.synchronize()
+
+
 def run_decode_only(args, dev):
     """Profiling aid: the decode kernel alone on N sequences x 96 heads."""
     import torch
@@ -660,7 +679,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-big-prefill", action="store_true",
                     help="skip the varlen and million-token prefill legs")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "headline"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "headline", "prologue"],
                     help="profiling aid: run one part only (no JSON line unless 'all')")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences (small ncu case)")

@@ -1466,7 +1466,8 @@ namespace {
 constexpr int kEvRing = 64;
 constexpr int kMaxDevices = 64;
 struct SplitStreams {
-  cudaStream_t state = nullptr;
+  cudaStream_t state = nullptr;   // highest priority: overlapped windows' state passes
+  cudaStream_t side = nullptr;    // lowest priority: a front-loaded call's second preparation
   cudaEvent_t fork = nullptr, join = nullptr;
   cudaEvent_t prep_done[kEvRing] = {}, state_done[kEvRing] = {};
   bool ready = false;
@@ -1482,7 +1483,8 @@ SplitStreams* split_streams(int dev) {
   if (st.ready) return &st;
   int least = 0, greatest = 0;
   if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
-  if (cudaStreamCreateWithPriority(&st.state, cudaStreamNonBlocking, greatest) != cudaSuccess)
+  if (cudaStreamCreateWithPriority(&st.state, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&st.side, cudaStreamNonBlocking, least) != cudaSuccess)
     return nullptr;
   bool ok = cudaEventCreateWithFlags(&st.fork, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&st.join, cudaEventDisableTiming) == cudaSuccess;
@@ -1564,18 +1566,117 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
     n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
     n_regions = 1;
   }
+  // Front-loaded form, for pairs that fit on the SMs in one wave but leave
+  // fewer than half of them free, when every record fits at once: a first
+  // window of most of the chunks is prepared on every SM (persistent CTAs);
+  // its state pass then runs beside the preparation of a short second
+  // window (short-lived CTAs) on the SMs it leaves free, and the second
+  // state pass ends the call.  The split balances the middle phase: a state
+  // pass takes about 0.22 of a preparation item's CTA time per chunk, and
+  // short-lived CTAs run at about 85 % of the persistent rate (both measured
+  // on these kernels), so tail / head = 0.374 (SMs - pairs) / pairs.
+  // KDA_SPLIT_TAIL=n sets the second window's chunks (0: off; a tuning knob).
+  long long head = 0;   // > 0: front-loaded windows [0, head) and [head, max_chunks)
+  size_t head_bytes = 0;
+  if (!overlap && !split_serial_only() && !a.trans_M && 2 * pairs > sms &&
+      8 * (sms - pairs) >= sms && max_chunks >= 16) {
+    const double r = 0.374 * static_cast<double>(sms - pairs) / static_cast<double>(pairs);
+    long long tail = static_cast<long long>(static_cast<double>(max_chunks) * r / (1.0 + r));
+    if (const char* ft = getenv("KDA_SPLIT_TAIL")) tail = atoll(ft);
+    if (tail >= 1 && tail < max_chunks) {
+      const long long h0 = max_chunks - tail;
+      const long long b0 = pairs * h0 < item_bound_all ? pairs * h0 : item_bound_all;
+      const long long b1 = pairs * tail < item_bound_all ? pairs * tail : item_bound_all;
+      if (b0 + b1 <= cap_items) {
+        head = h0;
+        head_bytes = static_cast<size_t>(b0) * kRecBytes;
+      }
+    }
+  }
 
   std::unique_lock<std::mutex> lock(g_split_mu, std::defer_lock);
   SplitStreams* st = nullptr;
   cudaStream_t s_state = stream;
-  if (overlap) {
+  if (overlap || head) {
     lock.lock();
     st = split_streams(dev);
     if (!st) return cudaErrorUnknown;
+  }
+  if (overlap) {
     s_state = st->state;
     if ((e = cudaEventRecord(st->fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(s_state, st->fork, 0)) != cudaSuccess) return e;
   }
+  // The state pass of one window on stream s; with pdl, as a programmatic
+  // dependent of the preparation just launched on s: its CTAs start on the
+  // SMs the preparation's tail frees and set up while it finishes.
+  auto launch_state = [&](const SplitWindow& win, cudaStream_t s, bool pdl) -> cudaError_t {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_seqs, a.heads, a.trans_M ? 2 : 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (a.trans_M) {
+      cfg.blockDim = dim3(kSThreads);
+      cfg.dynamicSmemBytes = kSSmem;
+      return cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, true>, a, win, maps[2], maps[4],
+                                maps[5]);
+    }
+    if (a.gate) {
+      cfg.blockDim = dim3(kSThreadsGated);
+      cfg.dynamicSmemBytes = kSSmemGated;
+      return cudaLaunchKernelEx(&cfg, chunk_state_kernel<true, false>, a, win, maps[2], maps[4],
+                                maps[5]);
+    }
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = kSSmem;
+    return cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, false>, a, win, maps[2], maps[4],
+                              maps[5]);
+  };
+  auto launch_prep = [&](const SplitWindow& win, long long grid, cudaStream_t s) -> cudaError_t {
+    if (grid <= 0) return cudaSuccess;
+    chunk_prep_kernel<<<static_cast<unsigned>(grid), kPThreads, kPSmem, s>>>(a, win, maps[0],
+                                                                              maps[1], maps[3]);
+    return cudaGetLastError();
+  };
+
+  if (head) {
+    // Front-loaded: prep(w0) and state(w0) on the caller's stream, the
+    // latter a programmatic dependent, so that its CTAs hold their SMs
+    // before anything else may be scheduled; prep(w1) on the lowest-priority
+    // side stream once prep(w0) is complete, on the SMs the state pass
+    // leaves; state(w1) on the caller's stream after both.
+    SplitWindow w0{}, w1{};
+    w0.rec = records;
+    w0.cw0 = 0;
+    w0.cw1 = static_cast<int>(head);
+    w0.first = true;
+    w0.s_run = run_state;
+    w1.rec = records + head_bytes;
+    w1.cw0 = static_cast<int>(head);
+    w1.cw1 = static_cast<int>(max_chunks);
+    w1.last = true;
+    w1.s_run = run_state;
+    w1.per_cta = kPrepItemsPerCta;
+    const long long items0 = pairs * head < item_bound_all ? pairs * head : item_bound_all;
+    long long items1 = pairs * (max_chunks - head);
+    if (items1 > item_bound_all) items1 = item_bound_all;
+    const long long grid0 = items0 < 2ll * sms ? items0 : 2ll * sms;
+    if ((e = launch_prep(w0, grid0, stream)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(st->prep_done[0], stream)) != cudaSuccess) return e;
+    if ((e = launch_state(w0, stream, grid0 > 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(st->side, st->prep_done[0], 0)) != cudaSuccess) return e;
+    if ((e = launch_prep(w1, (items1 + kPrepItemsPerCta - 1) / kPrepItemsPerCta, st->side)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(st->prep_done[1], st->side)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(stream, st->prep_done[1], 0)) != cudaSuccess) return e;
+    return launch_state(w1, stream, false);
+  }
+
   const size_t region_bytes = static_cast<size_t>(pairs * wc) * kRecBytes;
   for (long long w = 0; w < n_win || w == 0; ++w) {
     const long long cw0 = w * wc;
@@ -1600,44 +1701,13 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       win.per_cta = 0;
       grid_p = items < 2ll * sms ? items : 2ll * sms;
     }
-    if (grid_p > 0) {
-      chunk_prep_kernel<<<static_cast<unsigned>(grid_p), kPThreads, kPSmem, stream>>>(
-          a, win, maps[0], maps[1], maps[3]);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_prep(win, grid_p, stream)) != cudaSuccess) return e;
     if (overlap) {
       if ((e = cudaEventRecord(st->prep_done[w % kEvRing], stream)) != cudaSuccess) return e;
       if ((e = cudaStreamWaitEvent(s_state, st->prep_done[w % kEvRing], 0)) != cudaSuccess)
         return e;
     }
-    // On the caller's stream the state pass is a programmatic dependent of
-    // the preparation just launched: its CTAs start on the SMs the
-    // preparation's tail frees and set up while it finishes.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.n_seqs, a.heads, a.trans_M ? 2 : 1);
-    cfg.stream = s_state;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = overlap || grid_p == 0 ? 0 : 1;
-    if (a.trans_M) {
-      cfg.blockDim = dim3(kSThreads);
-      cfg.dynamicSmemBytes = kSSmem;
-      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, true>, a, win, maps[2], maps[4],
-                             maps[5]);
-    } else if (a.gate) {
-      cfg.blockDim = dim3(kSThreadsGated);
-      cfg.dynamicSmemBytes = kSSmemGated;
-      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<true, false>, a, win, maps[2], maps[4],
-                             maps[5]);
-    } else {
-      cfg.blockDim = dim3(kSThreads);
-      cfg.dynamicSmemBytes = kSSmem;
-      e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<false, false>, a, win, maps[2], maps[4],
-                             maps[5]);
-    }
-    if (e != cudaSuccess) return e;
+    if ((e = launch_state(win, s_state, !overlap && grid_p > 0)) != cudaSuccess) return e;
     if (overlap && (e = cudaEventRecord(st->state_done[w % kEvRing], s_state)) != cudaSuccess)
       return e;
   }

@@ -114,7 +114,12 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  * records fill at most 2 GiB when N x H <= 76 (windows of chunks then overlap
  * the state pass of one with the preparation of the next) and at most 16 GiB
  * otherwise; longer inputs run in windows with the state carried between
- * them.
+ * them.  When N x H fits the SMs in one wave but leaves fewer than half of
+ * them free and every record fits, the chunks run as two windows: the state
+ * pass of the first (most of the chunks) beside the preparation of the
+ * second on the SMs it leaves free.  The helper streams this uses are the
+ * library's own, joined to the caller's stream by events before the call
+ * returns.
  * A smaller workspace that still holds the order array, N x H fp32 states and
  * one record per pair runs the split form in more, smaller windows; below
  * that, and otherwise, one fused kernel per pair runs.  The

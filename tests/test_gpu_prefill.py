@@ -171,6 +171,29 @@ def test_split_overlapped_windows_match_serial(monkeypatch):
     assert_close(f1, rf, "bf16", "final_state")
 
 
+@pytest.mark.parametrize("tail", [None, "5"])
+def test_split_front_loaded_windows_match_serial(monkeypatch, tail):
+    """Pairs that fill more than half the SMs but fit in one wave run as two
+    windows: the first (most chunks) prepared on every SM, its state pass
+    beside the preparation of the short second one.  Results equal the
+    serial single window bit for bit.  One sequence spans both windows; the
+    other ends in the first and is carried through the second."""
+    monkeypatch.setenv("KDA_CHUNK_PATH", "split")
+    if tail is not None:
+        monkeypatch.setenv("KDA_SPLIT_TAIL", tail)
+    w = W["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=9, device=DEV, lengths=[5000, 100], heads=48)
+    o1, f1 = _run(d)
+    monkeypatch.setenv("KDA_SPLIT_SERIAL", "1")
+    o2, f2 = _run(d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    heads = [0, 17, 47]
+    ro, rf = _oracle(d, heads)
+    hs = torch.tensor(heads, device=DEV)
+    assert_close(o1[:, hs], ro, "bf16", "out")
+    assert_close(f1[:, hs], rf, "bf16", "final_state")
+
+
 def test_split_many_pairs_few_sequences_windows():
     """More than 304 sequence-head pairs from few sequences take the split form
     by default; with a workspace a few records per pair larger than the
