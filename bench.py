@@ -293,12 +293,15 @@ def run_gpu(args):
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
     algo = kda.algorithm(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk)
     tc = algo.startswith("tcgen05")
-    # The split path is two kernels per call (one window of chunks at this size).
-    kname, kfile, kprof, launches = {
+    kname, kfile, kprof = {
         "tcgen05_split": ("kda_chunk_split (chunk_prep_kernel + chunk_state_kernel)",
-                          "kda_chunk_split.cu", "chunk_split_prefill_T8192_H96.md", 2),
-        "tcgen05": ("kda_chunk_tc", "kda_chunk_tc.cu", "chunk_fwd_prefill_T8192_H96.md", 1),
-    }.get(algo, ("kda_recurrent", "kda_recurrent.cu", "chunk_fwd_prefill_T8192_H96.md", 1))
+                          "kda_chunk_split.cu", "chunk_split_prefill_T8192_H96.md"),
+        "tcgen05": ("kda_chunk_tc", "kda_chunk_tc.cu", "chunk_fwd_prefill_T8192_H96.md"),
+    }.get(algo, ("kda_recurrent", "kda_recurrent.cu", "chunk_fwd_prefill_T8192_H96.md"))
+    # Kernels per call, from the library's own window schedule (at this size
+    # the split form's two front-loaded windows: two preparations, two state
+    # passes).
+    launches = kda.launch_count(1, T, H, w.dk, w.dv, w.torch_dtype, w.chunk)
     traffic = kernel_traffic(kfile, kprof)
 
     # ---------------- e2e through the public API with host buffers ----------------

@@ -116,6 +116,8 @@ def _declare(lib):
     lib.kda_prologue.restype = ip
     lib.kda_chunk_fwd_algorithm.argtypes = [dp, ip]
     lib.kda_chunk_fwd_algorithm.restype = ip
+    lib.kda_chunk_fwd_launch_count.argtypes = [dp, ip, sz, ip]
+    lib.kda_chunk_fwd_launch_count.restype = ip
     lib.kda_debug_chunk_fwd_withhold.argtypes = [ip, vp, vp, vp, vp, vp, vp, vp, vp, dp, vp, sz,
                                                  vp, vp]
     lib.kda_debug_chunk_fwd_withhold.restype = ip
@@ -164,6 +166,22 @@ def algorithm(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=6
     if rc < 0:
         raise KDAError(rc, "kda_chunk_fwd_algorithm")
     return {0: "recurrent", 1: "tcgen05", 2: "tcgen05_split"}[rc]
+
+
+def launch_count(n_seqs, total_tokens, heads, dk, dv, dtype=torch.bfloat16, chunk=64,
+                 workspace_bytes=None, varlen=False) -> int:
+    """Kernels one kda_chunk_fwd call launches for these sizes (the workspace
+    ``workspace_size`` gives unless workspace_bytes is passed; varlen: with
+    cu_seqlens), on the current CUDA device."""
+    d = _dims(n_seqs, total_tokens, heads, dk, dv, dtype)
+    lib = load()
+    if workspace_bytes is None:
+        workspace_bytes = int(lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), int(chunk)))
+    rc = int(lib.kda_chunk_fwd_launch_count(ctypes.byref(d), int(chunk), int(workspace_bytes),
+                                            int(bool(varlen))))
+    if rc < 0:
+        raise KDAError(rc, "kda_chunk_fwd_launch_count")
+    return rc
 
 
 def checkpoint_offsets(lengths, interval: int) -> list:

@@ -141,6 +141,33 @@ size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk) {
   return b;
 }
 
+int kda_chunk_fwd_launch_count(const kda_dims* dims, int chunk, size_t workspace_bytes,
+                               int varlen) {
+  const int rc = check_dims(dims);
+  if (rc != KDA_OK) return rc;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+  const int N = dims->n_seqs;
+  if (N == 0 || dims->heads == 0) return 0;
+  const size_t need = order_bytes(N);
+  const int n_order = need > 0 && varlen ? 1 : 0;   // the length-order kernel
+  const size_t split_min = need + split_state_bytes(dims) +
+                           static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;
+  if (choose_path(dims, chunk) != Path::kSplit || workspace_bytes < split_min)
+    return n_order + 1;   // one fused or token-recurrence kernel
+  size_t rec_bytes = workspace_bytes - need - split_state_bytes(dims);
+  const size_t full = kda::split_record_bytes(N, dims->total_tokens, dims->heads);
+  if (rec_bytes > full) rec_bytes = full;
+  LaunchArgs a{};
+  a.n_seqs = N; a.heads = dims->heads; a.dk = dims->dk; a.dv = dims->dv;
+  a.dtype = dims->dtype; a.chunk = chunk; a.total_tokens = dims->total_tokens;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const int c = kda::split_launch_count(a, rec_bytes, sms);
+  return c < 0 ? KDA_ERR_WORKSPACE : n_order + c;
+}
+
 int kda_chunk_fwd_algorithm(const kda_dims* dims, int chunk) {
   const int rc = check_dims(dims);
   if (rc != KDA_OK) return rc;

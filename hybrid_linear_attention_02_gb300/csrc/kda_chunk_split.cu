@@ -1498,38 +1498,20 @@ SplitStreams* split_streams(int dev) {
 
 }  // namespace
 
-cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
-                               float* run_state, cudaStream_t stream) {
-  if (a.n_seqs == 0 || a.heads == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kPSmem));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel<false, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel<true, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSSmemGated));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_state_kernel<false, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
-  CUtensorMap maps[6] = {};
-  const int n_maps = a.gate ? 6 : 5;
-  if (a.total_tokens > 0) {
-    const void* bases[6] = {a.q, a.k, a.v, a.g, a.out, a.gate};
-    for (int i = 0; i < n_maps; ++i)
-      if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
-        return cudaErrorInvalidValue;
-  }
+// The window schedule of one call; no CUDA calls.  False when the record
+// buffer holds less than one record per pair.
+struct SplitPlan {
+  long long pairs = 0, cap_items = 0, max_chunks = 0, item_bound_all = 0;
+  long long wc = 0, n_win = 0, n_regions = 0;   // windows of wc chunks, n_regions record regions
+  bool overlap = false;                         // overlapped windows (helper stream)
+  long long head = 0;      // > 0: front-loaded windows [0, head) and [head, max_chunks)
+  size_t head_bytes = 0;   // records of the first front-loaded window
+};
+
+bool plan_split(const LaunchArgs& a, size_t record_bytes, int sms, SplitPlan* P) {
   const long long pairs = static_cast<long long>(a.n_seqs) * a.heads;
   const long long cap_items = static_cast<long long>(record_bytes / kRecBytes);
-  if (cap_items < pairs) return cudaErrorInvalidValue;
+  if (cap_items < pairs) return false;
   const long long max_chunks = (a.total_tokens + kC - 1) / kC;   // of any one sequence
   const long long item_bound_all =
       static_cast<long long>(a.heads) * (a.total_tokens / kC + a.n_seqs);
@@ -1576,7 +1558,7 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
   // short-lived CTAs run at about 85 % of the persistent rate (both measured
   // on these kernels), so tail / head = 0.374 (SMs - pairs) / pairs.
   // KDA_SPLIT_TAIL=n sets the second window's chunks (0: off; a tuning knob).
-  long long head = 0;   // > 0: front-loaded windows [0, head) and [head, max_chunks)
+  long long head = 0;
   size_t head_bytes = 0;
   if (!overlap && !split_serial_only() && !a.trans_M && 2 * pairs > sms &&
       8 * (sms - pairs) >= sms && max_chunks >= 16) {
@@ -1593,6 +1575,70 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
       }
     }
   }
+
+  P->pairs = pairs;
+  P->cap_items = cap_items;
+  P->max_chunks = max_chunks;
+  P->item_bound_all = item_bound_all;
+  P->wc = wc;
+  P->n_win = n_win;
+  P->n_regions = n_regions;
+  P->overlap = overlap;
+  P->head = head;
+  P->head_bytes = head_bytes;
+  return true;
+}
+
+int split_launch_count(const LaunchArgs& a, size_t record_bytes, int sms) {
+  SplitPlan P;
+  if (!plan_split(a, record_bytes, sms, &P)) return -1;
+  if (P.head) return 4;   // two preparations, two state passes
+  long long n = 0;
+  for (long long w = 0; w < P.n_win || w == 0; ++w) {
+    const long long cw0 = w * P.wc;
+    const long long cw1 = cw0 + P.wc < P.max_chunks ? cw0 + P.wc : P.max_chunks;
+    if (cw1 > cw0) ++n;   // the preparation (none for a window without chunks)
+    ++n;                  // the state pass
+  }
+  return static_cast<int>(n);
+}
+
+cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
+                               float* run_state, cudaStream_t stream) {
+  if (a.n_seqs == 0 || a.heads == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kPSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel<false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSSmemGated));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_state_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSSmem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  CUtensorMap maps[6] = {};
+  const int n_maps = a.gate ? 6 : 5;
+  if (a.total_tokens > 0) {
+    const void* bases[6] = {a.q, a.k, a.v, a.g, a.out, a.gate};
+    for (int i = 0; i < n_maps; ++i)
+      if (!make_token_map(&maps[i], bases[i], a.heads, a.total_tokens))
+        return cudaErrorInvalidValue;
+  }
+  SplitPlan P;
+  if (!plan_split(a, record_bytes, sms, &P)) return cudaErrorInvalidValue;
+  const long long pairs = P.pairs, max_chunks = P.max_chunks, item_bound_all = P.item_bound_all;
+  const long long wc = P.wc, n_win = P.n_win, n_regions = P.n_regions;
+  const bool overlap = P.overlap;
+  const long long head = P.head;
+  const size_t head_bytes = P.head_bytes;
 
   std::unique_lock<std::mutex> lock(g_split_mu, std::defer_lock);
   SplitStreams* st = nullptr;

@@ -138,6 +138,9 @@ struct SplitWindow {
 
 // Record-buffer bytes the split path needs for these sizes.
 size_t split_record_bytes(int n_seqs, long long total_tokens, int heads);
+// Kernels one launch_chunk_split call launches with this record buffer on a
+// device of sms SMs (-1 if the buffer holds less than one record per pair).
+int split_launch_count(const LaunchArgs& a, size_t record_bytes, int sms);
 cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t record_bytes,
                                float* run_state, cudaStream_t stream);
 

@@ -316,6 +316,19 @@ typedef enum {
 } kda_algo;
 
 /*
+ * Kernels one kda_chunk_fwd call launches on its stream for these dims, chunk
+ * size and workspace size, with cu_seqlens given (varlen != 0) or not, on the
+ * current device (the library's helper streams included): the length-order
+ * kernel, then the split form's preparation and state kernels per window, or
+ * one fused or token-recurrence kernel (N = 0 or H = 0: none).  A
+ * KDA_DEBUG_BOUNDS build adds its range check when given a dev_status.
+ * Returns the count (>= 0), or a negative kda_status for invalid dims or
+ * chunk, or KDA_ERR_CUDA if the device cannot be queried.
+ */
+KDA_API int kda_chunk_fwd_launch_count(const kda_dims* dims, int chunk, size_t workspace_bytes,
+                                       int varlen);
+
+/*
  * Which kernels kda_chunk_fwd runs for these dims and chunk size (given a
  * workspace of kda_chunk_fwd_workspace_size() bytes).  Returns a negative
  * kda_status for dims kda_chunk_fwd would reject.

@@ -229,6 +229,22 @@ def test_dispatch_boundaries(lib, monkeypatch):
     assert size(_dims(n=2, t=t, h=38)) == order(2) + states(2, 38) + cap(2)
 
 
+def test_launch_count_host_cases(lib):
+    """Kernels per kda_chunk_fwd call where no device query is needed: the
+    fused and token-recurrence paths launch one kernel, plus the length-order
+    kernel with cu_seqlens and more than one sequence."""
+    lc = lambda d, ws=0, varlen=0, c=64: lib.kda_chunk_fwd_launch_count(ctypes.byref(d), c, ws,
+                                                                        varlen)
+    fused = _dims(n=64, t=64 * 8192, h=96)                 # 6,144 pairs of 64 sequences
+    assert lib.kda_chunk_fwd_algorithm(ctypes.byref(fused), 64) == 1
+    assert lc(fused) == 1 and lc(fused, varlen=1) == 2
+    # Split by default, but a workspace below one record per pair: fused.
+    assert lc(_dims(n=1, t=8192, h=96), ws=1024) == 1
+    assert lc(_dims(n=1, t=256, h=1, dk=64, dv=64, dtype=0)) == 1   # token recurrence
+    assert lc(_dims(n=0, t=0, h=96)) == 0
+    assert lc(fused, c=48) == -2                           # KDA_ERR_UNSUPPORTED
+
+
 def test_path_override(lib, monkeypatch):
     d = _dims(n=1, t=8192, h=96)
     monkeypatch.setenv("KDA_CHUNK_PATH", "fused")

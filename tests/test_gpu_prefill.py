@@ -194,6 +194,26 @@ def test_split_front_loaded_windows_match_serial(monkeypatch, tail):
     assert_close(f1[:, hs], rf, "bf16", "final_state")
 
 
+def test_launch_count_follows_the_window_schedule(monkeypatch):
+    """kda_chunk_fwd_launch_count on the split form: front-loaded windows (two
+    preparations, two state passes), one serial window, overlapped windows
+    (a preparation and a state pass each)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    monkeypatch.delenv("KDA_SPLIT_SERIAL", raising=False)
+    monkeypatch.delenv("KDA_SPLIT_TAIL", raising=False)
+    H = sms * 5 // 8                                   # between half the SMs and all of them
+    assert kda.launch_count(1, 8192, H, 128, 128) == 4
+    monkeypatch.setenv("KDA_SPLIT_SERIAL", "1")
+    assert kda.launch_count(1, 8192, H, 128, 128) == 2
+    monkeypatch.delenv("KDA_SPLIT_SERIAL")
+    # Few pairs, 2^20 tokens: overlapped windows, a preparation and a state
+    # pass each; the same pairs and windows from two sequences add the
+    # length-order kernel.
+    c1 = kda.launch_count(1, 1 << 20, 32, 128, 128)
+    assert c1 >= 4 and c1 % 2 == 0
+    assert kda.launch_count(2, 1 << 20, 16, 128, 128, varlen=True) == c1 + 1
+
+
 def test_split_many_pairs_few_sequences_windows():
     """More than 304 sequence-head pairs from few sequences take the split form
     by default; with a workspace a few records per pair larger than the
