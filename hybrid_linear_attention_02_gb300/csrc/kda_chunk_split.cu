@@ -1550,19 +1550,18 @@ bool plan_split(const LaunchArgs& a, size_t record_bytes, int sms, SplitPlan* P)
   }
   // Front-loaded form, for pairs that fit on the SMs in one wave but leave
   // fewer than half of them free, when every record fits at once: a first
-  // window of most of the chunks is prepared on every SM (persistent CTAs);
-  // its state pass then runs beside the preparation of a short second
-  // window (short-lived CTAs) on the SMs it leaves free, and the second
-  // state pass ends the call.  The split balances the middle phase: a state
-  // pass takes about 0.22 of a preparation item's CTA time per chunk, and
-  // short-lived CTAs run at about 85 % of the persistent rate (both measured
-  // on these kernels), so tail / head = 0.374 (SMs - pairs) / pairs.
+  // window of most of the chunks is prepared on every SM; its state pass
+  // then runs beside the preparation of a short second window, two
+  // persistent CTAs on each SM it leaves free, and the second state pass
+  // ends the call.  The split balances the middle phase: a state-pass chunk
+  // takes about 0.22 of a preparation item's CTA time (measured on these
+  // kernels), so tail / head = 0.44 (SMs - pairs) / pairs.
   // KDA_SPLIT_TAIL=n sets the second window's chunks (0: off; a tuning knob).
   long long head = 0;
   size_t head_bytes = 0;
   if (!overlap && !split_serial_only() && !a.trans_M && 2 * pairs > sms &&
       8 * (sms - pairs) >= sms && max_chunks >= 16) {
-    const double r = 0.374 * static_cast<double>(sms - pairs) / static_cast<double>(pairs);
+    const double r = 0.44 * static_cast<double>(sms - pairs) / static_cast<double>(pairs);
     long long tail = static_cast<long long>(static_cast<double>(max_chunks) * r / (1.0 + r));
     if (const char* ft = getenv("KDA_SPLIT_TAIL")) tail = atoll(ft);
     if (tail >= 1 && tail < max_chunks) {
@@ -1691,9 +1690,10 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
 
   if (head) {
     // Front-loaded: prep(w0) and state(w0) on the caller's stream, the
-    // latter a programmatic dependent, so that its CTAs hold their SMs
-    // before anything else may be scheduled; prep(w1) on the lowest-priority
-    // side stream once prep(w0) is complete, on the SMs the state pass
+    // latter a programmatic dependent (launched once every prep(w0) CTA has
+    // started), so that its CTAs take the SMs prep(w0)'s tail frees before
+    // anything else may be scheduled; prep(w1) on the lowest-priority side
+    // stream once prep(w0) is complete, sized to the SMs the state pass
     // leaves; state(w1) on the caller's stream after both.
     SplitWindow w0{}, w1{};
     w0.rec = records;
@@ -1706,7 +1706,6 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
     w1.cw1 = static_cast<int>(max_chunks);
     w1.last = true;
     w1.s_run = run_state;
-    w1.per_cta = kPrepItemsPerCta;
     const long long items0 = pairs * head < item_bound_all ? pairs * head : item_bound_all;
     long long items1 = pairs * (max_chunks - head);
     if (items1 > item_bound_all) items1 = item_bound_all;
@@ -1715,9 +1714,8 @@ cudaError_t launch_chunk_split(const LaunchArgs& a, uint8_t* records, size_t rec
     if ((e = cudaEventRecord(st->prep_done[0], stream)) != cudaSuccess) return e;
     if ((e = launch_state(w0, stream, grid0 > 0)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(st->side, st->prep_done[0], 0)) != cudaSuccess) return e;
-    if ((e = launch_prep(w1, (items1 + kPrepItemsPerCta - 1) / kPrepItemsPerCta, st->side)) !=
-        cudaSuccess)
-      return e;
+    const long long free2 = 2ll * (sms - pairs);   // two CTAs on each SM the state pass leaves
+    if ((e = launch_prep(w1, items1 < free2 ? items1 : free2, st->side)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(st->prep_done[1], st->side)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(stream, st->prep_done[1], 0)) != cudaSuccess) return e;
     return launch_state(w1, stream, false);
