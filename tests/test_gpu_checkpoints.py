@@ -89,3 +89,33 @@ def test_checkpoints_resume_matches_uninterrupted_prefill():
     torch.cuda.synchronize()
     assert_close(out2, out[512:], "bf16", "resumed out")
     assert_close(fin2, fin, "bf16", "resumed final_state")
+
+
+def test_checkpoints_front_loaded_windows_match_serial(monkeypatch):
+    """96 sequence-head pairs run as front-loaded windows on the split form;
+    the checkpoints, outputs and final states equal those of one serial
+    window bit for bit, and the oracle's on three heads.  The first sequence
+    spans both windows, so the second window's checkpoints continue the
+    state the first one carried over."""
+    monkeypatch.setenv("KDA_CHUNK_PATH", "split")
+    w = inputs.WORKLOADS["prefill_T8192_H96_d128_bf16"]
+    d = inputs.make_prefill(w, seed=25, device=DEV, lengths=[5000, 100], heads=48)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+
+    def run():
+        r = kda.chunk_fwd(*x, d["init_state"], d["cu_seqlens"], chunk=64, ckpt_interval=128)
+        torch.cuda.synchronize()
+        return r
+
+    a = run()
+    monkeypatch.setenv("KDA_SPLIT_SERIAL", "1")
+    b = run()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    heads = [0, 31, 47]
+    hs = torch.tensor(heads, device=DEV)
+    ro, rf, rck = oracle.prefill(*[t[:, hs] for t in x], d["init_state"][:, hs],
+                                 d["cu_seqlens"], ckpt_interval=128)
+    assert_close(a[0][:, hs], ro, "bf16", "out")
+    assert_close(a[1][:, hs], rf, "bf16", "final_state")
+    assert_close(a[2][:, hs], rck, "bf16", "checkpoints")

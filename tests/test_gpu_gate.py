@@ -61,6 +61,24 @@ def test_gated_prefill_full_size():
     _check(d, "bf16")
 
 
+def test_gated_front_loaded_windows_match_serial(monkeypatch):
+    """96 sequence-head pairs run as front-loaded windows on the split form;
+    the gated state pass gives the serial single window's results bit for bit
+    (the gate tiles of the second window's chunks included)."""
+    monkeypatch.setenv("KDA_CHUNK_PATH", "split")
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=34, device=DEV,
+                            lengths=[5000, 100], heads=48)
+    T, H, dv = d["v"].shape
+    gate = inputs.make_output_gate(T, H, dv, d["v"].dtype, seed=4, device=DEV)
+    x = [d[n] for n in ("q", "k", "v", "g", "beta")]
+    run = lambda: kda.chunk_fwd(*x, d["init_state"], d["cu_seqlens"], chunk=64, gate=gate)
+    o1, f1 = run()
+    monkeypatch.setenv("KDA_SPLIT_SERIAL", "1")
+    o2, f2 = run()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
 def test_gated_decode_chain():
     wd = W["decode_256seq_H96_d128_64steps"]
     N, H = 8, 4
