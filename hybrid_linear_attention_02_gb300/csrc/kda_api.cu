@@ -149,6 +149,7 @@ int kda_chunk_fwd_launch_count(const kda_dims* dims, int chunk, size_t workspace
   const int N = dims->n_seqs;
   if (N == 0 || dims->heads == 0) return 0;
   const size_t need = order_bytes(N);
+  if (need > 0 && varlen && workspace_bytes < need) return KDA_ERR_WORKSPACE;   // as the call
   const int n_order = need > 0 && varlen ? 1 : 0;   // the length-order kernel
   const size_t split_min = need + split_state_bytes(dims) +
                            static_cast<size_t>(N) * dims->heads * kda::kSplitRecordBytes;

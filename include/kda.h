@@ -322,8 +322,10 @@ typedef enum {
  * kernel, then the split form's preparation and state kernels per window, or
  * one fused or token-recurrence kernel (N = 0 or H = 0: none).  A
  * KDA_DEBUG_BOUNDS build adds its range check when given a dev_status.
- * Returns the count (>= 0), or a negative kda_status for invalid dims or
- * chunk, or KDA_ERR_CUDA if the device cannot be queried.
+ * Returns the count (>= 0); a negative kda_status for invalid dims or chunk,
+ * KDA_ERR_WORKSPACE where the call itself would fail for want of workspace
+ * (packed sequences without room for the order array), or KDA_ERR_CUDA if
+ * the device cannot be queried.
  */
 KDA_API int kda_chunk_fwd_launch_count(const kda_dims* dims, int chunk, size_t workspace_bytes,
                                        int varlen);

@@ -237,7 +237,8 @@ def test_launch_count_host_cases(lib):
                                                                         varlen)
     fused = _dims(n=64, t=64 * 8192, h=96)                 # 6,144 pairs of 64 sequences
     assert lib.kda_chunk_fwd_algorithm(ctypes.byref(fused), 64) == 1
-    assert lc(fused) == 1 and lc(fused, varlen=1) == 2
+    assert lc(fused, ws=1 << 20) == 1 and lc(fused, ws=1 << 20, varlen=1) == 2
+    assert lc(fused, ws=0, varlen=1) == -6                 # KDA_ERR_WORKSPACE, as the call
     # Split by default, but a workspace below one record per pair: fused.
     assert lc(_dims(n=1, t=8192, h=96), ws=1024) == 1
     assert lc(_dims(n=1, t=256, h=1, dk=64, dv=64, dtype=0)) == 1   # token recurrence
