@@ -1544,8 +1544,16 @@ bool plan_split(const LaunchArgs& a, size_t record_bytes, int sms, SplitPlan* P)
   }
   if (split_serial_only() || a.trans_M) overlap = false;
   if (!overlap) {
-    wc = cap_items / pairs;
-    n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
+    if (cap_items >= item_bound_all) {
+      // Every record of the call fits: one window over every chunk index
+      // (max_chunks bounds each sequence by the total, so cap_items / pairs
+      // would cut packed sequences into windows most of which hold nothing).
+      wc = max_chunks > 0 ? max_chunks : 1;
+      n_win = 1;
+    } else {
+      wc = cap_items / pairs;
+      n_win = max_chunks > 0 ? (max_chunks + wc - 1) / wc : 1;
+    }
     n_regions = 1;
   }
   // Front-loaded form, for pairs that fit on the SMs in one wave but leave

@@ -126,7 +126,7 @@ constexpr size_t kSplitRecordBytes = 66048;      // one chunk record
 // run one after another and fewer of them is better.
 constexpr long long kSplitOverlapPairs = 76;
 constexpr size_t kSplitRecordBudgetOverlap = 2ull << 30;
-constexpr size_t kSplitRecordBudget = 16ull << 30;
+constexpr size_t kSplitRecordBudget = 32ull << 30;
 
 struct SplitWindow {
   uint8_t* rec;

@@ -112,7 +112,7 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_dims* dims, int chunk);
  * preparation kernel over every chunk at once, which writes a 66,048-byte
  * record per chunk into the workspace, then a state kernel per pair.  The
  * records fill at most 2 GiB when N x H <= 76 (windows of chunks then overlap
- * the state pass of one with the preparation of the next) and at most 16 GiB
+ * the state pass of one with the preparation of the next) and at most 32 GiB
  * otherwise; longer inputs run in windows with the state carried between
  * them.  When N x H fits the SMs in one wave but leaves fewer than half of
  * them free and every record fits, the chunks run as two windows: the state

@@ -189,10 +189,11 @@ def test_workspace_size(lib):
     # overlapped windows), the rest runs in windows.
     d = _dims(n=1, t=1 << 20, h=32)
     assert size(d) == 32 * 128 * 128 * 4 + ((2 << 30) // REC) * REC
-    # Many pairs from few sequences: still split, records capped at 16 GiB.
+    # Many pairs from few sequences: still split; all 408,000 records (26.9 GB)
+    # fit under the 32 GiB cap, so the call runs in one window.
     d = _dims(n=32, t=270000, h=96)
     assert algo(d) == 2
-    assert size(d) == 256 + 32 * 96 * 128 * 128 * 4 + ((16 << 30) // REC) * REC
+    assert size(d) == 256 + 32 * 96 * 128 * 128 * 4 + 96 * (270000 // 64 + 32) * REC
     # Many pairs from many sequences: one fused kernel per pair, order array only.
     d = _dims(n=64, t=270000, h=96)
     assert algo(d) == 1 and size(d) == 256
@@ -210,7 +211,7 @@ def test_dispatch_boundaries(lib, monkeypatch):
     """The split form serves up to 304 sequence-head pairs, or any pair count
     from at most 32 sequences, and never more than 1024 sequences; its record
     buffer is capped at 2 GiB up to 76 pairs (overlapped windows) and at
-    16 GiB above."""
+    32 GiB above."""
     monkeypatch.delenv("KDA_CHUNK_PATH", raising=False)
     algo = lambda d: lib.kda_chunk_fwd_algorithm(ctypes.byref(d), 64)
     size = lambda d: lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), 64)
@@ -225,7 +226,7 @@ def test_dispatch_boundaries(lib, monkeypatch):
     cap = lambda gib: ((gib << 30) // REC) * REC
     t = 1 << 20
     assert size(_dims(n=1, t=t, h=76)) == states(1, 76) + cap(2)
-    assert size(_dims(n=1, t=t, h=77)) == states(1, 77) + cap(16)
+    assert size(_dims(n=1, t=t, h=77)) == states(1, 77) + cap(32)
     assert size(_dims(n=2, t=t, h=38)) == order(2) + states(2, 38) + cap(2)
 
 
