@@ -138,6 +138,24 @@ struct SplitWindow {
 
 // Record-buffer bytes the split path needs for these sizes.
 size_t split_record_bytes(int n_seqs, long long total_tokens, int heads);
+constexpr int kSplitChunk = 64;                   // the split form's chunk length
+constexpr long long kSplitMinWindowChunks = 64;   // overlapped windows: at least this many chunks
+constexpr int kSplitEvRing = 64;                  // overlapped windows: events per device
+
+// The window schedule of one split-form call (kda_split_plan.cu; no CUDA
+// calls): plan_split fills it, false when the record buffer holds less than
+// one record per pair.
+struct SplitPlan {
+  long long pairs = 0, cap_items = 0, max_chunks = 0, item_bound_all = 0;
+  long long wc = 0, n_win = 0, n_regions = 0;   // windows of wc chunks, n_regions record regions
+  bool overlap = false;                         // overlapped windows (helper stream)
+  long long head = 0;      // > 0: front-loaded windows [0, head) and [head, max_chunks)
+  size_t head_bytes = 0;   // records of the first front-loaded window
+};
+bool plan_split(const LaunchArgs& a, size_t record_bytes, int sms, SplitPlan* P);
+// KDA_SPLIT_SERIAL=1: the split form's windows run one after another on the
+// caller's stream (no helper stream).
+bool split_serial_only();
 // Kernels one launch_chunk_split call launches with this record buffer on a
 // device of sms SMs (-1 if the buffer holds less than one record per pair).
 int split_launch_count(const LaunchArgs& a, size_t record_bytes, int sms);
