@@ -85,7 +85,7 @@ def tensor_block(T, H, kern_ms, hbm_peak):
             "peak_source": src, "unit": "TFLOP/s", "frac": achieved / peak,
             "flop_per_token_head": PREFILL_FLOP_PER_TOKEN_HEAD,
             "ceiling_frac_at_hbm_peak": per_byte * hbm_peak / 1e3 / peak,
-            "north_star_goal_frac": 0.5}
+            "goal_frac": 0.5}
 
 
 def decode_bytes(N, H, dk, dv, elt=2):
