@@ -214,6 +214,37 @@ def test_launch_count_follows_the_window_schedule(monkeypatch):
     assert kda.launch_count(2, 1 << 20, 16, 128, 128, varlen=True) == c1 + 1
 
 
+@pytest.mark.parametrize("lengths,heads", [([8192], 96), ([4096], 8), ([3000, 700], 8)])
+def test_launch_count_matches_the_kernels_launched(lengths, heads, monkeypatch):
+    """kda.launch_count (the figure bench.py reports as gpu_launches) equals
+    the library kernels one kda_chunk_fwd call launches, counted by the
+    PyTorch profiler's device activity: front-loaded windows (96 heads), one
+    serial window (8 heads), and packed sequences (the length-order kernel
+    too)."""
+    from torch.profiler import ProfilerActivity, profile
+    monkeypatch.delenv("KDA_SPLIT_SERIAL", raising=False)
+    monkeypatch.delenv("KDA_CHUNK_PATH", raising=False)
+    d = inputs.make_prefill(W["prefill_T8192_H96_d128_bf16"], seed=11, device=DEV,
+                            lengths=lengths, heads=heads)
+    N, T = len(lengths), sum(lengths)
+    cu = d["cu_seqlens"] if N > 1 else None
+    run = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], cu,
+                                chunk=64, n_seqs=N)
+    run()
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]):   # the profiler's first session may
+        torch.ones(1, device=DEV).add_(1)              # miss kernels: warm it up
+        torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        run()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if "kda::" in e.name or "chunk_" in e.name
+             or "order_kernel" in e.name]
+    if not names:
+        pytest.skip("the profiler recorded no device kernels here")
+    assert len(names) == kda.launch_count(N, T, heads, 128, 128, varlen=N > 1), names
+
+
 def test_split_many_pairs_few_sequences_windows():
     """More than 304 sequence-head pairs from few sequences take the split form
     by default; with a workspace a few records per pair larger than the
